@@ -1,0 +1,174 @@
+"""fp64 CPU oracle for the fused decoder operators -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path never calls it.
+
+It wraps ``oracle.c`` (plain single-threaded fp64 C, one loop per step of
+each operator's definition) with ctypes.  Inputs are numpy arrays in their
+storage type (float64, float32, or bfloat16 as uint16 bits) and are read by
+the C code exactly as stored; results come back as float64 arrays.
+
+Parity pins: see tests/test_oracle_pins.py.  Every function here is pinned by
+closed forms, invariants, hand-worked values and central finite differences.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+_DT = {np.dtype(np.float64): 0, np.dtype(np.float32): 1, np.dtype(np.uint16): 2}
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+_D = ctypes.c_double
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc -O2, ISO C11: no FMA contraction)."""
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= newest:
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.orc_rmsnorm_fwd.argtypes = [_P, _P, ctypes.c_int, _I, _I, _D, _P, _P]
+            lib.orc_rmsnorm_bwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _I, _D, _P, _P]
+            lib.orc_rope.argtypes = [_P, ctypes.c_int, _P, _I, _I, _I, _I, _D, ctypes.c_int, _P]
+            lib.orc_swiglu_fwd.argtypes = [_P, _P, ctypes.c_int, _I, _P]
+            lib.orc_swiglu_bwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _P, _P]
+            lib.orc_linear_ce.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
+                                          _P, _P, _P, _P]
+            lib.orc_linear_ce_rows.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
+                                               _P, _I, _P, _P, _P]
+            for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_rope", "orc_swiglu_fwd", "orc_swiglu_bwd",
+                      "orc_linear_ce", "orc_linear_ce_rows"):
+                getattr(lib, f).restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _c(a):
+    a = np.ascontiguousarray(a)
+    return a, a.ctypes.data
+
+
+def _dt(*arrs):
+    dts = {a.dtype for a in arrs}
+    if len(dts) != 1:
+        raise TypeError(f"mixed input dtypes {dts}")
+    return _DT[arrs[0].dtype]
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"{what}: oracle status {rc}")
+
+
+def rmsnorm_fwd(x, w, eps):
+    x, px = _c(x); w, pw = _c(w)
+    rows, cols = x.shape[0] if x.ndim > 1 else 1, x.shape[-1]
+    rows = x.size // cols
+    y = np.empty(x.shape, np.float64); rstd = np.empty((rows,), np.float64)
+    _check(_load().orc_rmsnorm_fwd(px, pw, _dt(x, w), rows, cols, eps, y.ctypes.data, rstd.ctypes.data),
+           "rmsnorm_fwd")
+    return y, rstd
+
+
+def rmsnorm_bwd(dy, x, w, eps):
+    dy, pdy = _c(dy); x, px = _c(x); w, pw = _c(w)
+    cols = x.shape[-1]; rows = x.size // cols
+    dx = np.empty(x.shape, np.float64); dw = np.empty((cols,), np.float64)
+    _check(_load().orc_rmsnorm_bwd(pdy, px, pw, _dt(dy, x, w), rows, cols, eps, dx.ctypes.data, dw.ctypes.data),
+           "rmsnorm_bwd")
+    return dx, dw
+
+
+def rope(t, theta, sign=1, pos=None):
+    """t [B, S, NH, D]; pos [B, S] int32 or None (p = s)."""
+    t, pt = _c(t)
+    B, S, NH, D = t.shape
+    ppos = None
+    if pos is not None:
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        assert pos.shape == (B, S)
+        ppos = pos.ctypes.data
+    out = np.empty(t.shape, np.float64)
+    _check(_load().orc_rope(pt, _dt(t), ppos, B, S, NH, D, theta, int(sign), out.ctypes.data), "rope")
+    return out
+
+
+def swiglu_fwd(g, u):
+    g, pg = _c(g); u, pu = _c(u)
+    y = np.empty(g.shape, np.float64)
+    _check(_load().orc_swiglu_fwd(pg, pu, _dt(g, u), g.size, y.ctypes.data), "swiglu_fwd")
+    return y
+
+
+def swiglu_bwd(dy, g, u):
+    dy, pdy = _c(dy); g, pg = _c(g); u, pu = _c(u)
+    dg = np.empty(g.shape, np.float64); du = np.empty(g.shape, np.float64)
+    _check(_load().orc_swiglu_bwd(pdy, pg, pu, _dt(dy, g, u), g.size, dg.ctypes.data, du.ctypes.data),
+           "swiglu_bwd")
+    return dg, du
+
+
+def linear_ce(X, W, labels, ignore_index=-100, reduction="mean", grad_scale=1.0, want_grads=True):
+    """Returns dict(loss, lse[T], dX[T,H], dW[V,H]) in float64."""
+    X, pX = _c(X); W, pW = _c(W)
+    labels = np.ascontiguousarray(labels, dtype=np.int64)
+    T, H = X.shape; V = W.shape[0]
+    assert W.shape[1] == H and labels.shape == (T,)
+    loss = np.zeros((1,), np.float64); lse = np.empty((T,), np.float64)
+    dX = np.empty((T, H), np.float64) if want_grads else None
+    dW = np.empty((V, H), np.float64) if want_grads else None
+    rc = _load().orc_linear_ce(pX, pW, _dt(X, W), labels.ctypes.data, T, H, V, int(ignore_index),
+                               0 if reduction == "mean" else 1, float(grad_scale), loss.ctypes.data,
+                               lse.ctypes.data, dX.ctypes.data if want_grads else None,
+                               dW.ctypes.data if want_grads else None)
+    _check(rc, "linear_ce")
+    return {"loss": float(loss[0]), "lse": lse, "dX": dX, "dW": dW}
+
+
+def linear_ce_rows(X, W, labels, rows, ignore_index=-100, reduction="mean", grad_scale=1.0):
+    """The definition on selected rows: dict(lse[k], loss_term[k], dX[k, H])."""
+    X, pX = _c(X); W, pW = _c(W)
+    labels = np.ascontiguousarray(labels, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    T, H = X.shape; V = W.shape[0]
+    k = rows.size
+    lse = np.empty((k,), np.float64); lt = np.empty((k,), np.float64); dX = np.empty((k, H), np.float64)
+    rc = _load().orc_linear_ce_rows(pX, pW, _dt(X, W), labels.ctypes.data, T, H, V, int(ignore_index),
+                                    0 if reduction == "mean" else 1, float(grad_scale), rows.ctypes.data, k,
+                                    lse.ctypes.data, lt.ctypes.data, dX.ctypes.data)
+    _check(rc, "linear_ce_rows")
+    return {"lse": lse, "loss_term": lt, "dX": dX}
+
+
+def rel_err(got, ref):
+    """max_i |g_i - o_i| / max(|o_i|, rms(o)) over one tensor (float64)."""
+    got = np.asarray(got, np.float64).ravel(); ref = np.asarray(ref, np.float64).ravel()
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    den = np.maximum(np.abs(ref), rms)
+    den = np.where(den > 0, den, 1.0)
+    return float(np.max(np.abs(got - ref) / den))

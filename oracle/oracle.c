@@ -1,0 +1,280 @@
+/*
+ * fp64 CPU oracle for the fused decoder operators -- TEST INFRASTRUCTURE.
+ *
+ * Only tests, the package smoke check and the benchmark's CPU baseline use
+ * this file.  It is the plain definition of each operator, in double
+ * precision, one loop per step of the definition, single-threaded, with no
+ * blocking, fusion or reordering.  It shares no code with the CUDA path.
+ *
+ * Sources (the web pages on Liger-Kernel that describe the method):
+ *  [P1] "Liger-Kernel核心技术：RollingBuffer与融合算子详解"
+ *       (Liger-Kernel core techniques: RollingBuffer and fused operators)
+ *  [P2] "Liger-Kernel内核级优化：FlashAttention与RollingBuffer详解"
+ *  [P3] "Liger-Kernel底层优化：新一代内核级推理加速引擎介绍"
+ *  [P4] "Liger-Kernel加持！ms-swift推理延迟降低至毫秒级"
+ * Where the pages leave a step open, the textbook definition of the named
+ * operator is taken; each such reading is marked READING.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* exact widening of one stored element to double */
+static double ld(const void* p, int dt, int64_t i) {
+    if (dt == ORC_F64) return ((const double*)p)[i];
+    if (dt == ORC_F32) return (double)((const float*)p)[i];
+    uint32_t u = ((uint32_t)((const uint16_t*)p)[i]) << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+static void widen(const void* p, int dt, int64_t off, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = ld(p, dt, off + i);
+}
+
+static int bad_dt(int dt) { return dt < ORC_F64 || dt > ORC_BF16; }
+
+/* ---------------------------------------------------------------- RMSNorm
+ * [P3] section "融合内核是如何工作的？来看一段简化版实现" (how the fused kernel
+ * works), the RMSNorm step of the fused RMSNorm + QKV + RoPE kernel: the sum
+ * of squares of the row, divided by the hidden size, plus epsilon, under an
+ * inverse square root, multiplies the element and the per-feature weight.
+ * The epsilon is a parameter here (the listing fixes 1e-6). */
+int orc_rmsnorm_fwd(const void* x, const void* w, int dt, int64_t rows, int64_t cols, double eps,
+                    double* y, double* rstd) {
+    if (!x || !w || !y || rows < 0 || cols <= 0 || bad_dt(dt)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double sum_sq = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double v = ld(x, dt, r * cols + j);
+            sum_sq += v * v;
+        }
+        double inv_rms = 1.0 / sqrt(sum_sq / (double)cols + eps);
+        if (rstd) rstd[r] = inv_rms;
+        for (int64_t j = 0; j < cols; ++j) y[r * cols + j] = ld(x, dt, r * cols + j) * inv_rms * ld(w, dt, j);
+    }
+    return 0;
+}
+
+/* READING: the pages give no backward.  It is the derivative of the forward
+ * above: with g = dy * w and r = 1/sqrt(mean(x^2)+eps), dr/dx_k = -r^3 x_k / H,
+ *     dx_k = r g_k - (r^3 / H) x_k sum_j g_j x_j,
+ *     dw_j = sum over rows of dy_j x_j r. */
+int orc_rmsnorm_bwd(const void* dy, const void* x, const void* w, int dt, int64_t rows, int64_t cols,
+                    double eps, double* dx, double* dw) {
+    if (!dy || !x || !w || !dx || !dw || rows < 0 || cols <= 0 || bad_dt(dt)) return -1;
+    for (int64_t j = 0; j < cols; ++j) dw[j] = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        double sum_sq = 0.0;
+        for (int64_t j = 0; j < cols; ++j) {
+            double v = ld(x, dt, r * cols + j);
+            sum_sq += v * v;
+        }
+        double rr = 1.0 / sqrt(sum_sq / (double)cols + eps);
+        double gx = 0.0;
+        for (int64_t j = 0; j < cols; ++j)
+            gx += ld(dy, dt, r * cols + j) * ld(w, dt, j) * ld(x, dt, r * cols + j);
+        for (int64_t j = 0; j < cols; ++j) {
+            double xj = ld(x, dt, r * cols + j), dyj = ld(dy, dt, r * cols + j);
+            double gj = dyj * ld(w, dt, j);
+            dx[r * cols + j] = rr * gj - (rr * rr * rr / (double)cols) * xj * gx;
+            dw[j] += dyj * xj * rr;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------- RoPE
+ * [P1] section "算子融合" (operator fusion), FusedRoPE paragraph: the rotation
+ * angle of each feature pair comes from the token position, generated from
+ * the thread index with no stored table.  [P3] fused-kernel listing, RoPE
+ * step: feature f is paired by f mod (head_dim/2), i.e. the pairs are
+ * (i, i + D/2), the two halves acting as real and imaginary parts.
+ * READING: the pages give no frequency schedule; the standard one is taken,
+ * phi(p, i) = p * theta^(-2i/D).  The listing's rotation mixes k with v and
+ * has no position term; it is read only for the pairing.
+ * Forward rotates by +phi, backward (the transpose of an orthogonal map) by
+ * -phi. */
+int orc_rope(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S, int64_t NH, int64_t D,
+             double theta, int sign, double* out) {
+    if (!t || !out || B < 0 || S < 0 || NH < 0 || D <= 0 || (D % 2) || bad_dt(dt) || theta <= 0.0) return -1;
+    if (sign != 1 && sign != -1) return -1;
+    const int64_t half = D / 2;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t s = 0; s < S; ++s) {
+            double p = pos ? (double)pos[b * S + s] : (double)s;
+            for (int64_t h = 0; h < NH; ++h) {
+                int64_t base = ((b * S + s) * NH + h) * D;
+                for (int64_t i = 0; i < half; ++i) {
+                    double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
+                    double phi = (double)sign * p * inv_freq;
+                    double c = cos(phi), sn = sin(phi);
+                    double a = ld(t, dt, base + i), bb = ld(t, dt, base + i + half);
+                    out[base + i] = a * c - bb * sn;
+                    out[base + i + half] = bb * c + a * sn;
+                }
+            }
+        }
+    return 0;
+}
+
+/* ----------------------------------------------------------------- SwiGLU
+ * [P1] section "算子融合", FusedLinearSwiGLU paragraph: the SiLU activation of
+ * the gate branch times the up branch, elementwise.  silu(g) = g * sigmoid(g).
+ * READING: the backward is the textbook derivative,
+ *     du = dy * silu(g),  dg = dy * u * s * (1 + g (1 - s)),  s = sigmoid(g). */
+static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+
+int orc_swiglu_fwd(const void* g, const void* u, int dt, int64_t n, double* y) {
+    if (!g || !u || !y || n < 0 || bad_dt(dt)) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        double gi = ld(g, dt, i);
+        y[i] = gi * sigmoid(gi) * ld(u, dt, i);
+    }
+    return 0;
+}
+
+int orc_swiglu_bwd(const void* dy, const void* g, const void* u, int dt, int64_t n, double* dg, double* du) {
+    if (!dy || !g || !u || !dg || !du || n < 0 || bad_dt(dt)) return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        double gi = ld(g, dt, i), ui = ld(u, dt, i), dyi = ld(dy, dt, i);
+        double s = sigmoid(gi);
+        du[i] = dyi * gi * s;
+        dg[i] = dyi * ui * s * (1.0 + gi * (1.0 - s));
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------- linear + CE
+ * [P1] section "算子融合", FusedCrossEntropyLoss paragraph: softmax and the
+ * negative log-likelihood are one step taken straight on the classifier-head
+ * output, the softmax never being stored.  READING: the classifier head is
+ * the linear map z = W x (no bias); the loss of a row is lse(z) - z[label];
+ * rows whose label is ignore_index contribute nothing; the mean divides by
+ * the count of the other rows (0 when there are none: loss and gradients 0).
+ * This is the unchunked definition: one whole row of logits at a time, its
+ * maximum, then lse = m + log sum exp(z - m).  No online merge. */
+static int64_t count_valid(const int64_t* labels, int64_t T, int64_t V, int64_t ignore_index, int* bad) {
+    int64_t n = 0;
+    *bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        if (labels[t] == ignore_index) continue;
+        if (labels[t] < 0 || labels[t] >= V) *bad = 1;
+        ++n;
+    }
+    return n;
+}
+
+/* logits of row t into z[V], returns lse */
+static double row_logits(const double* xt, const void* W, int dt, int64_t H, int64_t V, double* z,
+                         double* wrow) {
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        widen(W, dt, v * H, H, wrow);
+        double acc = 0.0;
+        for (int64_t h = 0; h < H; ++h) acc += xt[h] * wrow[h];
+        z[v] = acc;
+        if (acc > m) m = acc;
+    }
+    double se = 0.0;
+    for (int64_t v = 0; v < V; ++v) se += exp(z[v] - m);
+    return m + log(se);
+}
+
+int orc_linear_ce(const void* X, const void* W, int dt, const int64_t* labels, int64_t T, int64_t H,
+                  int64_t V, int64_t ignore_index, int reduction, double grad_scale, double* loss,
+                  double* lse, double* dX, double* dW) {
+    if (!X || !W || !labels || T < 0 || H <= 0 || V <= 0 || bad_dt(dt) || (reduction != 0 && reduction != 1))
+        return -1;
+    int bad = 0;
+    int64_t n_valid = count_valid(labels, T, V, ignore_index, &bad);
+    if (bad) return -5;
+    double scale = reduction == 0 ? (n_valid > 0 ? grad_scale / (double)n_valid : 0.0) : grad_scale;
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    double* xt = (double*)malloc(sizeof(double) * (size_t)H);
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!z || !xt || !wrow) {
+        free(z); free(xt); free(wrow);
+        return -1;
+    }
+    if (dW) memset(dW, 0, sizeof(double) * (size_t)(V * H));
+    double total = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t y = labels[t];
+        if (y == ignore_index) {
+            if (lse) lse[t] = 0.0;
+            if (dX) for (int64_t h = 0; h < H; ++h) dX[t * H + h] = 0.0;
+            continue;
+        }
+        widen(X, dt, t * H, H, xt);
+        double l = row_logits(xt, W, dt, H, V, z, wrow);
+        if (lse) lse[t] = l;
+        total += l - z[y];
+        /* D row = scale * (softmax - onehot), kept in z */
+        for (int64_t v = 0; v < V; ++v) z[v] = scale * (exp(z[v] - l) - (v == y ? 1.0 : 0.0));
+        if (dX) {
+            for (int64_t h = 0; h < H; ++h) dX[t * H + h] = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                widen(W, dt, v * H, H, wrow);
+                for (int64_t h = 0; h < H; ++h) dX[t * H + h] += z[v] * wrow[h];
+            }
+        }
+        if (dW)
+            for (int64_t v = 0; v < V; ++v)
+                for (int64_t h = 0; h < H; ++h) dW[v * H + h] += z[v] * xt[h];
+    }
+    /* the loss itself is not multiplied by grad_scale (the upstream gradient) */
+    if (loss) *loss = reduction == 0 ? (n_valid > 0 ? total / (double)n_valid : 0.0) : total;
+    free(z); free(xt); free(wrow);
+    return 0;
+}
+
+int orc_linear_ce_rows(const void* X, const void* W, int dt, const int64_t* labels, int64_t T, int64_t H,
+                       int64_t V, int64_t ignore_index, int reduction, double grad_scale,
+                       const int64_t* rows, int64_t n_rows, double* lse, double* loss_term, double* dX_rows) {
+    if (!X || !W || !labels || !rows || T < 0 || H <= 0 || V <= 0 || bad_dt(dt) ||
+        (reduction != 0 && reduction != 1))
+        return -1;
+    int bad = 0;
+    int64_t n_valid = count_valid(labels, T, V, ignore_index, &bad);
+    if (bad) return -5;
+    double scale = reduction == 0 ? (n_valid > 0 ? grad_scale / (double)n_valid : 0.0) : grad_scale;
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    double* xt = (double*)malloc(sizeof(double) * (size_t)H);
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!z || !xt || !wrow) {
+        free(z); free(xt); free(wrow);
+        return -1;
+    }
+    for (int64_t k = 0; k < n_rows; ++k) {
+        int64_t t = rows[k];
+        if (t < 0 || t >= T) {
+            free(z); free(xt); free(wrow);
+            return -2;
+        }
+        int64_t y = labels[t];
+        if (y == ignore_index) {
+            if (lse) lse[k] = 0.0;
+            if (loss_term) loss_term[k] = 0.0;
+            if (dX_rows) for (int64_t h = 0; h < H; ++h) dX_rows[k * H + h] = 0.0;
+            continue;
+        }
+        widen(X, dt, t * H, H, xt);
+        double l = row_logits(xt, W, dt, H, V, z, wrow);
+        if (lse) lse[k] = l;
+        if (loss_term) loss_term[k] = l - z[y];
+        if (dX_rows) {
+            for (int64_t v = 0; v < V; ++v) z[v] = scale * (exp(z[v] - l) - (v == y ? 1.0 : 0.0));
+            for (int64_t h = 0; h < H; ++h) dX_rows[k * H + h] = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                widen(W, dt, v * H, H, wrow);
+                for (int64_t h = 0; h < H; ++h) dX_rows[k * H + h] += z[v] * wrow[h];
+            }
+        }
+    }
+    free(z); free(xt); free(wrow);
+    return 0;
+}

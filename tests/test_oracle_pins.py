@@ -1,0 +1,218 @@
+"""Pins of the fp64 oracle to facts other than itself.
+
+Each operator is checked against closed forms, hand-worked values (tests/
+golden), invariants of the mathematics, and central finite differences on
+tiny inputs, chosen so that a plausible slip (a dropped term, a wrong sign,
+index or pairing, a transposed operand, eps in the wrong place, sum instead
+of mean) fails at least one test.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import golden
+
+RNG = np.random.default_rng(12345)
+
+
+# ------------------------------------------------------------------ RMSNorm
+def test_rmsnorm_constant_row_closed_form():
+    g = golden("rmsnorm_closed_forms.json")
+    x = np.full((2, g["H"]), g["a"]); w = np.ones(g["H"])
+    y, rstd = oracle.rmsnorm_fwd(x, w, g["eps"])
+    assert np.allclose(y, g["y"], rtol=1e-15, atol=0)
+    assert np.allclose(rstd, g["rstd"], rtol=1e-15, atol=0)
+
+
+def test_rmsnorm_scale_invariance_eps0():
+    x = RNG.standard_normal((5, 37)); w = 1 + 0.1 * RNG.standard_normal(37)
+    y0, _ = oracle.rmsnorm_fwd(x, w, 0.0)
+    for c in (0.5, 3.0, 1e3):
+        yc, _ = oracle.rmsnorm_fwd(c * x, w, 0.0)
+        assert np.max(np.abs(yc - y0)) < 1e-13
+
+
+def test_rmsnorm_unit_mean_square_and_weight_per_feature():
+    x = RNG.standard_normal((4, 64))
+    y, _ = oracle.rmsnorm_fwd(x, np.ones(64), 0.0)
+    assert np.allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-14)   # mean, not sum
+    w = np.arange(1, 9, dtype=np.float64)
+    y, _ = oracle.rmsnorm_fwd(np.full((1, 8), -3.0), w, 0.0)
+    assert np.allclose(y[0], -w, rtol=1e-15)                      # plain x*r*w, not (1+w)
+
+
+def _fd(f, x, h=1e-6):
+    g = np.zeros_like(x)
+    for i in np.ndindex(x.shape):
+        xp = x.copy(); xm = x.copy(); xp[i] += h; xm[i] -= h
+        g[i] = (f(xp) - f(xm)) / (2 * h)
+    return g
+
+
+def test_rmsnorm_bwd_finite_differences():
+    rows, H, eps = 3, 7, 1e-3
+    x = RNG.standard_normal((rows, H)); w = 1 + 0.1 * RNG.standard_normal(H); dy = RNG.standard_normal((rows, H))
+    dx, dw = oracle.rmsnorm_bwd(dy, x, w, eps)
+    L = lambda xx: float(np.sum(dy * oracle.rmsnorm_fwd(xx, w, eps)[0]))
+    Lw = lambda ww: float(np.sum(dy * oracle.rmsnorm_fwd(x, ww, eps)[0]))
+    fx, fw = _fd(L, x), _fd(Lw, w)
+    assert np.max(np.abs(dx - fx)) / np.max(np.abs(fx)) < 1e-7
+    assert np.max(np.abs(dw - fw)) / np.max(np.abs(fw)) < 1e-7
+
+
+def test_rmsnorm_bwd_orthogonal_to_x_when_eps0():
+    x = RNG.standard_normal((6, 33)); w = 1 + 0.1 * RNG.standard_normal(33); dy = RNG.standard_normal((6, 33))
+    dx, _ = oracle.rmsnorm_bwd(dy, x, w, 0.0)
+    assert np.max(np.abs(np.sum(dx * x, axis=1))) < 1e-12
+
+
+# --------------------------------------------------------------------- RoPE
+def test_rope_single_feature_angles():
+    for c in golden("rope_angles.json")["cases"]:
+        D, i, p = c["D"], c["i"], c["p"]
+        t = np.zeros((1, p + 1, 1, D)); t[0, p, 0, i] = 1.0
+        out = oracle.rope(t, c["theta"])
+        assert abs(out[0, p, 0, i] - c["cos"]) < 1e-12
+        assert abs(out[0, p, 0, i + D // 2] - c["sin"]) < 1e-12
+        others = np.delete(out[0, p, 0], [i, i + D // 2])
+        assert np.all(others == 0)
+        # the second half of a pair rotates the other way round
+        t2 = np.zeros_like(t); t2[0, p, 0, i + D // 2] = 1.0
+        o2 = oracle.rope(t2, c["theta"])
+        assert abs(o2[0, p, 0, i] + c["sin"]) < 1e-12 and abs(o2[0, p, 0, i + D // 2] - c["cos"]) < 1e-12
+
+
+def test_rope_norm_identity_inverse():
+    t = RNG.standard_normal((2, 9, 3, 16))
+    out = oracle.rope(t, 1e4)
+    half = 8
+    n_in = t[..., :half] ** 2 + t[..., half:] ** 2
+    n_out = out[..., :half] ** 2 + out[..., half:] ** 2
+    assert np.max(np.abs(n_in - n_out)) < 1e-13
+    assert np.array_equal(out[:, 0], t[:, 0])                     # position 0: identity
+    back = oracle.rope(out, 1e4, sign=-1)
+    assert np.max(np.abs(back - t)) < 1e-13                        # bwd o fwd = identity
+
+
+def test_rope_relative_position():
+    q = RNG.standard_normal((1, 1, 1, 32)); k = RNG.standard_normal((1, 1, 1, 32))
+    def dot(m, n):
+        rq = oracle.rope(q, 5e5, pos=np.array([[m]], np.int32))
+        rk = oracle.rope(k, 5e5, pos=np.array([[n]], np.int32))
+        return float(np.sum(rq * rk))
+    for m, n in ((5, 2), (100, 40), (8000, 7999)):
+        assert abs(dot(m, n) - dot(m + 17, n + 17)) < 1e-10
+    assert abs(dot(5, 2) - dot(9, 2)) > 1e-3
+
+
+def test_rope_bwd_is_adjoint():
+    x = RNG.standard_normal((2, 5, 2, 8)); dy = RNG.standard_normal((2, 5, 2, 8))
+    pos = np.array([[3, 1, 4, 1, 5], [9, 2, 6, 5, 3]], np.int32)
+    lhs = np.sum(dy * oracle.rope(x, 1e4, pos=pos))
+    rhs = np.sum(oracle.rope(dy, 1e4, sign=-1, pos=pos) * x)
+    assert abs(lhs - rhs) < 1e-12
+
+
+# ------------------------------------------------------------------- SwiGLU
+def test_swiglu_values():
+    g = golden("silu_values.json")
+    gate = np.array([0.0, 1.0, -1.0, 40.0, -40.0]); up = np.array([2.0, 3.0, 5.0, 0.5, 7.0])
+    y = oracle.swiglu_fwd(gate, up)
+    assert y[0] == 0.0
+    assert abs(y[1] - 3 * g["silu_1"]) < 1e-15 and abs(y[2] - 5 * g["silu_m1"]) < 1e-15
+    assert abs(y[3] - 40 * 0.5) < 1e-12
+    assert abs(y[4] - (-280.0 * math.exp(-40) / (1 + math.exp(-40)))) < 1e-28   # -40 * sigmoid(-40) * 7
+    dy = np.array([1.5, 2.0, 1.0, 1.0, 1.0])
+    dg, du = oracle.swiglu_bwd(dy, gate, up)
+    assert abs(dg[0] - 1.5 * 2.0 * g["dsilu_0"]) < 1e-15 and du[0] == 0.0
+    assert abs(dg[1] - 2.0 * 3.0 * g["dsilu_1"]) < 1e-14
+    assert abs(du[1] - 2.0 * g["silu_1"]) < 1e-15
+
+
+def test_swiglu_bwd_finite_differences():
+    gate = RNG.standard_normal(11) * 2; up = RNG.standard_normal(11); dy = RNG.standard_normal(11)
+    dg, du = oracle.swiglu_bwd(dy, gate, up)
+    fg = _fd(lambda gg: float(np.sum(dy * oracle.swiglu_fwd(gg, up))), gate)
+    fu = _fd(lambda uu: float(np.sum(dy * oracle.swiglu_fwd(gate, uu))), up)
+    assert np.max(np.abs(dg - fg)) < 1e-8 and np.max(np.abs(du - fu)) < 1e-8
+
+
+# --------------------------------------------------------------- linear CE
+def test_ce_three_class_golden():
+    g = golden("ce_three_class.json")
+    X = np.array([g["logits"]]); W = np.eye(3)
+    r = oracle.linear_ce(X, W, np.array([g["label"]]))
+    assert abs(r["loss"] - g["loss"]) < 1e-14
+    assert np.max(np.abs(r["dX"][0] - np.array(g["grad"]))) < 1e-15   # W = I: dX = D
+    assert np.max(np.abs(r["dW"] - np.outer(g["grad"], g["logits"]))) < 1e-14
+
+
+@pytest.mark.parametrize("V", [1024, 5, 77])
+def test_ce_uniform_logits_is_ln_v(V):
+    T, H = 6, 4
+    X = RNG.standard_normal((T, H)); W = np.zeros((V, H))
+    lab = RNG.integers(0, V, T)
+    assert abs(oracle.linear_ce(X, W, lab)["loss"] - math.log(V)) < 1e-13
+    W2 = RNG.standard_normal((V, H))
+    assert abs(oracle.linear_ce(np.zeros((T, H)), W2, lab)["loss"] - math.log(V)) < 1e-13
+
+
+def test_ce_large_vocab_ln_v():
+    for V in (128256, 151936):
+        r = oracle.linear_ce(np.zeros((1, 2)), np.ones((V, 2)), np.array([V - 1]), want_grads=False)
+        assert abs(r["loss"] - math.log(V)) < 1e-12
+
+
+def test_ce_grad_rows_sum_zero_and_ignore():
+    T, H, V = 7, 5, 9
+    X = RNG.standard_normal((T, H)); W = RNG.standard_normal((V, H))
+    lab = RNG.integers(0, V, T); lab[[1, 4]] = -100
+    r = oracle.linear_ce(X, W, lab)
+    # sum over the vocabulary of dW rows = sum_t (sum_v D_tv) X_t = 0
+    assert np.max(np.abs(r["dW"].sum(axis=0))) < 1e-14
+    assert np.all(r["dX"][[1, 4]] == 0.0)
+    X2 = X.copy(); X2[[1, 4]] = 1e3                                  # ignored rows do not matter
+    r2 = oracle.linear_ce(X2, W, lab)
+    assert abs(r2["loss"] - r["loss"]) < 1e-14 and np.max(np.abs(r2["dW"] - r["dW"])) < 1e-14
+
+
+def test_ce_all_ignored_and_bad_label():
+    X = RNG.standard_normal((3, 2)); W = RNG.standard_normal((4, 2))
+    r = oracle.linear_ce(X, W, np.array([-100, -100, -100]))
+    assert r["loss"] == 0.0 and np.all(r["dX"] == 0) and np.all(r["dW"] == 0)
+    with pytest.raises(ValueError, match="-5"):
+        oracle.linear_ce(X, W, np.array([0, 4, 1]))
+
+
+def test_ce_finite_differences_mean_and_sum():
+    T, H, V = 4, 3, 5
+    X = RNG.standard_normal((T, H)); W = RNG.standard_normal((V, H)); lab = np.array([2, -100, 4, 0])
+    for red in ("mean", "sum"):
+        r = oracle.linear_ce(X, W, lab, reduction=red, grad_scale=1.7)
+        fX = _fd(lambda xx: 1.7 * oracle.linear_ce(xx, W, lab, reduction=red, want_grads=False)["loss"], X)
+        fW = _fd(lambda ww: 1.7 * oracle.linear_ce(X, ww, lab, reduction=red, want_grads=False)["loss"], W)
+        assert np.max(np.abs(r["dX"] - fX)) < 1e-8
+        assert np.max(np.abs(r["dW"] - fW)) < 1e-8
+    rm = oracle.linear_ce(X, W, lab)["loss"]; rs = oracle.linear_ce(X, W, lab, reduction="sum")["loss"]
+    assert abs(rs - 3 * rm) < 1e-13                                   # 3 valid rows
+
+
+def test_ce_rows_matches_full_definition():
+    T, H, V = 9, 6, 13
+    X = RNG.standard_normal((T, H)); W = RNG.standard_normal((V, H)); lab = RNG.integers(0, V, T); lab[2] = -100
+    full = oracle.linear_ce(X, W, lab)
+    rows = np.array([0, 2, 8, 5])
+    part = oracle.linear_ce_rows(X, W, lab, rows)
+    assert np.max(np.abs(part["dX"] - full["dX"][rows])) < 1e-15
+    assert np.max(np.abs(part["lse"] - full["lse"][rows])) < 1e-15
+    assert abs(part["loss_term"][1]) == 0.0
+
+
+def test_storage_widening_is_exact():
+    import datagen
+    b = datagen.normal(0, "w", (4, 8), "bf16"); f = datagen.bf16_bits_to_f32(b)
+    y1, _ = oracle.rmsnorm_fwd(b, datagen.f32_to_bf16_bits(np.ones(8, np.float32)), 1e-6)
+    y2, _ = oracle.rmsnorm_fwd(f.astype(np.float64), np.ones(8), 1e-6)
+    assert np.array_equal(y1, y2)
