@@ -1,0 +1,432 @@
+"""Benchmark: the fused decoder-op chain of one Qwen-7B-like layer, fwd+bwd.
+
+One step runs every operator once, forward and backward, on independently
+drawn bf16 tensors of the layer's shapes at batch 1, seq S (default 32768):
+
+  RMSNorm fwd [S, 4096] -> RoPE fwd Q/K [1, S, 32, 128] -> SwiGLU fwd [S, 11008]
+  -> fused linear-CE fwd+bwd (S x 4096 x 151936, 10 % ignored labels)
+  -> SwiGLU bwd -> RoPE bwd -> RMSNorm bwd
+
+Prints one JSON line: tokens/s of the whole chain (device-resident inputs),
+the same through host buffers (e2e), the roofline of the dominant kernel
+(the linear-CE's tensor-core GEMMs, 6*S*H*V algorithmic flops per call),
+HBM GB/s of every memory-bound kernel, the oracle's CPU throughput on a
+bounded sample, and SM clocks sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--seq S] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own chain on its own data (weak
+scaling, no collective on the data path); the timed region is bracketed by
+barriers and the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HIDDEN, HEADS, HEAD_DIM, INTER, VOCAB = 4096, 32, 128, 11008, 151936
+THETA, EPS = 1e4, 1e-6
+METRIC = "fused decoder-op chain tokens/s fwd+bwd (RMSNorm, RoPE, SwiGLU, fused linear-CE)"
+UNIT = "tokens/s"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--seq", type=int, default=32768)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    return p.parse_args(argv)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+# ------------------------------------------------------------------ ranks
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Slowest rank's time (the job's time); identity on one process."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, dist, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workload
+def workload_config(S):
+    return {"workload": f"Qwen-7B-like layer op chain, batch 1, seq {S}: RMSNorm [{S}x{HIDDEN}] -> RoPE Q/K "
+                        f"[1,{S},{HEADS},{HEAD_DIM}] -> SwiGLU [{S}x{INTER}] -> fused linear-CE "
+                        f"{S}x{HIDDEN}x{VOCAB}, fwd+bwd",
+            "batch": 1, "seq_len": S, "hidden": HIDDEN, "heads": HEADS, "head_dim": HEAD_DIM,
+            "intermediate": INTER, "vocab": VOCAB, "ignore_frac": 0.10, "eps": EPS, "rope_theta": THETA,
+            "l2": "inputs larger than L2 (every tensor >= 2*S*4096 bytes; lm_head 1.24 GB)",
+            "parallelism": "one chain per GPU (weak scaling, no collective)"}
+
+
+def algorithmic(S):
+    """Algorithmic bytes (memory-bound kernels) and flops (linear-CE) per call."""
+    e = 2
+    SH, SI = S * HIDDEN, S * INTER
+    qk = 2 * S * HEADS * HEAD_DIM
+    return {
+        "rmsnorm_fwd": 2 * SH * e + S * 4 + HIDDEN * e,
+        "rmsnorm_bwd": 3 * SH * e + S * 4 + 2 * HIDDEN * e,
+        "rope_fwd": 2 * qk * e,
+        "rope_bwd": 2 * qk * e,
+        "swiglu_fwd": 3 * SI * e,
+        "swiglu_bwd": 5 * SI * e,
+        "linear_ce_flops": 6 * S * HIDDEN * VOCAB,
+    }
+
+
+def gen_inputs(S, seed_offset=0):
+    """Host inputs (numpy storage arrays; bf16 as uint16 bits)."""
+    from datagen import workloads
+    w = workloads.qwen_chain(S)
+    if seed_offset:
+        for v in w.values():
+            v.seed += 1000 * seed_offset
+    r, p, s, c = w["rmsnorm"], w["rope"], w["swiglu"], w["linear_ce"]
+    return {"x": r.make("x"), "w": r.make("w"), "dy_r": r.make("dy"),
+            "q": p.make("q"), "k": p.make("k"), "dq": p.make("dq"), "dk": p.make("dk"),
+            "gate": s.make("gate"), "up": s.make("up"), "dy_s": s.make("dy"),
+            "X": c.make("X"), "W": c.make("W"), "labels": c.make("labels")}
+
+
+def to_torch(a, device=None, pin=False):
+    import torch
+    if a.dtype == np.uint16:
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(a)
+    if pin:
+        return t.pin_memory()
+    return t.to(device) if device is not None else t
+
+
+class Chain:
+    """Device buffers of one chain and the calls of one step."""
+
+    def __init__(self, L, inputs, device):
+        import torch
+        self.L = L
+        bf = torch.bfloat16
+        S = inputs["x"].shape[0]
+        self.S = S
+        self.inp = {k: (to_torch(v, device) if v is not None else None) for k, v in inputs.items()}
+        self.y = torch.empty(S, HIDDEN, dtype=bf, device=device)
+        self.rstd = torch.empty(S, dtype=torch.float32, device=device)
+        self.dx = torch.empty(S, HIDDEN, dtype=bf, device=device)
+        self.dw = torch.empty(HIDDEN, dtype=bf, device=device)
+        self.ws_r = torch.empty(L.liger_rmsnorm_bwd_workspace(S, HIDDEN), dtype=torch.uint8, device=device)
+        self.ys = torch.empty(S, INTER, dtype=bf, device=device)
+        self.dg = torch.empty(S, INTER, dtype=bf, device=device)
+        self.du = torch.empty(S, INTER, dtype=bf, device=device)
+        self.loss = torch.empty(1, dtype=torch.float32, device=device)
+        self.dX = torch.empty(S, HIDDEN, dtype=bf, device=device)
+        self.dW = torch.empty(VOCAB, HIDDEN, dtype=bf, device=device)
+        self.ws_c = torch.empty(L.liger_linear_ce_workspace(S, HIDDEN, VOCAB, 0, L.LIGER_BF16), dtype=torch.uint8,
+                                device=device)
+
+    def launches_per_step(self):
+        chunk = min(4096, self.S)
+        nchunks = -(-self.S // chunk)
+        return 1 + 1 + 1 + (1 + 5 * nchunks + 1) + 1 + 1 + 2
+
+    def step(self, ev=None):
+        """One pass of every operator; ev: dict name -> list of (start, end) events."""
+        L, i = self.L, self.inp
+
+        def rec(name, fn):
+            if ev is None:
+                fn()
+                return
+            import torch
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            ev.setdefault(name, []).append((a, b))
+
+        rec("rmsnorm_fwd", lambda: L.liger_rmsnorm_fwd(i["x"], i["w"], self.y, self.rstd, EPS))
+        rec("rope_fwd", lambda: L.liger_rope_fwd(i["q"], i["k"], None, THETA))
+        rec("swiglu_fwd", lambda: L.liger_swiglu_fwd(i["gate"], i["up"], self.ys))
+        rec("linear_ce", lambda: L.liger_linear_ce_fwd_bwd(i["X"], i["W"], i["labels"], self.loss, self.dX, self.dW,
+                                                           self.ws_c))
+        rec("swiglu_bwd", lambda: L.liger_swiglu_bwd(i["dy_s"], i["gate"], i["up"], self.dg, self.du))
+        rec("rope_bwd", lambda: L.liger_rope_bwd(i["dq"], i["dk"], None, THETA))
+        rec("rmsnorm_bwd", lambda: L.liger_rmsnorm_bwd(i["dy_r"], i["x"], i["w"], self.rstd, self.dx, self.dw,
+                                                       self.ws_r))
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.idx = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        loaded = [x for x in sm if x > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(S, inputs, n_rows=32, n_tokens=1):
+    """Time the fp64 oracle (single-threaded) on a bounded sample of the
+    chain's workload; returns (tokens/s, description, seconds)."""
+    import oracle
+    r = np.random.default_rng(0).choice(S, n_rows, replace=False)
+    x, w, dy = inputs["x"][r], inputs["w"], inputs["dy_r"][r]
+    per_token = 0.0
+    t0 = time.perf_counter()
+    oracle.rmsnorm_fwd(x, w, EPS)
+    oracle.rmsnorm_bwd(dy, x, w, EPS)
+    per_token += (time.perf_counter() - t0) / n_rows
+    q = np.ascontiguousarray(inputs["q"][:, r]); k = np.ascontiguousarray(inputs["k"][:, r])
+    pos = r.astype(np.int32)[None, :]
+    t0 = time.perf_counter()
+    oracle.rope(q, THETA, pos=pos); oracle.rope(k, THETA, pos=pos)
+    oracle.rope(q, THETA, sign=-1, pos=pos); oracle.rope(k, THETA, sign=-1, pos=pos)
+    per_token += (time.perf_counter() - t0) / n_rows
+    g, u, ds = inputs["gate"][r], inputs["up"][r], inputs["dy_s"][r]
+    t0 = time.perf_counter()
+    oracle.swiglu_fwd(g, u)
+    oracle.swiglu_bwd(ds, g, u)
+    per_token += (time.perf_counter() - t0) / n_rows
+    lab = inputs["labels"]
+    valid = np.nonzero(lab != -100)[0][:n_tokens]
+    X = np.ascontiguousarray(inputs["X"][valid])
+    t0 = time.perf_counter()
+    oracle.linear_ce(X, inputs["W"], lab[valid])
+    per_token += (time.perf_counter() - t0) / len(valid)
+    desc = (f"fp64 oracle, 1 thread: RMSNorm/RoPE/SwiGLU fwd+bwd on {n_rows} random rows/positions of seq {S}, "
+            f"linear-CE fwd+bwd (lse, dX, dW) on {len(valid)} token(s) x full vocab {VOCAB}; tokens/s = 1 / sum of "
+            f"per-token times")
+    return 1.0 / per_token, desc, per_token
+
+
+def emit(d):
+    print(json.dumps(d), flush=True)
+
+
+# ---------------------------------------------------------------- arms
+def reference_arm(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    S = args.seq
+    inputs = gen_inputs(S)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, desc, _ = cpu_oracle_sample(S, inputs, n_rows=16, n_tokens=1)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.mean(vals)
+    d = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * S / value, "higher_is_better": True,
+         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(S),
+         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    emit(d)
+    return 0
+
+
+def native_arm(args):
+    import torch
+    rank, world, local = dist_env()
+    dist = dist_init(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import transformer_rmsnorm_fwd_gb300 as L
+    L.load()
+    S, K, W = args.seq, args.steps, args.warmup
+    assert W >= 0 and K >= 1
+    inputs = gen_inputs(S, seed_offset=rank)
+    chain = Chain(L, inputs, dev)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing
+    for _ in range(W):
+        chain.step()
+    ev = {}
+    clk = ClockSampler(local)
+    clk.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(K):
+        chain.step(ev)
+    t_end.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = clk.stop()
+    ms = max_over_ranks(t_start.elapsed_time(t_end), dist, dev)
+    tokens = sum_over_ranks(float(S * K), dist, dev)
+    value = tokens / (ms / 1000.0)
+    per_op = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+    loss = float(chain.loss.item())
+
+    # ---- end to end through host buffers: H2D of the step's inputs, D2H of the loss
+    e2e = None
+    if not args.no_e2e:
+        host = {k: to_torch(v, pin=True) for k, v in inputs.items()}
+        h_loss = torch.empty(1, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+
+        def e2e_step():
+            for k, t in host.items():
+                chain.inp[k].copy_(t, non_blocking=True)
+            chain.step()
+            h_loss.copy_(chain.loss, non_blocking=True)
+
+        for _ in range(max(1, W)):
+            e2e_step()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(K):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        ms_e = max_over_ranks(a.elapsed_time(b), dist, dev)
+        e2e = {"value": tokens / (ms_e / 1000.0), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": 4, "ms_per_step": ms_e / K}
+        del host
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    pk = peaks()
+    alg = algorithmic(S)
+    hbm = {}
+    for k in ("rmsnorm_fwd", "rmsnorm_bwd", "rope_fwd", "rope_bwd", "swiglu_fwd", "swiglu_bwd"):
+        gbs = alg[k] / (per_op[k] / 1000.0) / 1e9
+        hbm[k] = {"ms": round(per_op[k], 4), "bytes": alg[k], "gbs": round(gbs, 1),
+                  "frac": round(gbs / pk["hbm_gbs"], 4)}
+    ce_tf = alg["linear_ce_flops"] / (per_op["linear_ce"] / 1000.0) / 1e12
+    roofline = {"kernel": "liger_linear_ce_fwd_bwd (tcgen05 GEMMs + fused epilogues; 6*S*H*V flops per call)",
+                "bound": "tensor", "achieved": round(ce_tf, 1), "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                "frac": round(ce_tf / pk["bf16_sustained"], 4), "traffic": None,
+                "peak_source": f"{pk['src']} bf16 sustained (cuBLAS loop under the power cap)",
+                "ms_per_call": round(per_op["linear_ce"], 3)}
+    cpu = None
+    if not args.no_cpu:
+        v, desc, _ = cpu_oracle_sample(S, inputs)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+    d = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+         "data": "synthetic (seeded SplitMix64/Box-Muller, shapes and distributions of the Qwen-7B layer chain)",
+         "config": workload_config(S), "roofline": roofline, "hbm_kernels": hbm,
+         "hbm_peak_gbs": pk["hbm_gbs"], "cpu_baseline": cpu, "e2e": e2e,
+         "gpu_launches": chain.launches_per_step() * K, "clocks": clocks, "loss": loss}
+    emit(d)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+    return native_arm(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,177 @@
+/*
+ * liger.h -- C-ABI of libliger.so: fused decoder-layer operators for one
+ * NVIDIA GB300 GPU (sm_103a), hand-written CUDA.
+ *
+ * Operators (as described on the Liger-Kernel pages):
+ *   - RMSNorm forward / backward, a per-row reduction;
+ *   - RoPE, rotating Q and K in place;
+ *   - the SwiGLU activation silu(gate) * up and its backward;
+ *   - a fused linear cross-entropy that never writes the full [T x V]
+ *     logits to device memory.
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer (cudaMalloc'd or from a
+ *     device caching allocator) unless stated otherwise.  Tensors are dense
+ *     and row-major (C order).  Float tensor pointers must be 16-byte
+ *     aligned.
+ *   - The library allocates nothing and frees nothing: the caller owns every
+ *     buffer, including workspaces, and must keep them alive until the work
+ *     queued on `stream` has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls queue work on it and return without waiting, except
+ *     liger_linear_ce_fwd_bwd, which waits for its label scan (see there).
+ *   - `dtype` is LIGER_F32 or LIGER_BF16 and applies to every float tensor
+ *     of the call except the ones documented as float (rstd, loss); all
+ *     arithmetic is fp32 whatever the storage type.
+ *   - Sizes are element counts (int64_t).  Zero-sized problems are valid and
+ *     launch nothing.
+ *   - Every call returns a status (LIGER_OK = 0 or a negative code below).
+ *     Argument checks run before any work is queued: a call that fails them
+ *     queues nothing and leaves every output untouched.
+ *     liger_last_error() then describes the failure (per calling thread).
+ *   - The current CUDA device is the one the pointers belong to.
+ */
+#ifndef LIGER_H
+#define LIGER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* storage types */
+#define LIGER_F32 0
+#define LIGER_BF16 1
+
+/* status codes */
+#define LIGER_OK 0
+#define LIGER_ERR_NULL (-1)       /* a required pointer is NULL */
+#define LIGER_ERR_SHAPE (-2)      /* a size is negative or inconsistent */
+#define LIGER_ERR_DTYPE (-3)      /* dtype is not LIGER_F32 / LIGER_BF16 */
+#define LIGER_ERR_ALIGN (-4)      /* a float tensor pointer is not 16-byte aligned */
+#define LIGER_ERR_LABEL (-5)      /* a label is outside [0, V) and is not ignore_index */
+#define LIGER_ERR_WORKSPACE (-6)  /* workspace missing or smaller than required */
+#define LIGER_ERR_CUDA (-7)       /* a CUDA runtime call or kernel launch failed */
+
+/* Message for the last failing call on this thread ("" if none). */
+const char* liger_last_error(void);
+
+/* ------------------------------------------------------------- RMSNorm
+ * Source: the RMSNorm step of the fused RMSNorm + QKV + RoPE kernel on the
+ * page "Liger-Kernel底层优化：新一代内核级推理加速引擎介绍", section
+ * "融合内核是如何工作的？来看一段简化版实现": the row's sum of squares over the
+ * hidden size plus epsilon, under an inverse square root, scales the element
+ * and the per-feature weight.
+ *
+ * Forward, per row r of x [rows, cols]:
+ *     rstd[r] = 1 / sqrt(mean_j x[r,j]^2 + eps)
+ *     y[r,j]  = x[r,j] * rstd[r] * w[j]            (one rounding, at the store)
+ *   x, y: [rows, cols] in dtype; w: [cols] in dtype; rstd: [rows] float, may
+ *   be NULL (not stored).  y may alias x.
+ */
+int liger_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows, int64_t cols,
+                      float eps, int dtype, void* stream);
+
+/* Bytes of workspace liger_rmsnorm_bwd needs (fp32 per-block partial sums of
+ * dw): an upper bound valid on any device, min(rows, 1024) * cols * 4. */
+size_t liger_rmsnorm_bwd_workspace(int64_t rows, int64_t cols);
+
+/* Backward (the derivative of the forward; the pages give none):
+ *     g = dy * w,   s_r = sum_j g[r,j] x[r,j]
+ *     dx[r,j] = rstd[r] * g[r,j] - rstd[r]^3 / cols * x[r,j] * s_r
+ *     dw[j]   = sum_r dy[r,j] * x[r,j] * rstd[r]
+ *   dy, x, dx: [rows, cols]; w, dw: [cols], all in dtype; rstd: [rows] float
+ *   as written by the forward.  dx may alias dy.  dw is reduced in a fixed
+ *   order (deterministic run to run on one device).
+ *   ws: device workspace of at least liger_rmsnorm_bwd_workspace(rows, cols)
+ *   bytes, 16-byte aligned; its contents on entry do not matter.
+ */
+int liger_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float* rstd, void* dx, void* dw,
+                      void* ws, size_t ws_bytes, int64_t rows, int64_t cols, int dtype, void* stream);
+
+/* ---------------------------------------------------------------- RoPE
+ * Source: the FusedRoPE paragraph of the page "Liger-Kernel核心技术：
+ * RollingBuffer与融合算子详解", section "算子融合" (the angle comes from the
+ * token position, generated in the kernel with no stored table), and the
+ * RoPE step of the fused-kernel listing on the page "Liger-Kernel底层优化：
+ * 新一代内核级推理加速引擎介绍" (feature f is paired by f mod head_dim/2).
+ *
+ * In place on q [batch, seq, n_q_heads, head_dim] and k [batch, seq,
+ * n_k_heads, head_dim]: for each head and pair i in [0, head_dim/2),
+ *     phi = p * theta^(-2i/head_dim),   p = pos[b*seq + s] or s if pos is NULL
+ *     (a, b) = (v[i], v[i + head_dim/2])
+ *     v[i] = a cos(phi) - b sin(phi),   v[i + head_dim/2] = b cos(phi) + a sin(phi)
+ * The angle is formed and reduced modulo 2 pi in double precision, then
+ * cos/sin are taken in single precision.  head_dim must be even.  pos is an
+ * int32 device array [batch, seq] of values >= 0, or NULL.  q (k) may be NULL
+ * only when n_q_heads (n_k_heads) is 0.
+ */
+int liger_rope_fwd(void* q, void* k, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
+                   int64_t n_k_heads, int64_t head_dim, double theta, int dtype, void* stream);
+
+/* Backward: the same rotation by -phi (the transpose of the forward map),
+ * applied in place to the incoming gradients dq, dk.  Arguments as above. */
+int liger_rope_bwd(void* dq, void* dk, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
+                   int64_t n_k_heads, int64_t head_dim, double theta, int dtype, void* stream);
+
+/* -------------------------------------------------------------- SwiGLU
+ * Source: the FusedLinearSwiGLU paragraph of the page "Liger-Kernel核心技术：
+ * RollingBuffer与融合算子详解", section "算子融合": SiLU of the gate branch,
+ * then an elementwise product with the up branch, in registers.
+ *
+ * Forward:  y = silu(gate) * up,  silu(g) = g / (1 + exp(-g)).
+ *   gate, up, y: n elements in dtype (any shape; the op is pointwise).
+ *   y may alias gate or up.
+ */
+int liger_swiglu_fwd(const void* gate, const void* up, void* y, int64_t n, int dtype, void* stream);
+
+/* Backward (textbook derivative):  s = sigmoid(g)
+ *     dup   = dy * g * s
+ *     dgate = dy * up * s * (1 + g * (1 - s))
+ *   dgate may alias gate and dup may alias up (in-place backward). */
+int liger_swiglu_bwd(const void* dy, const void* gate, const void* up, void* dgate, void* dup, int64_t n,
+                     int dtype, void* stream);
+
+/* ------------------------------------------------ fused linear + CE
+ * Source: the FusedCrossEntropyLoss paragraph of the page "Liger-Kernel核心
+ * 技术：RollingBuffer与融合算子详解", section "算子融合" (softmax and NLL
+ * merged, the softmax never stored), with the running max / normaliser
+ * merge of the online softmax described on the page "Liger-Kernel内核级优化：
+ * FlashAttention与RollingBuffer详解".
+ *
+ *   z_t = W x_t  (fp32 accumulation), lse_t = log sum_v exp(z_t[v])
+ *   loss = sum over rows with labels[t] != ignore_index of (lse_t - z_t[labels[t]]),
+ *          divided by their count n_valid when reduction = 0 (mean; 0 if
+ *          n_valid = 0), not divided when reduction = 1 (sum)
+ *   D_t  = s * (softmax(z_t) - onehot(labels[t])),  s = grad_scale / n_valid
+ *          (mean) or grad_scale (sum);  D_t = 0 on ignored rows
+ *   dX = D W,  dW = D^T X
+ *
+ *   X: [T, H], W: [V, H] (row-major) in dtype; labels: [T] int64 device array;
+ *   loss: one float on the device; dX: [T, H] and dW: [V, H] in dtype, each
+ *   may be NULL (not computed).  Rows of dX whose label is ignore_index are
+ *   written as +0.0.
+ *   The tokens are processed in chunks of `chunk` rows (0 = automatic, at most
+ *   4096); per chunk the logits exist only in a [chunk x V] workspace buffer,
+ *   never as a [T x V] tensor.  dW is accumulated across chunks in fp32.
+ *   ws: device workspace of at least liger_linear_ce_workspace(T, H, V,
+ *   chunk, dtype) bytes, 256-byte aligned.  On return ws begins with
+ *   float lse[T] (0 on ignored rows), followed by float loss_row[T]
+ *   (lse_t - z_t[label], 0 on ignored rows).
+ *   Labels are validated on the device before any other work; the call waits
+ *   for that scan (one stream synchronisation) and returns LIGER_ERR_LABEL,
+ *   with nothing else queued, if a label is outside [0, V) and is not
+ *   ignore_index.
+ */
+size_t liger_linear_ce_workspace(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype);
+
+int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H, int64_t V,
+                            int64_t ignore_index, int reduction, float grad_scale, float* loss, void* dX, void* dW,
+                            void* ws, size_t ws_bytes, int64_t chunk, int dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIGER_H */

@@ -1,0 +1,11 @@
+"""Fused decoder-layer operators for one NVIDIA GB300 GPU (sm_103a).
+
+RMSNorm forward/backward, in-place RoPE on Q and K, the SwiGLU activation
+and a fused linear cross-entropy that never materialises the [T x V]
+logits, all hand-written CUDA behind the C-ABI of ``libliger.so``
+(``include/liger.h``).  This package is the Python binding of that library:
+see ``_native`` for the functions, which carry the C entry points' names.
+"""
+from ._native import (LIGER_BF16, LIGER_F32, LigerError, liger_linear_ce_fwd_bwd,  # noqa: F401
+                      liger_linear_ce_workspace, liger_rmsnorm_bwd, liger_rmsnorm_bwd_workspace, liger_rmsnorm_fwd,
+                      liger_rope_bwd, liger_rope_fwd, liger_swiglu_bwd, liger_swiglu_fwd, load)

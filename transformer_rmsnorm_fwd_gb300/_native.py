@@ -1,0 +1,180 @@
+"""Thin Python binding of libliger.so (argument marshalling only).
+
+Every function below has the name of the C entry point it calls and takes
+torch tensors that already live on the GPU; it passes their device
+pointers, sizes and the current CUDA stream to the library and raises
+``LigerError`` on a non-zero status.  All computation happens in the
+library's CUDA kernels; there is no fallback of any kind: if the library is
+missing, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libliger.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "liger.h")
+
+LIGER_F32, LIGER_BF16 = 0, 1
+STATUS = {0: "OK", -1: "LIGER_ERR_NULL", -2: "LIGER_ERR_SHAPE", -3: "LIGER_ERR_DTYPE", -4: "LIGER_ERR_ALIGN",
+          -5: "LIGER_ERR_LABEL", -6: "LIGER_ERR_WORKSPACE", -7: "LIGER_ERR_CUDA"}
+
+_lib = None
+_lock = threading.Lock()
+
+_P, _I64, _F, _D, _INT, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_int,
+                               ctypes.c_size_t)
+SIGNATURES = {
+    "liger_last_error": ([], ctypes.c_char_p),
+    "liger_rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _INT, _P], _INT),
+    "liger_rmsnorm_bwd_workspace": ([_I64, _I64], _SZ),
+    "liger_rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _INT, _P], _INT),
+    "liger_rope_fwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _D, _INT, _P], _INT),
+    "liger_rope_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _D, _INT, _P], _INT),
+    "liger_swiglu_fwd": ([_P, _P, _P, _I64, _INT, _P], _INT),
+    "liger_swiglu_bwd": ([_P, _P, _P, _P, _P, _I64, _INT, _P], _INT),
+    "liger_linear_ce_workspace": ([_I64, _I64, _I64, _I64, _INT], _SZ),
+    "liger_linear_ce_fwd_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _I64, _INT, _P],
+                                _INT),
+}
+
+
+class LigerError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def header_functions() -> list:
+    """Names of the functions include/liger.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(liger_[a-z_0-9]+)\s*\(", text, re.M)))
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libliger.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build() "
+                                   "(python -m transformer_rmsnorm_fwd_gb300.build)")
+            lib = ctypes.CDLL(p)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise LigerError(rc, load().liger_last_error().decode())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return LIGER_F32
+    if t.dtype == torch.bfloat16:
+        return LIGER_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream() -> int:
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dense(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ------------------------------------------------------------------ RMSNorm
+def liger_rmsnorm_fwd(x, w, y, rstd=None, eps: float = 1e-6):
+    _dense(x, w, y, rstd)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    _check(load().liger_rmsnorm_fwd(_ptr(x), _ptr(w), _ptr(y), _ptr(rstd), rows, cols, eps, _dtype_code(x),
+                                    _stream()))
+    return y, rstd
+
+
+def liger_rmsnorm_bwd_workspace(rows: int, cols: int) -> int:
+    return int(load().liger_rmsnorm_bwd_workspace(rows, cols))
+
+
+def liger_rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws):
+    _dense(dy, x, w, rstd, dx, dw, ws)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().liger_rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), _ptr(ws), nbytes,
+                                    rows, cols, _dtype_code(x), _stream()))
+    return dx, dw
+
+
+# --------------------------------------------------------------------- RoPE
+def _rope(fn, q, k, pos, theta):
+    _dense(q, k, pos)
+    B, S, Hq, D = q.shape
+    Hk = k.shape[2] if k is not None else 0
+    if k is not None and (k.shape[0] != B or k.shape[1] != S or k.shape[3] != D):
+        raise ValueError("q and k must agree in batch, seq and head_dim")
+    _check(fn(_ptr(q), _ptr(k), _ptr(pos), B, S, Hq, Hk, D, float(theta), _dtype_code(q), _stream()))
+    return q, k
+
+
+def liger_rope_fwd(q, k, pos=None, theta: float = 1e4):
+    return _rope(load().liger_rope_fwd, q, k, pos, theta)
+
+
+def liger_rope_bwd(dq, dk, pos=None, theta: float = 1e4):
+    return _rope(load().liger_rope_bwd, dq, dk, pos, theta)
+
+
+# ------------------------------------------------------------------- SwiGLU
+def liger_swiglu_fwd(gate, up, y):
+    _dense(gate, up, y)
+    _check(load().liger_swiglu_fwd(_ptr(gate), _ptr(up), _ptr(y), gate.numel(), _dtype_code(gate), _stream()))
+    return y
+
+
+def liger_swiglu_bwd(dy, gate, up, dgate, dup):
+    _dense(dy, gate, up, dgate, dup)
+    _check(load().liger_swiglu_bwd(_ptr(dy), _ptr(gate), _ptr(up), _ptr(dgate), _ptr(dup), gate.numel(),
+                                   _dtype_code(gate), _stream()))
+    return dgate, dup
+
+
+# ---------------------------------------------------------------- linear CE
+def liger_linear_ce_workspace(T: int, H: int, V: int, chunk: int = 0, dtype: int = LIGER_BF16) -> int:
+    return int(load().liger_linear_ce_workspace(T, H, V, chunk, dtype))
+
+
+def liger_linear_ce_fwd_bwd(X, W, labels, loss, dX, dW, ws, ignore_index: int = -100, reduction: str = "mean",
+                            grad_scale: float = 1.0, chunk: int = 0):
+    _dense(X, W, labels, loss, dX, dW, ws)
+    T, H = X.shape
+    V = W.shape[0]
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().liger_linear_ce_fwd_bwd(_ptr(X), _ptr(W), _ptr(labels), T, H, V, int(ignore_index),
+                                          0 if reduction == "mean" else 1, float(grad_scale), _ptr(loss), _ptr(dX),
+                                          _ptr(dW), _ptr(ws), nbytes, int(chunk), _dtype_code(X), _stream()))
+    return loss, dX, dW

@@ -1,0 +1,544 @@
+// Fused linear cross-entropy, forward and backward, token-chunked.
+//
+// Operator: the FusedCrossEntropyLoss paragraph of the page "Liger-Kernel核心
+// 技术：RollingBuffer与融合算子详解", section "算子融合" -- softmax and NLL in one
+// step on the classifier-head output, the softmax never stored -- with the
+// online softmax merge (running maximum and rescaled normaliser per tile) of
+// the page "Liger-Kernel内核级优化：FlashAttention与RollingBuffer详解".
+//
+// bf16 path (tensor cores), per chunk of C tokens (rows t0 .. t0+C):
+//   1. Z_c = X_c W^T on tcgen05; the epilogue never stores z: per 256-wide
+//      vocab tile it keeps the row max m and sum s of exp(z - m), writes
+//      P = exp(z - m) in bf16 to the [C x V] chunk buffer, and the logit at
+//      the label in fp32;
+//   2. one block per row merges the (m, s) of all vocab tiles into lse, the
+//      row's loss term, and rewrites P in place into the softmax part of D,
+//      S = scale * P * exp(m_tile - lse) (bf16);
+//   3. dX_c = S W on tcgen05 (W read MN-major); the epilogue subtracts the
+//      one-hot part, scale * W[label], in fp32; ignored rows written +0;
+//   4. dW (+)= S^T X_c on tcgen05 (both operands MN-major); the epilogue
+//      subtracts scale * X_t for the tokens labelled with the row (a sorted
+//      label list, binary-searched) in fp32, and accumulates across chunks in
+//      an fp32 [V x H] workspace, the last chunk writing W's dtype.
+// Keeping the one-hot term out of the bf16 operand matters: rounding
+// -scale to bf16 at every label would cost up to 2^-9 relative on the rows of
+// dW and dX that dominate their magnitude.
+// The full [T x V] logits never exist; per chunk only [C x V] bf16 does.
+//
+// fp32 path (and bf16 with H not a multiple of 8): the same steps with an
+// fp32 SIMT GEMM and an fp32 [C x V] chunk buffer holding z, then D.  TF32
+// tensor cores would miss the 1e-5 fp32 tolerance, so fp32 stays on FMA.
+#include <math.h>
+
+#include "tc_gemm.cuh"
+
+namespace liger {
+
+namespace {
+
+constexpr int kVT = tc::BN;   // vocab tile of the (m, s) partials
+constexpr int64_t kMaxChunkTC = 8192;   // tensor-core path: rows per chunk (label sort in one block)
+
+struct Hdr {
+    unsigned long long n_valid;
+    int bad;
+    int err;
+};
+
+struct Layout {
+    bool tc;
+    int64_t C, ldp, nvt, nchunks;
+    size_t lse, lossrow, zlab, hdr, keys, part, scr, acc, total;
+};
+
+inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+bool use_tc(int64_t H, int64_t V, int dtype) { return dtype == LIGER_BF16 && H % 8 == 0 && H >= 64 && V >= 256; }
+
+Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
+    Layout L{};
+    L.tc = use_tc(H, V, dtype);
+    int64_t C;
+    if (chunk > 0) C = chunk;
+    else if (L.tc) C = 4096;
+    else C = std::max<int64_t>(128, (int64_t{1} << 26) / std::max<int64_t>(V, 1));
+    if (L.tc) C = std::min<int64_t>(C, kMaxChunkTC);
+    C = std::max<int64_t>(1, std::min(C, std::max<int64_t>(T, 1)));
+    L.C = C;
+    L.nchunks = T > 0 ? ceil_div(T, C) : 0;
+    L.ldp = L.tc ? ((V + 7) / 8) * 8 : V;
+    L.nvt = ceil_div(V, kVT);
+    size_t o = 0;
+    L.lse = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
+    L.lossrow = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
+    L.zlab = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
+    L.hdr = o; o = up256(o + sizeof(Hdr));
+    L.keys = o; o = up256(o + (L.tc ? sizeof(unsigned long long) * static_cast<size_t>(C) : 0));
+    L.part = o; o = up256(o + (L.tc ? sizeof(float2) * static_cast<size_t>(C * L.nvt) : 0));
+    L.scr = o; o = up256(o + static_cast<size_t>(C) * static_cast<size_t>(L.ldp) * (L.tc ? 2 : 4));
+    const bool need_acc = L.nchunks > 1 && dtype == LIGER_BF16;
+    L.acc = o; o = up256(o + (need_acc ? sizeof(float) * static_cast<size_t>(V * H) : 0));
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------- kernels
+__global__ void label_scan(const int64_t* __restrict__ labels, int64_t T, int64_t V, int64_t ignore, Hdr* hdr) {
+    unsigned long long cnt = 0;
+    int bad = 0;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t y = labels[t];
+        if (y == ignore) continue;
+        ++cnt;
+        if (y < 0 || y >= V) bad = 1;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (cnt) atomicAdd(&hdr->n_valid, cnt);
+        if (bad) atomicOr(&hdr->bad, 1);
+    }
+}
+
+template <int NT>
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* sh) {
+    v = is_max ? warp_max(v) : warp_sum(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) sh[w] = v;
+    __syncthreads();
+    float r = is_max ? -INFINITY : 0.f;
+    for (int i = 0; i < NT / 32; ++i) r = is_max ? fmaxf(r, sh[i]) : r + sh[i];
+    return r;
+}
+
+// Sort the chunk's (label << 32 | row) keys (ignored rows -> ~0) in one block
+// (bitonic, in shared memory), for the one-hot correction of the dW epilogue.
+constexpr int kMaxSortKeys = 8192;
+__global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restrict__ labels, int n, int64_t ignore,
+                                                        int npow2, unsigned long long* __restrict__ out) {
+    extern __shared__ unsigned long long sk[];
+    for (int i = threadIdx.x; i < npow2; i += 1024) {
+        unsigned long long key = ~0ull;
+        if (i < n) {
+            const int64_t y = labels[i];
+            if (y != ignore) key = (static_cast<unsigned long long>(y) << 32) | static_cast<unsigned>(i);
+        }
+        sk[i] = key;
+    }
+    __syncthreads();
+    for (int k = 2; k <= npow2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < npow2; i += 1024) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const bool up = (i & k) == 0;
+                    const unsigned long long a = sk[i], b = sk[p];
+                    if ((a > b) == up) {
+                        sk[i] = b;
+                        sk[p] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < n; i += 1024) out[i] = sk[i];
+}
+
+// Merge the per-tile (m, s) of one chunk row into lse and rewrite P in place
+// into the softmax part of D, scale * P * exp(m_tile - lse) (the one-hot part
+// is applied exactly, in fp32, by the dX / dW GEMM epilogues).
+constexpr int kRowThreads = 256;
+__global__ void __launch_bounds__(kRowThreads) dlogits_bf16(const int64_t* __restrict__ labels, int64_t ignore,
+                                                            const float2* __restrict__ part, int nvt,
+                                                            const float* __restrict__ zlab, __nv_bfloat16* P,
+                                                            int64_t ldp, int V, float scale, float* __restrict__ lse,
+                                                            float* __restrict__ lossrow) {
+    extern __shared__ float fac[];   // [nvt]
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    const int64_t y = labels[row];
+    __nv_bfloat16* prow = P + row * ldp;
+    const int nv8 = (V + 7) / 8;
+    if (y == ignore) {
+        for (int k = threadIdx.x; k < nv8; k += kRowThreads) stg16(prow + static_cast<int64_t>(k) * 8, make_uint4(0, 0, 0, 0));
+        if (threadIdx.x == 0) {
+            lse[row] = 0.f;
+            lossrow[row] = 0.f;
+        }
+        return;
+    }
+    const float2* pr = part + row * nvt;
+    float m = -INFINITY;
+    for (int j = threadIdx.x; j < nvt; j += kRowThreads) m = fmaxf(m, pr[j].x);
+    m = block_reduce<kRowThreads>(m, true, red);
+    float s = 0.f;
+    for (int j = threadIdx.x; j < nvt; j += kRowThreads) {
+        const float2 p = pr[j];
+        s += p.y * expf(p.x - m);
+    }
+    s = block_reduce<kRowThreads>(s, false, red);
+    const float l = m + logf(s);
+    for (int j = threadIdx.x; j < nvt; j += kRowThreads) fac[j] = scale * expf(pr[j].x - l);
+    if (threadIdx.x == 0) {
+        lse[row] = l;
+        lossrow[row] = l - zlab[row];
+    }
+    __syncthreads();
+    for (int k = threadIdx.x; k < nv8; k += kRowThreads) {
+        const int col = k * 8;
+        const float f = fac[col / kVT];
+        float v[8];
+        unpack(ldg16(prow + col), v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] *= f;
+        stg16(prow + col, pack(v));
+    }
+}
+
+// fp32 path: z row -> lse, loss term, D (fp32, in place).
+__global__ void __launch_bounds__(kRowThreads) dlogits_f32(const int64_t* __restrict__ labels, int64_t ignore,
+                                                           float* Z, int64_t ldz, int V, float scale,
+                                                           float* __restrict__ lse, float* __restrict__ lossrow) {
+    __shared__ float red[32];
+    const int64_t row = blockIdx.x;
+    const int64_t y = labels[row];
+    float* z = Z + row * ldz;
+    if (y == ignore) {
+        for (int v = threadIdx.x; v < V; v += kRowThreads) z[v] = 0.f;
+        if (threadIdx.x == 0) {
+            lse[row] = 0.f;
+            lossrow[row] = 0.f;
+        }
+        return;
+    }
+    float m = -INFINITY;
+    for (int v = threadIdx.x; v < V; v += kRowThreads) m = fmaxf(m, z[v]);
+    m = block_reduce<kRowThreads>(m, true, red);
+    float s = 0.f;
+    for (int v = threadIdx.x; v < V; v += kRowThreads) s += expf(z[v] - m);
+    s = block_reduce<kRowThreads>(s, false, red);
+    const float l = m + logf(s);
+    const float zy = z[y];
+    __syncthreads();   // every thread has read z[y] before it is overwritten
+    if (threadIdx.x == 0) {
+        lse[row] = l;
+        lossrow[row] = l - zy;
+    }
+    for (int v = threadIdx.x; v < V; v += kRowThreads) z[v] = scale * (expf(z[v] - l) - (v == y ? 1.0f : 0.0f));
+}
+
+// loss = sum of the row terms (fixed order, fp64) / n_valid; NaN if a
+// tensor-core kernel recorded an error.
+__global__ void __launch_bounds__(1024) loss_final(const float* __restrict__ lossrow, int64_t T, double denom,
+                                                   const Hdr* hdr, float* loss) {
+    __shared__ double red[32];
+    double s = 0.0;
+    for (int64_t t = threadIdx.x; t < T; t += 1024) s += static_cast<double>(lossrow[t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int i = 0; i < 32; ++i) tot += red[i];
+        float r = denom > 0.0 ? static_cast<float>(tot / denom) : 0.0f;
+        if (hdr->err != 0) r = __int_as_float(0x7fc00000);
+        *loss = r;
+    }
+}
+
+// Generic SIMT GEMM, C[m, n] = sum_k A(m, k) B(k, n), fp32 accumulation.
+// A(m, k) = A[m*sam + k*sak], B(k, n) = B[k*sbk + n*sbn].
+//  mode 0: outf[m, n]  = acc          mode 2: outf[m, n] += acc
+//  mode 1: outT[m, n]  = acc          mode 3: outT[m, n]  = acc + outf[m, n]
+// mode 1 writes +0 on rows whose label is ignore_index (labels may be NULL).
+constexpr int SB = 64, SK = 16;
+template <typename TA, typename TB, typename TO, int MODE>
+__global__ void __launch_bounds__(256) simt_gemm(int M, int N, int K, const TA* __restrict__ A, int64_t sam,
+                                                 int64_t sak, const TB* __restrict__ B, int64_t sbk, int64_t sbn,
+                                                 float* outf, TO* outT, int64_t ldo, const int64_t* __restrict__ labels,
+                                                 int64_t ignore) {
+    __shared__ float As[SK][SB + 1], Bs[SK][SB + 1];
+    const int m0 = blockIdx.y * SB, n0 = blockIdx.x * SB;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < K; k0 += SK) {
+        for (int i = threadIdx.x; i < SB * SK; i += 256) {
+            const int mm = i / SK, kk = i % SK;
+            const int gm = m0 + mm, gk = k0 + kk;
+            As[kk][mm] = (gm < M && gk < K) ? ldf(A + gm * sam + gk * sak) : 0.f;
+            const int nn = i % SB, kb = i / SB;
+            const int gn = n0 + nn, gk2 = k0 + kb;
+            Bs[kb][nn] = (gn < N && gk2 < K) ? ldf(B + gk2 * sbk + gn * sbn) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int kk = 0; kk < SK; ++kk) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i], b[i] = Bs[kk][tx * 4 + i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int gm = m0 + ty * 4 + i;
+        if (gm >= M) continue;
+        const bool zero = MODE == 1 && labels != nullptr && labels[gm] == ignore;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int gn = n0 + tx * 4 + j;
+            if (gn >= N) continue;
+            const int64_t o = static_cast<int64_t>(gm) * ldo + gn;
+            if (MODE == 0) outf[o] = acc[i][j];
+            else if (MODE == 1) stf(outT + o, zero ? 0.f : acc[i][j]);
+            else if (MODE == 2) outf[o] += acc[i][j];
+            else stf(outT + o, acc[i][j] + outf[o]);
+        }
+    }
+}
+
+template <typename TA, typename TB, typename TO, int MODE>
+int simt(int M, int N, int K, const TA* A, int64_t sam, int64_t sak, const TB* B, int64_t sbk, int64_t sbn,
+         float* outf, TO* outT, int64_t ldo, const int64_t* labels, int64_t ignore, cudaStream_t st) {
+    if (M == 0 || N == 0) return LIGER_OK;
+    dim3 grid(static_cast<unsigned>(ceil_div(N, SB)), static_cast<unsigned>(ceil_div(M, SB)));
+    if (grid.y > 65535) return fail(LIGER_ERR_SHAPE, "linear_ce: SIMT grid too large");
+    simt_gemm<TA, TB, TO, MODE><<<grid, 256, 0, st>>>(M, N, K, A, sam, sak, B, sbk, sbn, outf, outT, ldo, labels,
+                                                      ignore);
+    return check_launch("simt_gemm");
+}
+
+// ----------------------------------------------------------- orchestration
+struct Args {
+    const void* X;
+    const void* W;
+    const int64_t* labels;
+    int64_t T, H, V, ignore;
+    int reduction;
+    float grad_scale;
+    float* loss;
+    void* dX;
+    void* dW;
+    uint8_t* ws;
+    int dtype;
+    cudaStream_t st;
+};
+
+template <typename TI>
+int run_simt(const Args& a, const Layout& L, float scale) {
+    const TI* X = static_cast<const TI*>(a.X);
+    const TI* W = static_cast<const TI*>(a.W);
+    TI* dX = static_cast<TI*>(a.dX);
+    TI* dW = static_cast<TI*>(a.dW);
+    float* lse = reinterpret_cast<float*>(a.ws + L.lse);
+    float* lossrow = reinterpret_cast<float*>(a.ws + L.lossrow);
+    float* Z = reinterpret_cast<float*>(a.ws + L.scr);
+    float* acc = reinterpret_cast<float*>(a.ws + L.acc);
+    const bool f32 = a.dtype == LIGER_F32;
+    const int H = static_cast<int>(a.H), V = static_cast<int>(a.V);
+    int rc;
+    for (int64_t c = 0; c < L.nchunks; ++c) {
+        const int64_t t0 = c * L.C;
+        const int cl = static_cast<int>(std::min(L.C, a.T - t0));
+        const bool first = c == 0, last = c == L.nchunks - 1;
+        if ((rc = simt<TI, TI, TI, 0>(cl, V, H, X + t0 * H, H, 1, W, 1, H, Z, (TI*)nullptr, V, nullptr, 0, a.st)))
+            return rc;
+        dlogits_f32<<<cl, kRowThreads, 0, a.st>>>(a.labels + t0, a.ignore, Z, V, V, scale, lse + t0, lossrow + t0);
+        if ((rc = check_launch("dlogits_f32"))) return rc;
+        if (dX && (rc = simt<float, TI, TI, 1>(cl, H, V, Z, V, 1, W, H, 1, nullptr, dX + t0 * H, H, a.labels + t0,
+                                               a.ignore, a.st)))
+            return rc;
+        if (dW) {
+            const TI* Xc = X + t0 * H;
+            if (f32) {
+                float* dWf = reinterpret_cast<float*>(dW);
+                rc = first ? simt<float, TI, float, 0>(V, H, cl, Z, 1, V, Xc, H, 1, dWf, nullptr, H, nullptr, 0, a.st)
+                           : simt<float, TI, float, 2>(V, H, cl, Z, 1, V, Xc, H, 1, dWf, nullptr, H, nullptr, 0, a.st);
+            } else if (first && last) {
+                rc = simt<float, TI, TI, 1>(V, H, cl, Z, 1, V, Xc, H, 1, nullptr, dW, H, nullptr, 0, a.st);
+            } else if (first) {
+                rc = simt<float, TI, TI, 0>(V, H, cl, Z, 1, V, Xc, H, 1, acc, nullptr, H, nullptr, 0, a.st);
+            } else if (!last) {
+                rc = simt<float, TI, TI, 2>(V, H, cl, Z, 1, V, Xc, H, 1, acc, nullptr, H, nullptr, 0, a.st);
+            } else {
+                rc = simt<float, TI, TI, 3>(V, H, cl, Z, 1, V, Xc, H, 1, acc, dW, H, nullptr, 0, a.st);
+            }
+            if (rc) return rc;
+        }
+    }
+    return LIGER_OK;
+}
+
+int run_tc(const Args& a, const Layout& L, float scale) {
+    using namespace tc;
+    static bool sort_attr = false;
+    if (!sort_attr) {
+        if (cudaFuncSetAttribute(sort_label_keys, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(sizeof(unsigned long long) * kMaxSortKeys)) != cudaSuccess)
+            return check_launch("sort_label_keys attribute");
+        sort_attr = true;
+    }
+    const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(a.X);
+    const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(a.W);
+    float* lse = reinterpret_cast<float*>(a.ws + L.lse);
+    float* lossrow = reinterpret_cast<float*>(a.ws + L.lossrow);
+    float* zlab = reinterpret_cast<float*>(a.ws + L.zlab);
+    Hdr* hdr = reinterpret_cast<Hdr*>(a.ws + L.hdr);
+    float2* part = reinterpret_cast<float2*>(a.ws + L.part);
+    __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(a.ws + L.scr);
+    float* acc = reinterpret_cast<float*>(a.ws + L.acc);
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(a.ws + L.keys);
+    const int H = static_cast<int>(a.H), V = static_cast<int>(a.V);
+    int rc;
+    CUtensorMap mW_k, mW_mn;
+    if ((rc = make_map(&mW_k, W, H, V, H, BK, BN))) return rc;          // B of Z = X W^T  (K-major)
+    if ((rc = make_map(&mW_mn, W, H, V, H, MN_BOX, BK))) return rc;     // B of dX = D W   (MN-major)
+    const size_t fac_smem = sizeof(float) * static_cast<size_t>(L.nvt);
+    for (int64_t c = 0; c < L.nchunks; ++c) {
+        const int64_t t0 = c * L.C;
+        const int cl = static_cast<int>(std::min(L.C, a.T - t0));
+        const bool first = c == 0, last = c == L.nchunks - 1;
+        const __nv_bfloat16* Xc = X + t0 * H;
+        CUtensorMap mX_k, mX_mn, mD_k, mD_mn;
+        if ((rc = make_map(&mX_k, Xc, H, cl, H, BK, BM))) return rc;     // A of Z (K-major)
+        if ((rc = make_map(&mX_mn, Xc, H, cl, H, MN_BOX, BK))) return rc;  // B of dW (MN-major)
+        if ((rc = make_map(&mD_k, P, V, cl, L.ldp, BK, BM))) return rc;  // A of dX (K-major)
+        if ((rc = make_map(&mD_mn, P, V, cl, L.ldp, MN_BOX, BK))) return rc;  // A of dW (MN-major)
+
+        EpiParams e{};
+        e.err = &hdr->err;
+        e.ignore_index = a.ignore;
+        e.labels = a.labels + t0;
+        // 1. logits -> P, (m, s) partials, z at label
+        e.M = cl;
+        e.N = V;
+        e.raster_n_fastest = 0;
+        e.p_out = P;
+        e.ldp = L.ldp;
+        e.part = part;
+        e.nvt = static_cast<int>(L.nvt);
+        e.zlab = zlab + t0;
+        if ((rc = launch_gemm<0, 0, EPI_LOGITS>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
+        // 2. lse, loss terms, P -> D in place
+        dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
+                                                          zlab + t0, P, L.ldp, V, scale, lse + t0, lossrow + t0);
+        if ((rc = check_launch("dlogits_bf16"))) return rc;
+        // 3. dX_c = D W, minus scale * W[label] in fp32
+        if (a.dX) {
+            EpiParams d = e;
+            d.M = cl;
+            d.N = H;
+            d.out = static_cast<__nv_bfloat16*>(a.dX) + t0 * H;
+            d.ldo = H;
+            d.corr_src = W;
+            d.ld_corr = H;
+            d.corr_scale = scale;
+            if ((rc = launch_gemm<0, 1, EPI_STORE>(mD_k, mW_mn, cl, H, V, d, a.st))) return rc;
+        }
+        // 4. dW (+)= D^T X_c, minus scale * X_t in fp32 for each token t labelled with the row
+        if (a.dW) {
+            int npow2 = 1;
+            while (npow2 < cl) npow2 <<= 1;
+            sort_label_keys<<<1, 1024, sizeof(unsigned long long) * npow2, a.st>>>(a.labels + t0, cl, a.ignore, npow2,
+                                                                                    keys);
+            if ((rc = check_launch("sort_label_keys"))) return rc;
+            EpiParams d = e;
+            d.corr_src = Xc;
+            d.ld_corr = H;
+            d.corr_scale = scale;
+            d.keys = keys;
+            d.nkeys = cl;
+            d.M = V;
+            d.N = H;
+            d.raster_n_fastest = 1;
+            d.labels = nullptr;
+            d.acc = acc;
+            d.lda = H;
+            d.out = static_cast<__nv_bfloat16*>(a.dW);
+            d.ldo = H;
+            d.acc_read = first ? 0 : 1;
+            d.acc_write = last ? 0 : 1;
+            d.out_write = last ? 1 : 0;
+            if ((rc = launch_gemm<1, 1, EPI_ACCUM>(mD_mn, mX_mn, V, H, cl, d, a.st))) return rc;
+        }
+    }
+    return LIGER_OK;
+}
+
+}  // namespace
+}  // namespace liger
+
+using namespace liger;
+
+extern "C" size_t liger_linear_ce_workspace(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
+    if (T < 0 || H <= 0 || V <= 0 || chunk < 0 || (dtype != LIGER_F32 && dtype != LIGER_BF16)) return 0;
+    return layout(T, H, V, chunk, dtype).total;
+}
+
+extern "C" int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H,
+                                       int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
+                                       void* dX, void* dW, void* ws, size_t ws_bytes, int64_t chunk, int dtype,
+                                       void* stream) {
+    clear_error();
+    if (dtype != LIGER_F32 && dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "linear_ce: dtype %d", dtype);
+    if (T < 0 || H <= 0 || V <= 0 || chunk < 0 || H > (1 << 30) || V > (1 << 30) || T > (int64_t{1} << 31) ||
+        (reduction != 0 && reduction != 1))
+        return fail(LIGER_ERR_SHAPE, "linear_ce: T=%lld H=%lld V=%lld chunk=%lld reduction=%d", (long long)T,
+                    (long long)H, (long long)V, (long long)chunk, reduction);
+    if (!X || !W || !loss || (T > 0 && !labels)) return fail(LIGER_ERR_NULL, "linear_ce: X, W, labels, loss required");
+    if (!aligned16(X) || !aligned16(W) || (dX && !aligned16(dX)) || (dW && !aligned16(dW)) ||
+        (reinterpret_cast<uintptr_t>(loss) & 3) || (reinterpret_cast<uintptr_t>(labels) & 7))
+        return fail(LIGER_ERR_ALIGN, "linear_ce: X, W, dX, dW must be 16-byte aligned");
+    const Layout L = layout(T, H, V, chunk, dtype);
+    if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255))
+        return fail(LIGER_ERR_WORKSPACE, "linear_ce: workspace of %zu bytes (256-byte aligned) required, got %zu",
+                    L.total, ws_bytes);
+    cudaStream_t st = as_stream(stream);
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
+    Hdr* hdr = reinterpret_cast<Hdr*>(w8 + L.hdr);
+    if (cudaMemsetAsync(hdr, 0, sizeof(Hdr), st) != cudaSuccess) return check_launch("linear_ce memset");
+    Hdr h{};
+    if (T > 0) {
+        const int grid = static_cast<int>(std::min<int64_t>(ceil_div(T, 256), 4 * sm_count()));
+        label_scan<<<grid, 256, 0, st>>>(labels, T, V, ignore_index, hdr);
+        if (int rc = check_launch("label_scan")) return rc;
+        if (cudaMemcpyAsync(&h, hdr, sizeof(Hdr), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return check_launch("linear_ce label scan");
+        if (h.bad) return fail(LIGER_ERR_LABEL, "linear_ce: a label is outside [0, %lld) and is not %lld", (long long)V,
+                               (long long)ignore_index);
+    }
+    const int64_t n_valid = static_cast<int64_t>(h.n_valid);
+    const size_t esz = dtype == LIGER_F32 ? 4 : 2;
+    if (n_valid == 0) {
+        // nothing to learn from: loss 0, zero gradients (PyTorch would give NaN for the mean)
+        bool ok = cudaMemsetAsync(loss, 0, sizeof(float), st) == cudaSuccess;
+        if (dX) ok = ok && cudaMemsetAsync(dX, 0, static_cast<size_t>(T * H) * esz, st) == cudaSuccess;
+        if (dW) ok = ok && cudaMemsetAsync(dW, 0, static_cast<size_t>(V * H) * esz, st) == cudaSuccess;
+        if (T > 0) ok = ok && cudaMemsetAsync(w8 + L.lse, 0, sizeof(float) * static_cast<size_t>(T), st) == cudaSuccess;
+        if (T > 0) ok = ok && cudaMemsetAsync(w8 + L.lossrow, 0, sizeof(float) * static_cast<size_t>(T), st) == cudaSuccess;
+        return ok ? LIGER_OK : check_launch("linear_ce memset");
+    }
+    const float scale = reduction == 0 ? static_cast<float>(static_cast<double>(grad_scale) / static_cast<double>(n_valid))
+                                       : grad_scale;
+    Args a{X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st};
+    int rc;
+    if (L.tc) rc = run_tc(a, L, scale);
+    else if (dtype == LIGER_F32) rc = run_simt<float>(a, L, scale);
+    else rc = run_simt<__nv_bfloat16>(a, L, scale);
+    if (rc) return rc;
+    const double denom = reduction == 0 ? static_cast<double>(n_valid) : 1.0;
+    loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + L.lossrow), T, denom, hdr, loss);
+    return check_launch("loss_final");
+}

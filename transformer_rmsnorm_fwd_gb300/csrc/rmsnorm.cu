@@ -1,0 +1,373 @@
+// RMSNorm forward and backward.
+//
+// Operator: the RMSNorm step of the fused RMSNorm + QKV + RoPE kernel on the
+// page "Liger-Kernel底层优化：新一代内核级推理加速引擎介绍", section
+// "融合内核是如何工作的？来看一段简化版实现": rstd = 1/sqrt(mean(x^2) + eps),
+// y = x * rstd * w.  The backward is the derivative of that forward.
+//
+// GB300 design (HBM-bound, ~2 bytes/element each way in bf16):
+//  * forward: one warp per row, the row held in registers as 16-byte
+//    vectors (VPL vectors per lane), w held in registers across rows, one
+//    warp-shuffle reduction, no shared memory and no block barrier; a
+//    persistent grid of (SMs x resident blocks) warps strides over rows.
+//  * backward: one block per contiguous group of rows; each thread owns
+//    fixed columns and keeps its share of dw in fp32 registers across the
+//    group's rows (no atomics); the row dot product is a shuffle + one
+//    barrier (double-buffered shared slots); the next row is prefetched while
+//    the current one is reduced.  Per-block dw partials go to the workspace
+//    and a second kernel sums them in a fixed order, so dw is deterministic.
+#include "common.cuh"
+
+namespace liger {
+namespace {
+
+constexpr int kFwdThreads = 256;
+constexpr int kMaxPartials = 1024;
+
+template <typename T, int VPL>
+__global__ void __launch_bounds__(kFwdThreads) rmsnorm_fwd_warp(const T* x, const T* __restrict__ w, T* y,
+                                                                 float* __restrict__ rstd, int64_t rows, int cols,
+                                                                 float eps) {
+    constexpr int EPV = Vec<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int nvec = cols / EPV;
+    uint4 wv[VPL];
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+        const int v = j * 32 + lane;
+        wv[j] = v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0);
+    }
+    const float inv_cols = 1.0f / static_cast<float>(cols);
+    for (int64_t r = warp0; r < rows; r += nwarps) {
+        const T* xr = x + r * cols;
+        uint4 xv[VPL];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int v = j * 32 + lane;
+            xv[j] = v < nvec ? ldg16(xr + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0);
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            float f[EPV];
+            unpack(xv[j], f);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+        ss = warp_sum(ss);
+        const float rs = 1.0f / sqrtf(ss * inv_cols + eps);
+        T* yr = y + r * cols;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int v = j * 32 + lane;
+            if (v < nvec) {
+                float f[EPV], g[EPV];
+                unpack(xv[j], f);
+                unpack(wv[j], g);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) f[e] = (f[e] * rs) * g[e];
+                stg16(yr + static_cast<int64_t>(v) * EPV, pack(f));
+            }
+        }
+        if (rstd != nullptr && lane == 0) rstd[r] = rs;
+    }
+}
+
+// Any cols (scalar, two passes over the row): one block per row.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_generic(const T* x, const T* __restrict__ w, T* y,
+                                                           float* __restrict__ rstd, int64_t rows, int cols,
+                                                           float eps) {
+    __shared__ float red[32];
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const T* xr = x + r * cols;
+        float ss = 0.f;
+        for (int j = threadIdx.x; j < cols; j += blockDim.x) {
+            const float f = ldf(xr + j);
+            ss = fmaf(f, f, ss);
+        }
+        ss = warp_sum(ss);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+        const float rs = 1.0f / sqrtf(tot / static_cast<float>(cols) + eps);
+        T* yr = y + r * cols;
+        for (int j = threadIdx.x; j < cols; j += blockDim.x) stf(yr + j, (ldf(xr + j) * rs) * ldf(w + j));
+        if (rstd != nullptr && threadIdx.x == 0) rstd[r] = rs;
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ bwd
+template <typename T, int VPT>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_block(const T* dy, const T* __restrict__ x,
+                                                         const T* __restrict__ w, const float* __restrict__ rstd,
+                                                         T* dx, float* __restrict__ part, int64_t rows, int cols,
+                                                         int64_t rows_per_block) {
+    constexpr int EPV = Vec<T>::N;
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, wid = tid >> 5, NW = NT >> 5;
+    const int nvec = cols / EPV;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per_block;
+    const int64_t r1 = min(rows, r0 + rows_per_block);
+    uint4 wv[VPT];
+    float dwa[VPT][EPV];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = j * NT + tid;
+        wv[j] = v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) dwa[j][e] = 0.f;
+    }
+    const float inv_cols = 1.0f / static_cast<float>(cols);
+    uint4 nx[VPT], ndy[VPT];
+    float nrs = 0.f;
+    auto fetch = [&](int64_t r) {
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = j * NT + tid;
+            const int64_t off = r * cols + static_cast<int64_t>(v) * EPV;
+            nx[j] = v < nvec ? ldg16(x + off) : make_uint4(0, 0, 0, 0);
+            ndy[j] = v < nvec ? ldg16(dy + off) : make_uint4(0, 0, 0, 0);
+        }
+        nrs = rstd[r];
+    };
+    if (r0 < r1) fetch(r0);
+    for (int64_t r = r0; r < r1; ++r) {
+        uint4 cx[VPT], cdy[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            cx[j] = nx[j];
+            cdy[j] = ndy[j];
+        }
+        const float rs = nrs;
+        if (r + 1 < r1) fetch(r + 1);
+        float gx = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            float fx[EPV], fd[EPV], fw[EPV];
+            unpack(cx[j], fx);
+            unpack(cdy[j], fd);
+            unpack(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) gx = fmaf(fd[e] * fw[e], fx[e], gx);
+        }
+        gx = warp_sum(gx);
+        if (lane == 0) red[r & 1][wid] = gx;
+        __syncthreads();
+        float tot = 0.f;
+        for (int i = 0; i < NW; ++i) tot += red[r & 1][i];
+        const float c = rs * rs * rs * inv_cols * tot;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = j * NT + tid;
+            if (v < nvec) {
+                float fx[EPV], fd[EPV], fw[EPV], o[EPV];
+                unpack(cx[j], fx);
+                unpack(cdy[j], fd);
+                unpack(wv[j], fw);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    o[e] = rs * (fd[e] * fw[e]) - c * fx[e];
+                    dwa[j][e] = fmaf(fd[e] * fx[e], rs, dwa[j][e]);
+                }
+                stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, pack(o));
+            }
+        }
+    }
+    float* pr = part + static_cast<int64_t>(blockIdx.x) * cols;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = j * NT + tid;
+        if (v < nvec) {
+#pragma unroll
+            for (int e = 0; e < EPV; e += 4) {
+                float q[4] = {dwa[j][e], dwa[j][e + 1], dwa[j][e + 2], dwa[j][e + 3]};
+                stg16(pr + static_cast<int64_t>(v) * EPV + e, pack(q));
+            }
+        }
+    }
+}
+
+// Any cols (scalar): one block per row group, partial dw accumulated in the
+// block's own workspace row (no other block touches it).
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_generic(const T* dy, const T* __restrict__ x,
+                                                           const T* __restrict__ w, const float* __restrict__ rstd,
+                                                           T* dx, float* __restrict__ part, int64_t rows, int cols,
+                                                           int64_t rows_per_block) {
+    __shared__ float red[32];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per_block;
+    const int64_t r1 = min(rows, r0 + rows_per_block);
+    float* pr = part + static_cast<int64_t>(blockIdx.x) * cols;
+    for (int j = threadIdx.x; j < cols; j += blockDim.x) pr[j] = 0.f;
+    for (int64_t r = r0; r < r1; ++r) {
+        const float rs = rstd[r];
+        float gx = 0.f;
+        for (int j = threadIdx.x; j < cols; j += blockDim.x)
+            gx = fmaf(ldf(dy + r * cols + j) * ldf(w + j), ldf(x + r * cols + j), gx);
+        gx = warp_sum(gx);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = gx;
+        __syncthreads();
+        float tot = 0.f;
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) tot += red[i];
+        const float c = rs * rs * rs / static_cast<float>(cols) * tot;
+        for (int j = threadIdx.x; j < cols; j += blockDim.x) {
+            const float fx = ldf(x + r * cols + j), fd = ldf(dy + r * cols + j);
+            stf(dx + r * cols + j, rs * (fd * ldf(w + j)) - c * fx);
+            pr[j] = fmaf(fd * fx, rs, pr[j]);
+        }
+        __syncthreads();
+    }
+}
+
+// dw[j] = sum_b part[b, j] in ascending b: 8 slices of the partial rows per
+// 32 columns, combined in slice order.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_dw_reduce(const float* __restrict__ part, T* __restrict__ dw,
+                                                         int nparts, int cols) {
+    __shared__ float red[8][33];
+    const int cl = threadIdx.x & 31, sl = threadIdx.x >> 5;
+    const int col = blockIdx.x * 32 + cl;
+    const int per = (nparts + 7) / 8;
+    const int b0 = sl * per, b1 = min(nparts, b0 + per);
+    float s = 0.f;
+    if (col < cols)
+        for (int b = b0; b < b1; ++b) s += part[static_cast<int64_t>(b) * cols + col];
+    red[sl][cl] = s;
+    __syncthreads();
+    if (sl == 0 && col < cols) {
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t += red[i][cl];
+        stf(dw + col, t);
+    }
+}
+
+template <typename T>
+int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows, int cols, float eps,
+               cudaStream_t st) {
+    constexpr int EPV = Vec<T>::N;
+    const T* xp = static_cast<const T*>(x);
+    const T* wp = static_cast<const T*>(w);
+    T* yp = static_cast<T*>(y);
+    const int sms = sm_count();
+    if (cols % EPV == 0) {
+        const int nvec = cols / EPV;
+        const int64_t need_blocks = ceil_div(rows, kFwdThreads / 32);
+        auto go = [&](auto kern) {
+            int per_sm = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFwdThreads, 0);
+            if (per_sm < 1) per_sm = 1;
+            const int64_t grid = std::min<int64_t>(need_blocks, static_cast<int64_t>(sms) * per_sm);
+            kern<<<static_cast<unsigned>(grid), kFwdThreads, 0, st>>>(xp, wp, yp, rstd, rows, cols, eps);
+            return check_launch("rmsnorm_fwd");
+        };
+        if (nvec <= 32) return go(rmsnorm_fwd_warp<T, 1>);
+        if (nvec <= 64) return go(rmsnorm_fwd_warp<T, 2>);
+        if (nvec <= 128) return go(rmsnorm_fwd_warp<T, 4>);
+        if (nvec <= 256) return go(rmsnorm_fwd_warp<T, 8>);
+        if (nvec <= 512) return go(rmsnorm_fwd_warp<T, 16>);
+        if (nvec <= 1024) return go(rmsnorm_fwd_warp<T, 32>);
+    }
+    const int64_t grid = std::min<int64_t>(rows, static_cast<int64_t>(sms) * 8);
+    rmsnorm_fwd_generic<T><<<static_cast<unsigned>(grid), 256, 0, st>>>(xp, wp, yp, rstd, rows, cols, eps);
+    return check_launch("rmsnorm_fwd_generic");
+}
+
+int64_t bwd_partials(int64_t rows) {
+    return std::max<int64_t>(1, std::min<int64_t>({rows, static_cast<int64_t>(sm_count()) * 4, kMaxPartials}));
+}
+
+template <typename T>
+int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, void* dx, void* dw, float* part,
+               int64_t rows, int cols, cudaStream_t st) {
+    constexpr int EPV = Vec<T>::N;
+    const int64_t P = bwd_partials(rows);
+    const int64_t rpb = ceil_div(rows, P);
+    const int64_t grid = ceil_div(rows, rpb);
+    const T* dyp = static_cast<const T*>(dy);
+    const T* xp = static_cast<const T*>(x);
+    const T* wp = static_cast<const T*>(w);
+    T* dxp = static_cast<T*>(dx);
+    bool done = false;
+    if (cols % EPV == 0) {
+        const int nvec = cols / EPV;
+        auto go = [&](auto kern, int vpt) {
+            const int nt = static_cast<int>(std::min<int64_t>(256, ceil_div(ceil_div(nvec, vpt), 32) * 32));
+            kern<<<static_cast<unsigned>(grid), nt, 0, st>>>(dyp, xp, wp, rstd, dxp, part, rows, cols, rpb);
+            done = true;
+        };
+        if (nvec <= 256) go(rmsnorm_bwd_block<T, 1>, 1);
+        else if (nvec <= 512) go(rmsnorm_bwd_block<T, 2>, 2);
+        else if (nvec <= 1024) go(rmsnorm_bwd_block<T, 4>, 4);
+        else if (nvec <= 2048) go(rmsnorm_bwd_block<T, 8>, 8);
+    }
+    if (!done)
+        rmsnorm_bwd_generic<T><<<static_cast<unsigned>(grid), 256, 0, st>>>(dyp, xp, wp, rstd, dxp, part, rows, cols,
+                                                                            rpb);
+    int rc = check_launch("rmsnorm_bwd");
+    if (rc) return rc;
+    rmsnorm_dw_reduce<T><<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, st>>>(
+        part, static_cast<T*>(dw), static_cast<int>(grid), cols);
+    return check_launch("rmsnorm_dw_reduce");
+}
+
+int check_common(int64_t rows, int64_t cols, int dtype) {
+    if (dtype != LIGER_F32 && dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "rmsnorm: dtype %d", dtype);
+    if (rows < 0 || cols <= 0 || cols > (1 << 30))
+        return fail(LIGER_ERR_SHAPE, "rmsnorm: rows=%lld cols=%lld", (long long)rows, (long long)cols);
+    return LIGER_OK;
+}
+
+}  // namespace
+}  // namespace liger
+
+using namespace liger;
+
+extern "C" int liger_rmsnorm_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows, int64_t cols,
+                                 float eps, int dtype, void* stream) {
+    clear_error();
+    if (int rc = check_common(rows, cols, dtype)) return rc;
+    if (rows == 0) return LIGER_OK;
+    if (!x || !w || !y) return fail(LIGER_ERR_NULL, "rmsnorm_fwd: x, w and y are required");
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (rstd && (reinterpret_cast<uintptr_t>(rstd) & 3)))
+        return fail(LIGER_ERR_ALIGN, "rmsnorm_fwd: tensors must be 16-byte aligned");
+    if (!(eps >= 0.f)) return fail(LIGER_ERR_SHAPE, "rmsnorm_fwd: eps must be >= 0");
+    cudaStream_t st = as_stream(stream);
+    return dtype == LIGER_F32 ? launch_fwd<float>(x, w, y, rstd, rows, (int)cols, eps, st)
+                              : launch_fwd<__nv_bfloat16>(x, w, y, rstd, rows, (int)cols, eps, st);
+}
+
+extern "C" size_t liger_rmsnorm_bwd_workspace(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return static_cast<size_t>(std::min<int64_t>(rows, kMaxPartials)) * static_cast<size_t>(cols) * sizeof(float);
+}
+
+extern "C" int liger_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float* rstd, void* dx, void* dw,
+                                 void* ws, size_t ws_bytes, int64_t rows, int64_t cols, int dtype, void* stream) {
+    clear_error();
+    if (int rc = check_common(rows, cols, dtype)) return rc;
+    if (!dw || (rows > 0 && (!dy || !x || !w || !dx || !rstd)))
+        return fail(LIGER_ERR_NULL, "rmsnorm_bwd: dy, x, w, rstd, dx and dw are required");
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(w) || !aligned16(dx) || !aligned16(dw) ||
+        (reinterpret_cast<uintptr_t>(rstd) & 3))
+        return fail(LIGER_ERR_ALIGN, "rmsnorm_bwd: tensors must be 16-byte aligned");
+    const size_t need = liger_rmsnorm_bwd_workspace(rows, cols);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+        return fail(LIGER_ERR_WORKSPACE, "rmsnorm_bwd: workspace of %zu bytes (16-byte aligned) required, got %zu",
+                    need, ws_bytes);
+    cudaStream_t st = as_stream(stream);
+    if (rows == 0) {
+        // dw of an empty batch is zero
+        const size_t bytes = static_cast<size_t>(cols) * (dtype == LIGER_F32 ? 4 : 2);
+        if (cudaMemsetAsync(dw, 0, bytes, st) != cudaSuccess) return check_launch("rmsnorm_bwd memset");
+        return LIGER_OK;
+    }
+    float* part = static_cast<float*>(ws);
+    return dtype == LIGER_F32 ? launch_bwd<float>(dy, x, w, rstd, dx, dw, part, rows, (int)cols, st)
+                              : launch_bwd<__nv_bfloat16>(dy, x, w, rstd, dx, dw, part, rows, (int)cols, st);
+}

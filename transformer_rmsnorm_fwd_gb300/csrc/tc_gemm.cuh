@@ -1,0 +1,578 @@
+// Persistent, warp-specialised bf16 GEMM on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA) for sm_103a, with the fused epilogues of the linear
+// cross-entropy.
+//
+//   C[m, n] = sum_k A(m, k) * B(n, k)        (bf16 x bf16 -> fp32 in TMEM)
+//
+// A and B are each read by TMA in 128-byte-swizzled tiles, either K-major
+// (K contiguous) or MN-major (M / N contiguous); the layout is a template
+// parameter and becomes the operand-major bits of the MMA instruction
+// descriptor and the LBO / SBO of the shared-memory descriptors.
+//
+// Block = 6 warps, one block per SM (the 4-stage ring takes ~193 KB of
+// shared memory):
+//   warp 0      TMA producer (one lane): A/B tiles into a 4-stage ring;
+//   warp 1      TMEM owner and MMA issuer (one lane): 4 x tcgen05.mma
+//               (M=128, N=256, K=16) per 64-wide k-block, tcgen05.commit
+//               frees the ring slot, a second commit hands the accumulator
+//               to the epilogue;
+//   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane),
+//               reads it with tcgen05.ld 32 columns at a time and applies the
+//               fused epilogue; the accumulator is double-buffered in TMEM
+//               (2 x 256 columns) so tile i's epilogue overlaps tile i+1's
+//               MMAs.
+// Every mbarrier wait is bounded (about 4 s of %globaltimer); on expiry the
+// waiting role records an error code in *ep.err, stops issuing work, waits
+// (bounded) for the copies and MMAs it already issued, and the block frees
+// its TMEM and exits.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace liger {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;          // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX = 64;      // MN-major TMA box: 64 (MN) x 64 (K) = 8 KB
+constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr unsigned long long WAIT_NS = 4000000000ull;
+
+enum Epi : int { EPI_LOGITS = 0, EPI_STORE = 1, EPI_ACCUM = 2 };
+
+enum Err : int { ERR_TMA_EMPTY = 1, ERR_MMA_FULL = 2, ERR_MMA_TMEM = 3, ERR_EPI_TMEM = 4 };
+
+struct EpiParams {
+    int M, N;                           // logical problem size (epilogue masks)
+    int raster_n_fastest;               // tile order: 0 = m fastest, 1 = n fastest
+    int* err;                           // error word (device)
+    // EPI_LOGITS: P = exp(z - m_tile) as bf16, per-(row, n-tile) (m, sum), z at label
+    const int64_t* labels;              // [M] (chunk rows)
+    int64_t ignore_index;
+    __nv_bfloat16* p_out;
+    int64_t ldp;
+    float2* part;
+    int nvt;
+    float* zlab;                        // [M]
+    // EPI_STORE: bf16 out [M, N] (ldo), rows with label == ignore_index -> +0
+    __nv_bfloat16* out;
+    int64_t ldo;
+    // EPI_ACCUM: fp32 accumulator acc [M, N] (lda); flags
+    float* acc;
+    int64_t lda;
+    int acc_read, acc_write, out_write;
+    // one-hot correction applied in fp32 (the bf16 operand carries only the
+    // softmax part): EPI_STORE subtracts corr_scale * corr_src[labels[row], :];
+    // EPI_ACCUM subtracts corr_scale * corr_src[t, :] for every token t whose
+    // label is this row, found in keys[0, nkeys) = sorted (label << 32 | t).
+    const __nv_bfloat16* corr_src;
+    int64_t ld_corr;
+    float corr_scale;
+    const unsigned long long* keys;
+    int nkeys;
+};
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded wait for phase `parity` of barrier `bar`: false after WAIT_NS.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 256; ++i)
+            if (mbar_try(bar, parity)) return true;
+        if (globaltimer() - t0 > WAIT_NS) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading
+// and stride byte offsets (>> 4), version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, dense.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+           (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(m >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// v[0..32) -= s * src[0..32) over the 8-column groups that start below n_left
+__device__ __forceinline__ void sub_scaled32(float (&v)[32], const __nv_bfloat16* src, float s, int n_left) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (g * 8 < n_left) {
+            float f[8];
+            unpack(ldg16(src + g * 8), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[g * 8 + e] = fmaf(-s, f[e], v[g * 8 + e]);
+        }
+    }
+}
+
+__device__ __forceinline__ int lower_bound_u64(const unsigned long long* a, int n, unsigned long long key) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] < key) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+// --------------------------------------------------------------- kernel
+template <int A_MN, int B_MN, int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+                   int K, EpiParams ep) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    const uint32_t slot = bar0 + 8u * (2 * STAGES + 4);
+    uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 4));
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+    const int ntiles = num_m * num_n;
+    const int nkb = (K + BK - 1) / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        prefetch_map(&tmA);
+        prefetch_map(&tmB);
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(slot_ptr);
+
+    auto tile_mn = [&](int t, int& mi, int& ni) {
+        if (ep.raster_n_fastest) {
+            mi = t / num_n;
+            ni = t - mi * num_n;
+        } else {
+            ni = t / num_m;
+            mi = t - ni * num_m;
+        }
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_phase[STAGES];
+            bool issued[STAGES];
+            for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                int mi, ni;
+                tile_mn(t, mi, ni);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u)) {
+                        atomicExch(ep.err, ERR_TMA_EMPTY);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t fb = full_bar(stage);
+                    mbar_expect_tx(fb, STAGE_BYTES);
+                    if (A_MN) {
+#pragma unroll
+                        for (int j = 0; j < BM / MN_BOX; ++j)
+                            tma_load_2d(sa + j * MN_BOX_BYTES, &tmA, fb, mi * BM + j * MN_BOX, kb * BK);
+                    } else {
+                        tma_load_2d(sa, &tmA, fb, kb * BK, mi * BM);
+                    }
+                    if (B_MN) {
+#pragma unroll
+                        for (int j = 0; j < BN / MN_BOX; ++j)
+                            tma_load_2d(sb + j * MN_BOX_BYTES, &tmB, fb, ni * BN + j * MN_BOX, kb * BK);
+                    } else {
+                        tma_load_2d(sb, &tmB, fb, kb * BK, ni * BN);
+                    }
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy already issued land before the block exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued[s]) mbar_wait(full_bar(s), issued_phase[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
+            // K-major SW128: rows of 128 B, 8-row groups 1024 B apart (SBO), K step 32 B.
+            // MN-major SW128: 64-element MN atoms 8 KB apart (LBO), 8-row K groups 1024 B
+            // apart (SBO), K step 16 rows = 2048 B.
+            const uint32_t a_lbo = A_MN ? MN_BOX_BYTES : 16u, b_lbo = B_MN ? MN_BOX_BYTES : 16u;
+            const uint32_t a_kstep = A_MN ? UMMA_K * 128u : UMMA_K * 2u;
+            const uint32_t b_kstep = B_MN ? UMMA_K * 128u : UMMA_K * 2u;
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            bool any = false;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+                const int as = it & 1;
+                const uint32_t aphase = (it >> 1) & 1;
+                if (!mbar_wait(tempty_bar(as), aphase ^ 1u)) {
+                    atomicExch(ep.err, ERR_MMA_TMEM);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(as * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase)) {
+                        atomicExch(ep.err, ERR_MMA_FULL);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        const uint64_t da = smem_desc(sa + k * a_kstep, a_lbo, 1024u);
+                        const uint64_t db = smem_desc(sb + k * b_kstep, b_lbo, 1024u);
+                        mma_bf16(d, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    any = true;
+                    mma_commit(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(tfull_bar(as));
+            }
+            if (!ok && any) {
+                // wait for the MMAs already issued: commit to a free barrier and wait on it
+                mma_commit(tfull_bar(it & 1));
+                mbar_wait(tfull_bar(it & 1), ((it >> 1) & 1));
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                 // TMEM lane quarter this warp may access
+        const int rl = q * 32 + lane;           // accumulator row of this thread
+        int it = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+            int mi, ni;
+            tile_mn(t, mi, ni);
+            const int as = it & 1;
+            const uint32_t aphase = (it >> 1) & 1;
+            const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(as), aphase));
+            if (!got) {
+                if (lane == 0) atomicExch(ep.err, ERR_EPI_TMEM);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + static_cast<uint32_t>(as * BN) + (static_cast<uint32_t>(q * 32) << 16);
+            const int row = mi * BM + rl;
+            const int n0 = ni * BN;
+            const bool row_ok = row < ep.M;
+            if (EPI == EPI_LOGITS) {
+                const int64_t y = row_ok ? ep.labels[row] : ep.ignore_index;
+                const bool live = row_ok && y != ep.ignore_index;
+                float m = -INFINITY, zl = 0.f;
+                bool has_lab = false;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = n0 + c * 32 + j;
+                        if (col < ep.N) m = fmaxf(m, v[j]);
+                        if (col == y) {
+                            zl = v[j];
+                            has_lab = true;
+                        }
+                    }
+                }
+                const float ml = m * 1.4426950408889634f;
+                float sum = 0.f;
+                __nv_bfloat16* prow = ep.p_out + static_cast<int64_t>(row) * ep.ldp + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = n0 + c * 32 + j;
+                        const float e = col < ep.N ? exp2f(fmaf(v[j], 1.4426950408889634f, -ml)) : 0.f;
+                        v[j] = e;
+                        sum += e;
+                    }
+                    if (live) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int col = n0 + c * 32 + g * 8;
+                            if (col < ep.N) {
+                                uint4 u = make_uint4(pack_bf2(v[g * 8 + 0], v[g * 8 + 1]),
+                                                     pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
+                                                     pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
+                                                     pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
+                                stg16(prow + c * 32 + g * 8, u);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(as));
+                if (live) {
+                    ep.part[static_cast<int64_t>(row) * ep.nvt + ni] = make_float2(m, sum);
+                    if (has_lab) ep.zlab[row] = zl;
+                }
+            } else if (EPI == EPI_STORE) {
+                const int64_t y = (row_ok && ep.labels != nullptr) ? ep.labels[row] : ep.ignore_index;
+                const bool zero = !row_ok || (ep.labels != nullptr && y == ep.ignore_index);
+                const __nv_bfloat16* crow =
+                    (ep.corr_src != nullptr && !zero) ? ep.corr_src + y * ep.ld_corr + n0 : nullptr;
+                __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    if (crow != nullptr) sub_scaled32(v, crow + c * 32, ep.corr_scale, ep.N - (n0 + c * 32));
+                    if (row_ok) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int col = n0 + c * 32 + g * 8;
+                            if (col < ep.N) {
+                                uint4 u;
+                                if (zero) {
+                                    u = make_uint4(0, 0, 0, 0);
+                                } else {
+                                    u = make_uint4(pack_bf2(v[g * 8 + 0], v[g * 8 + 1]),
+                                                   pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
+                                                   pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
+                                                   pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
+                                }
+                                stg16(orow + c * 32 + g * 8, u);
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(as));
+            } else {
+                float* arow = ep.acc + static_cast<int64_t>(row) * ep.lda + n0;
+                __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
+                int k_lo = 0, k_hi = 0;
+                if (row_ok && ep.keys != nullptr) {
+                    const unsigned long long key = static_cast<unsigned long long>(row) << 32;
+                    k_lo = lower_bound_u64(ep.keys, ep.nkeys, key);
+                    k_hi = lower_bound_u64(ep.keys, ep.nkeys, key + (1ull << 32));
+                }
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    for (int kk = k_lo; kk < k_hi; ++kk) {
+                        const int64_t t = static_cast<int64_t>(ep.keys[kk] & 0xFFFFFFFFull);
+                        sub_scaled32(v, ep.corr_src + t * ep.ld_corr + n0 + c * 32, ep.corr_scale,
+                                     ep.N - (n0 + c * 32));
+                    }
+                    if (row_ok) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const int col = n0 + c * 32 + g * 4;
+                            if (col < ep.N) {
+                                float* ap = arow + c * 32 + g * 4;
+                                if (ep.acc_read) {
+                                    float o[4];
+                                    unpack(ldg16(ap), o);
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) v[g * 4 + e] += o[e];
+                                }
+                                if (ep.acc_write) {
+                                    float o[4] = {v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]};
+                                    stg16(ap, pack(o));
+                                }
+                            }
+                        }
+                        if (ep.out_write) {
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                const int col = n0 + c * 32 + g * 8;
+                                if (col < ep.N) {
+                                    uint4 u = make_uint4(pack_bf2(v[g * 8 + 0], v[g * 8 + 1]),
+                                                         pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
+                                                         pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
+                                                         pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
+                                    stg16(orow + c * 32 + g * 8, u);
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(as));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------ host side
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no
+// link-time dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn();
+
+// 2-D bf16 map over a row-major matrix [outer, inner] with row stride
+// `ld` elements, box (box_inner x box_outer), 128-byte swizzle, zero fill.
+int make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_inner,
+             int box_outer);
+
+// Launch C = A(M x K) * B(N x K) with the given epilogue.  A_MN / B_MN say
+// whether each operand is MN-major.  grid_limit = 0: one block per SM.
+template <int A_MN, int B_MN, int EPI>
+int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K, const EpiParams& ep,
+                cudaStream_t st, int grid_limit = 0) {
+    auto kern = tc_gemm_kernel<A_MN, B_MN, EPI>;
+    static bool attr_set = false;   // per instantiation; the attribute is per function
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+            return check_launch("tc_gemm attribute");
+        attr_set = true;
+    }
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    int grid = sm_count();
+    if (grid_limit > 0) grid = std::min(grid, grid_limit);
+    grid = std::max(1, std::min(grid, tiles));
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, M, N, K, ep);
+    return check_launch("tc_gemm");
+}
+
+}  // namespace tc
+}  // namespace liger
