@@ -6,10 +6,11 @@
 // y = x * rstd * w.  The backward is the derivative of that forward.
 //
 // GB300 design (HBM-bound, ~2 bytes/element each way in bf16):
-//  * forward: one warp per row, the row held in registers as 16-byte
-//    vectors (VPL vectors per lane), w held in registers across rows, one
-//    warp-shuffle reduction, no shared memory and no block barrier; a
-//    persistent grid of (SMs x resident blocks) warps strides over rows.
+//  * forward: one warp per row, the row held packed in registers as 16-byte
+//    vectors (VPL vectors per lane; 64 registers for a 4096-wide bf16 row),
+//    w re-read per row through L1, one warp-shuffle reduction, no shared
+//    memory and no block barrier; a persistent grid of (SMs x resident
+//    blocks) warps strides over rows.
 //  * backward: one block per contiguous group of rows; each thread owns
 //    fixed columns and keeps its share of dw in fp32 registers across the
 //    group's rows (no atomics); the row dot product is a shuffle + one
@@ -25,7 +26,7 @@ constexpr int kFwdThreads = 256;
 constexpr int kMaxPartials = 1024;
 
 template <typename T, int VPL>
-__global__ void __launch_bounds__(kFwdThreads) rmsnorm_fwd_warp(const T* x, const T* __restrict__ w, T* y,
+__global__ void __launch_bounds__(kFwdThreads, 2) rmsnorm_fwd_warp(const T* x, const T* __restrict__ w, T* y,
                                                                  float* __restrict__ rstd, int64_t rows, int cols,
                                                                  float eps) {
     constexpr int EPV = Vec<T>::N;
@@ -33,16 +34,10 @@ __global__ void __launch_bounds__(kFwdThreads) rmsnorm_fwd_warp(const T* x, cons
     const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int nvec = cols / EPV;
-    uint4 wv[VPL];
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-        const int v = j * 32 + lane;
-        wv[j] = v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0);
-    }
     const float inv_cols = 1.0f / static_cast<float>(cols);
     for (int64_t r = warp0; r < rows; r += nwarps) {
         const T* xr = x + r * cols;
-        uint4 xv[VPL];
+        uint4 xv[VPL];   // the row stays packed in registers: 4 registers per 16-byte vector
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int v = j * 32 + lane;
@@ -59,13 +54,15 @@ __global__ void __launch_bounds__(kFwdThreads) rmsnorm_fwd_warp(const T* x, cons
         ss = warp_sum(ss);
         const float rs = 1.0f / sqrtf(ss * inv_cols + eps);
         T* yr = y + r * cols;
+        // w is re-read per row through L1 (every warp of the SM reads the same
+        // cols elements), which keeps it out of the register budget
 #pragma unroll
         for (int j = 0; j < VPL; ++j) {
             const int v = j * 32 + lane;
             if (v < nvec) {
                 float f[EPV], g[EPV];
                 unpack(xv[j], f);
-                unpack(wv[j], g);
+                unpack(ldg16_nc(w + static_cast<int64_t>(v) * EPV), g);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) f[e] = (f[e] * rs) * g[e];
                 stg16(yr + static_cast<int64_t>(v) * EPV, pack(f));
@@ -371,3 +368,4 @@ extern "C" int liger_rmsnorm_bwd(const void* dy, const void* x, const void* w, c
     return dtype == LIGER_F32 ? launch_bwd<float>(dy, x, w, rstd, dx, dw, part, rows, (int)cols, st)
                               : launch_bwd<__nv_bfloat16>(dy, x, w, rstd, dx, dw, part, rows, (int)cols, st);
 }
+
