@@ -91,6 +91,38 @@ size_t liger_rmsnorm_bwd_workspace(int64_t rows, int64_t cols);
 int liger_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float* rstd, void* dx, void* dw,
                       void* ws, size_t ws_bytes, int64_t rows, int64_t cols, int dtype, void* stream);
 
+/* RMSNorm backward that allocates nothing and takes no workspace.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory when they call the backward: code whose
+ * operator interface carries only its input and output tensors and has no
+ * slot for a scratch buffer, loops that must not call cudaMalloc (it can wait
+ * for the whole device to go idle and so stalls other streams), and
+ * processes that make every device allocation once, at start-up, under a
+ * fixed memory budget.
+ *
+ * Same operator, arguments and results as liger_rmsnorm_bwd, without ws and
+ * ws_bytes.  The per-block fp32 partial sums of dw go to a scratch array of
+ * LIGER_RMSNORM_BWD_NOALLOC_SCRATCH_BYTES (16 MiB) that the library reserves
+ * in device memory itself: every GPU on which the library is loaded holds
+ * that array until the process exits.  The first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call on a device before any stream capture.  The
+ * function calls no cudaMalloc, cudaFree or allocating library routine.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero: a call writes every partial sum it
+ *     reads.  Calls whose work can overlap on the GPU (several streams,
+ *     several host threads) race on the array: the caller must order them.
+ *   - Partial rows: min(rows, 4 x SMs, 1024, 16 MiB / (4 * cols)).  When the
+ *     last term is the smallest, fewer partials are summed than by
+ *     liger_rmsnorm_bwd, so dw may differ from it by rounding only.
+ *   - cols above 16 MiB / 4 = 4194304 does not fit one partial row: the call
+ *     returns LIGER_ERR_WORKSPACE and queues nothing.
+ */
+#define LIGER_RMSNORM_BWD_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int liger_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* w, const float* rstd, void* dx, void* dw,
+                              int64_t rows, int64_t cols, int dtype, void* stream);
+
 /* ---------------------------------------------------------------- RoPE
  * Source: the FusedRoPE paragraph of the page "Liger-Kernel核心技术：
  * RollingBuffer与融合算子详解", section "算子融合" (the angle comes from the

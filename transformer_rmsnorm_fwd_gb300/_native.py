@@ -32,6 +32,7 @@ SIGNATURES = {
     "liger_rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _INT, _P], _INT),
     "liger_rmsnorm_bwd_workspace": ([_I64, _I64], _SZ),
     "liger_rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _INT, _P], _INT),
+    "liger_rmsnorm_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "liger_rope_fwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _D, _INT, _P], _INT),
     "liger_rope_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _D, _INT, _P], _INT),
     "liger_swiglu_fwd": ([_P, _P, _P, _I64, _INT, _P], _INT),
@@ -127,6 +128,18 @@ def liger_rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws):
     nbytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(load().liger_rmsnorm_bwd(_ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), _ptr(ws), nbytes,
                                     rows, cols, _dtype_code(x), _stream()))
+    return dx, dw
+
+
+def liger_rmsnorm_bwd_noalloc(dy, x, w, rstd, dx, dw):
+    """RMSNorm backward with no workspace argument: the library keeps the
+    scratch in its own fixed device array (see liger.h for who needs this and
+    the limits: calls that overlap on the GPU share that array)."""
+    _dense(dy, x, w, rstd, dx, dw)
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    _check(load().liger_rmsnorm_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(w), _ptr(rstd), _ptr(dx), _ptr(dw), rows, cols,
+                                            _dtype_code(x), _stream()))
     return dx, dw
 
 

@@ -369,3 +369,103 @@ extern "C" int liger_rmsnorm_bwd(const void* dy, const void* x, const void* w, c
                               : launch_bwd<__nv_bfloat16>(dy, x, w, rstd, dx, dw, part, rows, (int)cols, st);
 }
 
+// ------------------------------------------------ backward without workspace
+// For callers that cannot hand this library a device buffer at call time
+// (see liger_rmsnorm_bwd_noalloc in liger.h), the dw partial sums live in a
+// fixed array of device memory that the library itself reserves.  Host code
+// must not pass the array's name to a kernel (on the host that name is only a
+// stand-in); its device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current.
+#include <mutex>
+
+namespace liger {
+namespace {
+
+constexpr size_t kNoAllocBytes = LIGER_RMSNORM_BWD_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) float g_noalloc_part[kNoAllocBytes / sizeof(float)];
+
+constexpr int kNoAllocMaxDev = 64;
+static float* g_noalloc_addr[kNoAllocMaxDev] = {nullptr};
+static std::mutex g_noalloc_mu;
+
+int noalloc_scratch(float** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return fail(LIGER_ERR_CUDA, "rmsnorm_bwd_noalloc: no current CUDA device");
+    if (dev >= kNoAllocMaxDev) return fail(LIGER_ERR_CUDA, "rmsnorm_bwd_noalloc: device %d not supported", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_part);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(LIGER_ERR_CUDA, "rmsnorm_bwd_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+        g_noalloc_addr[dev] = static_cast<float*>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return LIGER_OK;
+}
+
+// Same kernels as launch_bwd, with at most max_parts partial rows.
+template <typename T>
+int launch_bwd_noalloc(const void* dy, const void* x, const void* w, const float* rstd, void* dx, void* dw,
+                       float* part, int64_t rows, int cols, int64_t max_parts, cudaStream_t st) {
+    constexpr int EPV = Vec<T>::N;
+    const int64_t P = std::max<int64_t>(1, std::min(bwd_partials(rows), max_parts));
+    const int64_t rpb = ceil_div(rows, P);
+    const int64_t grid = ceil_div(rows, rpb);
+    const T* dyp = static_cast<const T*>(dy);
+    const T* xp = static_cast<const T*>(x);
+    const T* wp = static_cast<const T*>(w);
+    T* dxp = static_cast<T*>(dx);
+    bool done = false;
+    if (cols % EPV == 0) {
+        const int nvec = cols / EPV;
+        auto go = [&](auto kern, int vpt) {
+            const int nt = static_cast<int>(std::min<int64_t>(256, ceil_div(ceil_div(nvec, vpt), 32) * 32));
+            kern<<<static_cast<unsigned>(grid), nt, 0, st>>>(dyp, xp, wp, rstd, dxp, part, rows, cols, rpb);
+            done = true;
+        };
+        if (nvec <= 256) go(rmsnorm_bwd_block<T, 1>, 1);
+        else if (nvec <= 512) go(rmsnorm_bwd_block<T, 2>, 2);
+        else if (nvec <= 1024) go(rmsnorm_bwd_block<T, 4>, 4);
+        else if (nvec <= 2048) go(rmsnorm_bwd_block<T, 8>, 8);
+    }
+    if (!done)
+        rmsnorm_bwd_generic<T><<<static_cast<unsigned>(grid), 256, 0, st>>>(dyp, xp, wp, rstd, dxp, part, rows, cols,
+                                                                            rpb);
+    int rc = check_launch("rmsnorm_bwd_noalloc");
+    if (rc) return rc;
+    rmsnorm_dw_reduce<T><<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, st>>>(
+        part, static_cast<T*>(dw), static_cast<int>(grid), cols);
+    return check_launch("rmsnorm_dw_reduce");
+}
+
+}  // namespace
+}  // namespace liger
+
+extern "C" int liger_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* w, const float* rstd, void* dx,
+                                         void* dw, int64_t rows, int64_t cols, int dtype, void* stream) {
+    clear_error();
+    if (int rc = check_common(rows, cols, dtype)) return rc;
+    if (static_cast<size_t>(cols) * sizeof(float) > kNoAllocBytes)
+        return fail(LIGER_ERR_WORKSPACE,
+                    "rmsnorm_bwd_noalloc: cols=%lld needs more than the %zu-byte built-in scratch (max cols %zu)",
+                    (long long)cols, kNoAllocBytes, kNoAllocBytes / sizeof(float));
+    if (!dw || (rows > 0 && (!dy || !x || !w || !dx || !rstd)))
+        return fail(LIGER_ERR_NULL, "rmsnorm_bwd_noalloc: dy, x, w, rstd, dx and dw are required");
+    if (!aligned16(dy) || !aligned16(x) || !aligned16(w) || !aligned16(dx) || !aligned16(dw) ||
+        (reinterpret_cast<uintptr_t>(rstd) & 3))
+        return fail(LIGER_ERR_ALIGN, "rmsnorm_bwd_noalloc: tensors must be 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    if (rows == 0) {
+        const size_t bytes = static_cast<size_t>(cols) * (dtype == LIGER_F32 ? 4 : 2);
+        if (cudaMemsetAsync(dw, 0, bytes, st) != cudaSuccess) return check_launch("rmsnorm_bwd_noalloc memset");
+        return LIGER_OK;
+    }
+    float* part = nullptr;
+    if (int rc = noalloc_scratch(&part)) return rc;
+    const int64_t max_parts = static_cast<int64_t>(kNoAllocBytes / (static_cast<size_t>(cols) * sizeof(float)));
+    return dtype == LIGER_F32
+               ? launch_bwd_noalloc<float>(dy, x, w, rstd, dx, dw, part, rows, (int)cols, max_parts, st)
+               : launch_bwd_noalloc<__nv_bfloat16>(dy, x, w, rstd, dx, dw, part, rows, (int)cols, max_parts, st);
+}
