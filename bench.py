@@ -176,9 +176,10 @@ class Chain:
                                 device=device)
 
     def launches_per_step(self):
-        chunk = min(4096, self.S)
+        chunk = min(self.S, 8192, max(128, (self.S + 1) // 2))
         nchunks = -(-self.S // chunk)
-        return 1 + 1 + 1 + (1 + 5 * nchunks + 1) + 1 + 1 + 2
+        # per chunk: logits GEMM, dlogits, dX GEMM, label sort, label starts, dW GEMM
+        return 1 + 1 + 1 + (1 + 6 * nchunks + 1) + 1 + 1 + 2
 
     def step(self, ev=None):
         """One pass of every operator; ev: dict name -> list of (start, end) events."""
@@ -204,6 +205,38 @@ class Chain:
         rec("rope_bwd", lambda: L.liger_rope_bwd(i["dq"], i["dk"], None, THETA))
         rec("rmsnorm_bwd", lambda: L.liger_rmsnorm_bwd(i["dy_r"], i["x"], i["w"], self.rstd, self.dx, self.dw,
                                                        self.ws_r))
+
+
+def isolated_times(chain, dev, n=10):
+    """Each memory-bound operator of the chain timed alone (median of n launches,
+    L2 flushed by writing 512 MB before each): ms per call."""
+    import torch
+    L, i = chain.L, chain.inp
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    ops = {
+        "rmsnorm_fwd": lambda: L.liger_rmsnorm_fwd(i["x"], i["w"], chain.y, chain.rstd, EPS),
+        "rmsnorm_bwd": lambda: L.liger_rmsnorm_bwd(i["dy_r"], i["x"], i["w"], chain.rstd, chain.dx, chain.dw,
+                                                   chain.ws_r),
+        "rope_fwd": lambda: L.liger_rope_fwd(i["q"], i["k"], None, THETA),
+        "rope_bwd": lambda: L.liger_rope_bwd(i["dq"], i["dk"], None, THETA),
+        "swiglu_fwd": lambda: L.liger_swiglu_fwd(i["gate"], i["up"], chain.ys),
+        "swiglu_bwd": lambda: L.liger_swiglu_bwd(i["dy_s"], i["gate"], i["up"], chain.dg, chain.du),
+    }
+    out = {}
+    for name, fn in ops.items():
+        fn()
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        out[name] = statistics.median(ts)
+    del flush
+    return out
 
 
 # ------------------------------------------------------------------ clocks
@@ -356,36 +389,61 @@ def native_arm(args):
     tokens = sum_over_ranks(float(S * K), dist, dev)
     value = tokens / (ms / 1000.0)
     per_op = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
+    iso = isolated_times(chain, dev)
     loss = float(chain.loss.item())
 
-    # ---- end to end through host buffers: H2D of the step's inputs, D2H of the loss
+    # ---- end to end through host buffers: every step copies its inputs host -> device from
+    # pinned memory and reads its loss back.  The copies run on a second stream into the
+    # other half of a double-buffered input set, overlapping the previous step's kernels;
+    # the timed region spans all K steps' copies and kernels.
     e2e = None
     if not args.no_e2e:
         host = {k: to_torch(v, pin=True) for k, v in inputs.items()}
-        h_loss = torch.empty(1, dtype=torch.float32).pin_memory()
+        h_loss = torch.empty(K + max(1, W), dtype=torch.float32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
+        sets = [chain.inp, {k: torch.empty_like(v) for k, v in chain.inp.items()}]
+        copy_stream = torch.cuda.Stream(device=dev)
+        compute = torch.cuda.current_stream(dev)
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        consumed = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def e2e_step():
-            for k, t in host.items():
-                chain.inp[k].copy_(t, non_blocking=True)
-            chain.step()
-            h_loss.copy_(chain.loss, non_blocking=True)
+        def enqueue_copy(i):
+            s = i % 2
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(consumed[s])      # the step that last used this set is done
+                for k, t in host.items():
+                    sets[s][k].copy_(t, non_blocking=True)
+                copied[s].record(copy_stream)
 
-        for _ in range(max(1, W)):
-            e2e_step()
+        def run(n, offset):
+            enqueue_copy(0)
+            for i in range(n):
+                s = i % 2
+                if i + 1 < n:
+                    enqueue_copy(i + 1)
+                compute.wait_event(copied[s])
+                chain.inp = sets[s]
+                chain.step()
+                consumed[s].record(compute)
+                h_loss[offset + i].copy_(chain.loss[0], non_blocking=True)
+
+        for ev in consumed:
+            ev.record(compute)
+        run(max(1, W), K)
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(K):
-            e2e_step()
-        b.record()
+        a.record(compute)
+        run(K, 0)
+        b.record(compute)
         torch.cuda.synchronize()
         ms_e = max_over_ranks(a.elapsed_time(b), dist, dev)
         e2e = {"value": tokens / (ms_e / 1000.0), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": 4, "ms_per_step": ms_e / K}
-        del host
+               "d2h_bytes_per_step": 4, "ms_per_step": ms_e / K,
+               "pipelining": "inputs of step i+1 copied on a second stream during step i (double-buffered)"}
+        chain.inp = sets[0]
+        del host, sets
 
     if rank != 0:
         if dist:
@@ -397,8 +455,10 @@ def native_arm(args):
     hbm = {}
     for k in ("rmsnorm_fwd", "rmsnorm_bwd", "rope_fwd", "rope_bwd", "swiglu_fwd", "swiglu_bwd"):
         gbs = alg[k] / (per_op[k] / 1000.0) / 1e9
+        gi = alg[k] / (iso[k] / 1000.0) / 1e9
         hbm[k] = {"ms": round(per_op[k], 4), "bytes": alg[k], "gbs": round(gbs, 1),
-                  "frac": round(gbs / pk["hbm_gbs"], 4)}
+                  "frac": round(gbs / pk["hbm_gbs"], 4), "ms_isolated": round(iso[k], 4),
+                  "gbs_isolated": round(gi, 1), "frac_isolated": round(gi / pk["hbm_gbs"], 4)}
     ce_tf = alg["linear_ce_flops"] / (per_op["linear_ce"] / 1000.0) / 1e12
     roofline = {"kernel": "liger_linear_ce_fwd_bwd (tcgen05 GEMMs + fused epilogues; 6*S*H*V flops per call)",
                 "bound": "tensor", "achieved": round(ce_tf, 1), "peak": pk["bf16_sustained"], "unit": "TFLOP/s",

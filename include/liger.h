@@ -113,7 +113,7 @@ int liger_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float*
  *     Nothing in it needs to start at zero: a call writes every partial sum it
  *     reads.  Calls whose work can overlap on the GPU (several streams,
  *     several host threads) race on the array: the caller must order them.
- *   - Partial rows: min(rows, 4 x SMs, 1024, 16 MiB / (4 * cols)).  When the
+ *   - Partial rows: min(rows, 2 x SMs, 1024, 16 MiB / (4 * cols)).  When the
  *     last term is the smallest, fewer partials are summed than by
  *     liger_rmsnorm_bwd, so dw may differ from it by rounding only.
  *   - cols above 16 MiB / 4 = 4194304 does not fit one partial row: the call
@@ -147,6 +147,31 @@ int liger_rope_fwd(void* q, void* k, const int32_t* pos, int64_t batch, int64_t 
  * applied in place to the incoming gradients dq, dk.  Arguments as above. */
 int liger_rope_bwd(void* dq, void* dk, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
                    int64_t n_k_heads, int64_t head_dim, double theta, int dtype, void* stream);
+
+/* RoPE variants (the other conventions in use beside the pages' half-split
+ * pairing), same rotation and the same in-place semantics:
+ *   - pairing 0: pairs (i, i + head_dim/2) (as liger_rope_fwd); pairing 1:
+ *     interleaved pairs (2i, 2i+1), angle index i;
+ *   - q_token_stride / k_token_stride: elements between consecutive tokens
+ *     (b, s) of q / k (>= heads * head_dim), so that q and k can be views into
+ *     a packed [batch, seq, (n_q + 2 n_k) * head_dim] QKV buffer; heads of a
+ *     token stay contiguous (head h at h * head_dim);
+ *   - cos_tab / sin_tab: both NULL (angles from theta as above), or both
+ *     [n_tab, head_dim/2] float device tables indexed by position, used as
+ *     given (for scaled frequency schedules); theta is then ignored.  Positions
+ *     outside [0, n_tab) are clamped to the table; keep them inside.
+ *   q and k need only be aligned to their element size here (views into a
+ *   packed buffer); 16-byte aligned head starts select the vector path.
+ *   The _bwd variant negates the sine (transpose of the forward map).
+ */
+int liger_rope_fwd_ex(void* q, void* k, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
+                      int64_t n_k_heads, int64_t head_dim, int64_t q_token_stride, int64_t k_token_stride, int pairing,
+                      const float* cos_tab, const float* sin_tab, int64_t n_tab, double theta, int dtype,
+                      void* stream);
+int liger_rope_bwd_ex(void* dq, void* dk, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
+                      int64_t n_k_heads, int64_t head_dim, int64_t q_token_stride, int64_t k_token_stride, int pairing,
+                      const float* cos_tab, const float* sin_tab, int64_t n_tab, double theta, int dtype,
+                      void* stream);
 
 /* -------------------------------------------------------------- SwiGLU
  * Source: the FusedLinearSwiGLU paragraph of the page "Liger-Kernel核心技术：
@@ -185,9 +210,11 @@ int liger_swiglu_bwd(const void* dy, const void* gate, const void* up, void* dga
  *   loss: one float on the device; dX: [T, H] and dW: [V, H] in dtype, each
  *   may be NULL (not computed).  Rows of dX whose label is ignore_index are
  *   written as +0.0.
- *   The tokens are processed in chunks of `chunk` rows (0 = automatic, at most
- *   4096); per chunk the logits exist only in a [chunk x V] workspace buffer,
- *   never as a [T x V] tensor.  dW is accumulated across chunks in fp32.
+ *   The tokens are processed in chunks of `chunk` rows (0 = automatic:
+ *   min(T, 8192, max(128, ceil(T/2))) on the bf16 tensor-core path; a chunk
+ *   larger than 8192 rows is reduced to 8192 there); per chunk the logits
+ *   exist only in a [chunk x V] workspace buffer, never as a [T x V] tensor
+ *   (T > 128).  dW is accumulated across chunks in fp32.
  *   ws: device workspace of at least liger_linear_ce_workspace(T, H, V,
  *   chunk, dtype) bytes, 256-byte aligned.  On return ws begins with
  *   float lse[T] (0 on ignored rows), followed by float loss_row[T]

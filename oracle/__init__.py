@@ -53,13 +53,15 @@ def _load():
             lib.orc_rmsnorm_fwd.argtypes = [_P, _P, ctypes.c_int, _I, _I, _D, _P, _P]
             lib.orc_rmsnorm_bwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _I, _D, _P, _P]
             lib.orc_rope.argtypes = [_P, ctypes.c_int, _P, _I, _I, _I, _I, _D, ctypes.c_int, _P]
+            lib.orc_rope_ex.argtypes = [_P, ctypes.c_int, _P, _I, _I, _I, _I, _D, ctypes.c_int, ctypes.c_int, _P, _P,
+                                        _I, _P]
             lib.orc_swiglu_fwd.argtypes = [_P, _P, ctypes.c_int, _I, _P]
             lib.orc_swiglu_bwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _P, _P]
             lib.orc_linear_ce.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
                                           _P, _P, _P, _P]
             lib.orc_linear_ce_rows.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
                                                _P, _I, _P, _P, _P]
-            for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_rope", "orc_swiglu_fwd", "orc_swiglu_bwd",
+            for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_rope", "orc_rope_ex", "orc_swiglu_fwd", "orc_swiglu_bwd",
                       "orc_linear_ce", "orc_linear_ce_rows"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -113,6 +115,28 @@ def rope(t, theta, sign=1, pos=None):
         ppos = pos.ctypes.data
     out = np.empty(t.shape, np.float64)
     _check(_load().orc_rope(pt, _dt(t), ppos, B, S, NH, D, theta, int(sign), out.ctypes.data), "rope")
+    return out
+
+
+def rope_ex(t, theta=1e4, sign=1, pos=None, pairing="half", cos_tab=None, sin_tab=None):
+    """RoPE variants on t [B, S, NH, D]: pairing "half" (i, i+D/2) or
+    "interleaved" (2i, 2i+1); optional explicit cos/sin tables [n, D/2]."""
+    t, pt = _c(t)
+    B, S, NH, D = t.shape
+    ppos = None
+    if pos is not None:
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        ppos = pos.ctypes.data
+    pc = ps = None
+    n_tab = 0
+    if cos_tab is not None:
+        cos_tab = np.ascontiguousarray(cos_tab, dtype=np.float64)
+        sin_tab = np.ascontiguousarray(sin_tab, dtype=np.float64)
+        assert cos_tab.shape == sin_tab.shape and cos_tab.shape[1] == D // 2
+        pc, ps, n_tab = cos_tab.ctypes.data, sin_tab.ctypes.data, cos_tab.shape[0]
+    out = np.empty(t.shape, np.float64)
+    _check(_load().orc_rope_ex(pt, _dt(t), ppos, B, S, NH, D, float(theta), int(sign),
+                               1 if pairing == "interleaved" else 0, pc, ps, n_tab, out.ctypes.data), "rope_ex")
     return out
 
 

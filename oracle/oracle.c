@@ -121,6 +121,44 @@ int orc_rope(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S, in
     return 0;
 }
 
+/* RoPE variants (the pages' listing pairs halves; the interleaved pairing
+ * (2i, 2i+1) and caller-supplied cos/sin tables are the other conventions in
+ * use).  Same rotation, written out per pair. */
+int orc_rope_ex(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S, int64_t NH, int64_t D,
+                double theta, int sign, int pairing, const double* cos_tab, const double* sin_tab, int64_t n_tab,
+                double* out) {
+    if (!t || !out || B < 0 || S < 0 || NH < 0 || D <= 0 || (D % 2) || bad_dt(dt)) return -1;
+    if ((sign != 1 && sign != -1) || (pairing != 0 && pairing != 1)) return -1;
+    if ((cos_tab == NULL) != (sin_tab == NULL)) return -1;
+    if (!cos_tab && !(theta > 0.0)) return -1;
+    const int64_t half = D / 2;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t s = 0; s < S; ++s) {
+            int64_t p = pos ? (int64_t)pos[b * S + s] : s;
+            if (cos_tab && (p < 0 || p >= n_tab)) return -2;
+            for (int64_t h = 0; h < NH; ++h) {
+                int64_t base = ((b * S + s) * NH + h) * D;
+                for (int64_t i = 0; i < half; ++i) {
+                    double c, sn;
+                    if (cos_tab) {
+                        c = cos_tab[p * half + i];
+                        sn = (double)sign * sin_tab[p * half + i];
+                    } else {
+                        double phi = (double)sign * (double)p * pow(theta, -2.0 * (double)i / (double)D);
+                        c = cos(phi);
+                        sn = sin(phi);
+                    }
+                    int64_t ia = pairing ? base + 2 * i : base + i;
+                    int64_t ib = pairing ? base + 2 * i + 1 : base + i + half;
+                    double a = ld(t, dt, ia), bb = ld(t, dt, ib);
+                    out[ia] = a * c - bb * sn;
+                    out[ib] = bb * c + a * sn;
+                }
+            }
+        }
+    return 0;
+}
+
 /* ----------------------------------------------------------------- SwiGLU
  * [P1] section "算子融合", FusedLinearSwiGLU paragraph: the SiLU activation of
  * the gate branch times the up branch, elementwise.  silu(g) = g * sigmoid(g).

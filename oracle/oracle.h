@@ -37,6 +37,14 @@ int orc_rmsnorm_bwd(const void* dy, const void* x, const void* w, int dt, int64_
 int orc_rope(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S, int64_t NH, int64_t D,
              double theta, int sign, double* out);
 
+/* RoPE variants.  pairing 0: pairs (i, i + D/2); pairing 1: pairs (2i, 2i+1).
+ * cos_tab / sin_tab (both NULL, or both given): explicit [n_tab, D/2] tables
+ * indexed by position, used instead of theta^(-2i/D) (the sign still applies
+ * to the sine). */
+int orc_rope_ex(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S, int64_t NH, int64_t D,
+                double theta, int sign, int pairing, const double* cos_tab, const double* sin_tab, int64_t n_tab,
+                double* out);
+
 /* SwiGLU forward y = silu(g) * u and its backward. */
 int orc_swiglu_fwd(const void* g, const void* u, int dt, int64_t n, double* y);
 int orc_swiglu_bwd(const void* dy, const void* g, const void* u, int dt, int64_t n, double* dg, double* du);

@@ -220,3 +220,47 @@ def test_zero_sized_calls(cuda_lib):
     dw = torch.full((64,), 3.0, dtype=torch.bfloat16, device="cuda")
     cuda_lib.liger_rmsnorm_bwd(e, e, w, torch.empty(0, device="cuda"), e, dw, None)
     assert torch.all(dw == 0)
+
+
+# ------------------------------------------------------------ RoPE variants
+@pytest.mark.parametrize("dtype,pairing,D", [("bf16", "interleaved", 128), ("f32", "interleaved", 64),
+                                             ("bf16", "half", 128), ("f32", "interleaved", 6),
+                                             ("bf16", "interleaved", 24)])
+def test_rope_ex_packed_qkv_views(cuda_lib, dtype, pairing, D):
+    """q and k as views into a packed [B, S, (Hq + 2 Hk) * D] QKV buffer; v untouched."""
+    import torch
+    B, S, Hq, Hk = 2, 37, 5, 2
+    W = (Hq + 2 * Hk) * D
+    qkv = datagen.normal(41, "qkv", (B, S, W), dtype)
+    pos = datagen.positions(41, "qp", (B, S), 32768)
+    t = dev(qkv)
+    tq = t.view(-1)[0:]                              # q starts at element 0 of each token
+    tk = t.view(-1)[Hq * D:]                         # k starts after the q heads
+    cuda_lib.liger_rope_fwd_ex(tq, tk, W, W, Hq, Hk, D, B, S, dev(pos), 5e5, pairing)
+    out = host(t)
+    q = np.ascontiguousarray(qkv[:, :, : Hq * D].reshape(B, S, Hq, D))
+    k = np.ascontiguousarray(qkv[:, :, Hq * D: (Hq + Hk) * D].reshape(B, S, Hk, D))
+    oq = oracle.rope_ex(q, 5e5, pos=pos, pairing=pairing).reshape(B, S, Hq * D)
+    ok = oracle.rope_ex(k, 5e5, pos=pos, pairing=pairing).reshape(B, S, Hk * D)
+    assert oracle.rel_err(out[:, :, : Hq * D], oq) <= TOL[dtype]
+    assert oracle.rel_err(out[:, :, Hq * D: (Hq + Hk) * D], ok) <= TOL[dtype]
+    assert np.array_equal(bits(t)[:, :, (Hq + Hk) * D:], qkv[:, :, (Hq + Hk) * D:].view(bits(t).dtype))
+    cuda_lib.liger_rope_bwd_ex(tq, tk, W, W, Hq, Hk, D, B, S, dev(pos), 5e5, pairing)
+    assert oracle.rel_err(host(t), datagen.to_f64(qkv, dtype)) <= (1e-5 if dtype == "f32" else 2e-2)
+    del torch
+
+
+@pytest.mark.parametrize("pairing", ["half", "interleaved"])
+def test_rope_ex_explicit_tables(cuda_lib, pairing):
+    """Caller-supplied cos/sin tables (a scaled schedule: angles p * 0.25 * theta^(-2i/D))."""
+    import torch
+    B, S, H, D = 1, 64, 3, 64
+    i = np.arange(D // 2)
+    ang = np.arange(S)[:, None] * 0.25 * (1e4 ** (-2.0 * i / D))[None, :]
+    cos_t, sin_t = np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+    q = datagen.normal(42, "tq", (B, S, H, D), "f32")
+    tq = dev(q)
+    cuda_lib.liger_rope_fwd_ex(tq, None, H * D, 0, H, 0, D, B, S, None, 0.0, pairing,
+                               torch.from_numpy(cos_t).cuda(), torch.from_numpy(sin_t).cuda())
+    want = oracle.rope_ex(q, 0.0, pairing=pairing, cos_tab=cos_t.astype(np.float64), sin_tab=sin_t.astype(np.float64))
+    assert oracle.rel_err(host(tq), want) <= 1e-5

@@ -216,3 +216,37 @@ def test_storage_widening_is_exact():
     y1, _ = oracle.rmsnorm_fwd(b, datagen.f32_to_bf16_bits(np.ones(8, np.float32)), 1e-6)
     y2, _ = oracle.rmsnorm_fwd(f.astype(np.float64), np.ones(8), 1e-6)
     assert np.array_equal(y1, y2)
+
+
+# ------------------------------------------------------------ RoPE variants
+def test_rope_ex_half_pairing_equals_rope():
+    t = RNG.standard_normal((2, 7, 3, 16))
+    pos = RNG.integers(0, 5000, (2, 7)).astype(np.int32)
+    assert np.array_equal(oracle.rope_ex(t, 5e5, pos=pos), oracle.rope(t, 5e5, pos=pos))
+
+
+def test_rope_ex_interleaved_single_feature_angles():
+    # interleaved pairs (2i, 2i+1): a unit vector at feature 2i rotates to (cos, sin) at (2i, 2i+1)
+    for c in golden("rope_angles.json")["cases"]:
+        D, i, p = c["D"], c["i"], c["p"]
+        t = np.zeros((1, p + 1, 1, D)); t[0, p, 0, 2 * i] = 1.0
+        out = oracle.rope_ex(t, c["theta"], pairing="interleaved")
+        assert abs(out[0, p, 0, 2 * i] - c["cos"]) < 1e-12 and abs(out[0, p, 0, 2 * i + 1] - c["sin"]) < 1e-12
+        assert np.count_nonzero(np.abs(out[0, p, 0]) > 1e-15) == 2
+
+
+def test_rope_ex_table_matches_schedule_and_inverse():
+    D, P = 16, 40
+    i = np.arange(D // 2)
+    ang = np.arange(P)[:, None] * (1e4 ** (-2.0 * i / D))[None, :]
+    cos_t, sin_t = np.cos(ang), np.sin(ang)
+    t = RNG.standard_normal((1, P, 2, D))
+    for pairing in ("half", "interleaved"):
+        a = oracle.rope_ex(t, 1e4, pairing=pairing)
+        b = oracle.rope_ex(t, 0.0, pairing=pairing, cos_tab=cos_t, sin_tab=sin_t)
+        assert np.max(np.abs(a - b)) < 1e-12
+        back = oracle.rope_ex(b, 0.0, sign=-1, pairing=pairing, cos_tab=cos_t, sin_tab=sin_t)
+        assert np.max(np.abs(back - t)) < 1e-13
+    # a table that is not a rotation (scaled cos) is applied as given
+    s = oracle.rope_ex(np.ones((1, 1, 1, 2)), 0.0, cos_tab=np.array([[0.5]]), sin_tab=np.array([[0.0]]))
+    assert np.allclose(s[0, 0, 0], [0.5, 0.5])

@@ -7,5 +7,5 @@ logits, all hand-written CUDA behind the C-ABI of ``libliger.so``
 see ``_native`` for the functions, which carry the C entry points' names.
 """
 from ._native import (LIGER_BF16, LIGER_F32, LigerError, liger_linear_ce_fwd_bwd,  # noqa: F401
-                      liger_linear_ce_workspace, liger_rmsnorm_bwd, liger_rmsnorm_bwd_workspace, liger_rmsnorm_fwd,
-                      liger_rope_bwd, liger_rope_fwd, liger_swiglu_bwd, liger_swiglu_fwd, load)
+                      liger_linear_ce_workspace, liger_rmsnorm_bwd, liger_rmsnorm_bwd_noalloc, liger_rmsnorm_bwd_workspace, liger_rmsnorm_fwd,
+                      liger_rope_bwd, liger_rope_bwd_ex, liger_rope_fwd, liger_rope_fwd_ex, liger_swiglu_bwd, liger_swiglu_fwd, load)

@@ -35,6 +35,10 @@ SIGNATURES = {
     "liger_rmsnorm_bwd_noalloc": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _INT, _P], _INT),
     "liger_rope_fwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _D, _INT, _P], _INT),
     "liger_rope_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _D, _INT, _P], _INT),
+    "liger_rope_fwd_ex": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _INT, _P, _P, _I64, _D, _INT, _P],
+                          _INT),
+    "liger_rope_bwd_ex": ([_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _INT, _P, _P, _I64, _D, _INT, _P],
+                          _INT),
     "liger_swiglu_fwd": ([_P, _P, _P, _I64, _INT, _P], _INT),
     "liger_swiglu_bwd": ([_P, _P, _P, _P, _P, _I64, _INT, _P], _INT),
     "liger_linear_ce_workspace": ([_I64, _I64, _I64, _I64, _INT], _SZ),
@@ -160,6 +164,32 @@ def liger_rope_fwd(q, k, pos=None, theta: float = 1e4):
 
 def liger_rope_bwd(dq, dk, pos=None, theta: float = 1e4):
     return _rope(load().liger_rope_bwd, dq, dk, pos, theta)
+
+
+def _rope_ex(fn, q, k, q_token_stride, k_token_stride, n_q_heads, n_k_heads, head_dim, batch, seq, pos, theta,
+             pairing, cos_tab, sin_tab):
+    for t in (pos, cos_tab, sin_tab):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("pos and tables must be contiguous CUDA tensors")
+    n_tab = cos_tab.shape[0] if cos_tab is not None else 0
+    dt = _dtype_code(q if q is not None else k)
+    _check(fn(_ptr(q), _ptr(k), _ptr(pos), batch, seq, n_q_heads, n_k_heads, head_dim, q_token_stride,
+              k_token_stride, 1 if pairing == "interleaved" else 0, _ptr(cos_tab), _ptr(sin_tab), n_tab,
+              float(theta), dt, _stream()))
+
+
+def liger_rope_fwd_ex(q, k, q_token_stride, k_token_stride, n_q_heads, n_k_heads, head_dim, batch, seq, pos=None,
+                      theta=1e4, pairing="half", cos_tab=None, sin_tab=None):
+    """RoPE variants in place on (possibly strided) q / k views: see liger.h.
+    q and k are torch tensors whose data_ptr() is the first element of the view."""
+    _rope_ex(load().liger_rope_fwd_ex, q, k, q_token_stride, k_token_stride, n_q_heads, n_k_heads, head_dim, batch,
+             seq, pos, theta, pairing, cos_tab, sin_tab)
+
+
+def liger_rope_bwd_ex(dq, dk, q_token_stride, k_token_stride, n_q_heads, n_k_heads, head_dim, batch, seq, pos=None,
+                      theta=1e4, pairing="half", cos_tab=None, sin_tab=None):
+    _rope_ex(load().liger_rope_bwd_ex, dq, dk, q_token_stride, k_token_stride, n_q_heads, n_k_heads, head_dim, batch,
+             seq, pos, theta, pairing, cos_tab, sin_tab)
 
 
 # ------------------------------------------------------------------- SwiGLU

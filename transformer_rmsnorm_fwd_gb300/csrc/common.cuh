@@ -77,6 +77,14 @@ __device__ __forceinline__ uint4 ldg16_nc(const void* p) {
     return r;
 }
 __device__ __forceinline__ void stg16(void* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
+// streaming load (evict-first): data read once by this kernel
+__device__ __forceinline__ uint4 ldg16_cs(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
 // streaming store (evict-first): output that is not re-read by this kernel
 __device__ __forceinline__ void stg16_cs(void* p, const uint4& v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)

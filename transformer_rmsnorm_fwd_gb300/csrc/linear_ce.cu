@@ -17,8 +17,9 @@
 //   3. dX_c = S W on tcgen05 (W read MN-major); the epilogue subtracts the
 //      one-hot part, scale * W[label], in fp32; ignored rows written +0;
 //   4. dW (+)= S^T X_c on tcgen05 (both operands MN-major); the epilogue
-//      subtracts scale * X_t for the tokens labelled with the row (a sorted
-//      label list, binary-searched) in fp32, and accumulates across chunks in
+//      subtracts scale * X_t for the tokens labelled with the row (the chunk's
+//      labels sorted once, indexed by a [V+1] start table) in fp32, and
+//      prefetches and accumulates across chunks in
 //      an fp32 [V x H] workspace, the last chunk writing W's dtype.
 // Keeping the one-hot term out of the bf16 operand matters: rounding
 // -scale to bf16 at every label would cost up to 2^-9 relative on the rows of
@@ -48,7 +49,7 @@ struct Hdr {
 struct Layout {
     bool tc;
     int64_t C, ldp, nvt, nchunks;
-    size_t lse, lossrow, zlab, hdr, keys, part, scr, acc, total;
+    size_t lse, lossrow, zlab, hdr, keys, lstart, part, scr, acc, total;
 };
 
 inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -60,7 +61,8 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     L.tc = use_tc(H, V, dtype);
     int64_t C;
     if (chunk > 0) C = chunk;
-    else if (L.tc) C = 4096;
+    // automatic: at most half the tokens (never all T rows at once, for T > 128), at most 8192 rows
+    else if (L.tc) C = std::min<int64_t>(kMaxChunkTC, std::max<int64_t>(128, (T + 1) / 2));
     else C = std::max<int64_t>(128, (int64_t{1} << 26) / std::max<int64_t>(V, 1));
     if (L.tc) C = std::min<int64_t>(C, kMaxChunkTC);
     C = std::max<int64_t>(1, std::min(C, std::max<int64_t>(T, 1)));
@@ -74,6 +76,7 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     L.zlab = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
     L.hdr = o; o = up256(o + sizeof(Hdr));
     L.keys = o; o = up256(o + (L.tc ? sizeof(unsigned long long) * static_cast<size_t>(C) : 0));
+    L.lstart = o; o = up256(o + (L.tc ? sizeof(int) * static_cast<size_t>(V + 1) : 0));
     L.part = o; o = up256(o + (L.tc ? sizeof(float2) * static_cast<size_t>(C * L.nvt) : 0));
     L.scr = o; o = up256(o + static_cast<size_t>(C) * static_cast<size_t>(L.ldp) * (L.tc ? 2 : 4));
     const bool need_acc = L.nchunks > 1 && dtype == LIGER_BF16;
@@ -148,6 +151,21 @@ __global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restric
         }
     }
     for (int i = threadIdx.x; i < n; i += 1024) out[i] = sk[i];
+}
+
+// lstart[v] = first index of label v in the sorted chunk keys, v in [0, V]
+// (so the tokens labelled v are keys[lstart[v] .. lstart[v+1])).
+__global__ void label_starts(const unsigned long long* __restrict__ keys, int n, int V, int* __restrict__ lstart) {
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v <= V; v += gridDim.x * blockDim.x) {
+        const unsigned long long key = static_cast<unsigned long long>(v) << 32;
+        int lo = 0, hi = n;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (keys[mid] < key) lo = mid + 1;
+            else hi = mid;
+        }
+        lstart[v] = lo;
+    }
 }
 
 // Merge the per-tile (m, s) of one chunk row into lse and rewrite P in place
@@ -399,6 +417,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(a.ws + L.scr);
     float* acc = reinterpret_cast<float*>(a.ws + L.acc);
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(a.ws + L.keys);
+    int* lstart = reinterpret_cast<int*>(a.ws + L.lstart);
     const int H = static_cast<int>(a.H), V = static_cast<int>(a.V);
     int rc;
     CUtensorMap mW_k, mW_mn;
@@ -423,7 +442,9 @@ int run_tc(const Args& a, const Layout& L, float scale) {
         // 1. logits -> P, (m, s) partials, z at label
         e.M = cl;
         e.N = V;
-        e.raster_n_fastest = 0;
+        e.raster = RASTER_M_FASTEST;
+        e.hint_a = HINT_EVICT_LAST;    // X_c: reused by every vocab tile, keep in L2
+        e.hint_b = HINT_EVICT_FIRST;   // W: streamed once per chunk
         e.p_out = P;
         e.ldp = L.ldp;
         e.part = part;
@@ -441,6 +462,9 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             d.N = H;
             d.out = static_cast<__nv_bfloat16*>(a.dX) + t0 * H;
             d.ldo = H;
+            d.raster = RASTER_N_GROUPS;
+            d.hint_a = HINT_NORMAL;        // D and W: reused within a wave of tiles
+            d.hint_b = HINT_NORMAL;
             d.corr_src = W;
             d.ld_corr = H;
             d.corr_scale = scale;
@@ -453,15 +477,21 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             sort_label_keys<<<1, 1024, sizeof(unsigned long long) * npow2, a.st>>>(a.labels + t0, cl, a.ignore, npow2,
                                                                                     keys);
             if ((rc = check_launch("sort_label_keys"))) return rc;
+            label_starts<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(V + 1, 256), 8 * sm_count())), 256, 0,
+                           a.st>>>(keys, cl, V, lstart);
+            if ((rc = check_launch("label_starts"))) return rc;
             EpiParams d = e;
             d.corr_src = Xc;
             d.ld_corr = H;
             d.corr_scale = scale;
             d.keys = keys;
             d.nkeys = cl;
+            d.lstart = lstart;
             d.M = V;
             d.N = H;
-            d.raster_n_fastest = 1;
+            d.raster = RASTER_N_FASTEST;
+            d.hint_a = HINT_EVICT_FIRST;   // D^T: each vocab row block read by one wave
+            d.hint_b = HINT_EVICT_LAST;    // X_c: reused by every vocab row block, keep in L2
             d.labels = nullptr;
             d.acc = acc;
             d.lda = H;

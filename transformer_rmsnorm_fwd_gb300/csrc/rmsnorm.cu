@@ -18,6 +18,7 @@
 //    the current one is reduced.  Per-block dw partials go to the workspace
 //    and a second kernel sums them in a fixed order, so dw is deterministic.
 #include "common.cuh"
+#include "mbarrier.cuh"
 
 namespace liger {
 namespace {
@@ -244,6 +245,106 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_reduce(const float* __restrict
     }
 }
 
+// ------------------------------------------------- rows staged by bulk copy
+// Rows travel HBM -> shared memory by 1-D bulk copies (cp.async.bulk) into a
+// ring of `nst` buffers per warp (forward) or per block (backward), so that
+// several rows per warp are in flight without holding them in registers.
+// Every wait is bounded; on expiry the kernel records it in g_stage_err,
+// waits (bounded) for the copies it issued and stops.
+static __device__ int g_stage_err;
+
+struct Stage {
+    uint8_t* base;     // shared buffers
+    uint32_t bar0;     // first mbarrier (8 bytes each)
+};
+
+template <typename T>
+__global__ void rmsnorm_fwd_staged(const T* x, const T* __restrict__ w, T* y, float* __restrict__ rstd,
+                                   int64_t rows, int cols, float eps, int nst) {
+    constexpr int EPV = Vec<T>::N;
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int nw = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rb = static_cast<uint32_t>(cols) * sizeof(T);      // row bytes (multiple of 16)
+    const int nvec = cols / EPV;
+    uint8_t* wbuf = sm;
+    uint8_t* ring = sm + rb + static_cast<size_t>(warp) * nst * rb;
+    const uint32_t bars = smem_u32(sm + static_cast<size_t>(rb) * (1 + nw * nst));
+    const uint32_t wbar = bars + 8u * nw * nst;
+    const uint32_t mybar = bars + 8u * warp * nst;
+    if (lane == 0)
+        for (int s = 0; s < nst; ++s) mbar_init(mybar + 8u * s, 1);
+    if (threadIdx.x == 0) mbar_init(wbar, 1);
+    mbar_init_fence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(wbar, rb);
+        bulk_g2s(smem_u32(wbuf), w, rb, wbar);
+    }
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * nw + warp;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * nw;
+    if (lane == 0)
+        for (int s = 0; s < nst; ++s) {
+            const int64_t r = gw + s * stride;
+            if (r < rows) {
+                mbar_expect_tx(mybar + 8u * s, rb);
+                bulk_g2s(smem_u32(ring + s * rb), x + r * cols, rb, mybar + 8u * s);
+            }
+        }
+    bool ok = __all_sync(0xffffffffu, mbar_wait(wbar, 0));
+    const float inv_cols = 1.0f / static_cast<float>(cols);
+    int it = 0;
+    for (int64_t r = gw; ok && r < rows; r += stride, ++it) {
+        const int s = it % nst;
+        const uint32_t ph = static_cast<uint32_t>(it / nst) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(mybar + 8u * s, ph))) {
+            ok = false;
+            break;
+        }
+        const uint8_t* xb = ring + s * rb;
+        float ss = 0.f;
+        for (int v = lane; v < nvec; v += 32) {
+            float f[EPV];
+            unpack(*reinterpret_cast<const uint4*>(xb + v * 16), f);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+        ss = warp_sum(ss);
+        const float rs = 1.0f / sqrtf(ss * inv_cols + eps);
+        T* yr = y + r * cols;
+        for (int v = lane; v < nvec; v += 32) {
+            float f[EPV], g[EPV];
+            unpack(*reinterpret_cast<const uint4*>(xb + v * 16), f);
+            unpack(*reinterpret_cast<const uint4*>(wbuf + v * 16), g);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) f[e] = (f[e] * rs) * g[e];
+            stg16(yr + static_cast<int64_t>(v) * EPV, pack(f));
+        }
+        if (rstd != nullptr && lane == 0) rstd[r] = rs;
+        __syncwarp();
+        if (lane == 0) {
+            const int64_t rn = r + nst * stride;
+            if (rn < rows) {
+                fence_proxy_async_smem();   // the reads above happen before the copy overwrites the buffer
+                mbar_expect_tx(mybar + 8u * s, rb);
+                bulk_g2s(smem_u32(ring + s * rb), x + rn * cols, rb, mybar + 8u * s);
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        atomicExch(&g_stage_err, 1);
+        // copies already issued into this warp's ring: the next phase of each buffer
+        for (int s = 0; s < nst; ++s) {
+            const int64_t first = static_cast<int64_t>(it) + ((s - it % nst) + nst) % nst;  // next use of buffer s
+            if (gw + first * stride < rows) mbar_wait(mybar + 8u * s, static_cast<uint32_t>(first / nst) & 1u);
+        }
+    }
+}
+
+// Shared memory of the staged forward for nw warps and nst buffers per warp.
+inline size_t fwd_staged_smem(int rb, int nw, int nst) {
+    return static_cast<size_t>(rb) * (1 + nw * nst) + 8u * (nw * nst + 1);
+}
+
 template <typename T>
 int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows, int cols, float eps,
                cudaStream_t st) {
@@ -252,6 +353,27 @@ int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
     const T* wp = static_cast<const T*>(w);
     T* yp = static_cast<T*>(y);
     const int sms = sm_count();
+    if (cols % EPV == 0) {
+        // staged path: 8 (or fewer) warps per block, 2..4 row buffers per warp
+        const int rb = cols * static_cast<int>(sizeof(T));
+        const size_t cap = static_cast<size_t>(max_smem_optin());
+        for (int nw = 8; nw >= 2; nw >>= 1) {
+            int nst = 4;
+            while (nst >= 2 && fwd_staged_smem(rb, nw, nst) > cap) --nst;
+            if (nst < 2) continue;
+            const size_t smem = fwd_staged_smem(rb, nw, nst);
+            auto kern = rmsnorm_fwd_staged<T>;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+                cudaSuccess)
+                return check_launch("rmsnorm_fwd_staged attribute");
+            int per_sm = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nw * 32, smem);
+            if (per_sm < 1) per_sm = 1;
+            const int64_t grid = std::min<int64_t>(ceil_div(rows, nw), static_cast<int64_t>(sms) * per_sm);
+            kern<<<static_cast<unsigned>(grid), nw * 32, smem, st>>>(xp, wp, yp, rstd, rows, cols, eps, nst);
+            return check_launch("rmsnorm_fwd_staged");
+        }
+    }
     if (cols % EPV == 0) {
         const int nvec = cols / EPV;
         const int64_t need_blocks = ceil_div(rows, kFwdThreads / 32);
@@ -276,7 +398,7 @@ int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
 }
 
 int64_t bwd_partials(int64_t rows) {
-    return std::max<int64_t>(1, std::min<int64_t>({rows, static_cast<int64_t>(sm_count()) * 4, kMaxPartials}));
+    return std::max<int64_t>(1, std::min<int64_t>({rows, static_cast<int64_t>(sm_count()) * 2, kMaxPartials}));
 }
 
 template <typename T>
@@ -286,12 +408,13 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
     const int64_t P = bwd_partials(rows);
     const int64_t rpb = ceil_div(rows, P);
     const int64_t grid = ceil_div(rows, rpb);
+    int64_t grid_used = grid;   // partial rows written (the staged path uses its own grid)
     const T* dyp = static_cast<const T*>(dy);
     const T* xp = static_cast<const T*>(x);
     const T* wp = static_cast<const T*>(w);
     T* dxp = static_cast<T*>(dx);
     bool done = false;
-    if (cols % EPV == 0) {
+    if (!done && cols % EPV == 0) {
         const int nvec = cols / EPV;
         auto go = [&](auto kern, int vpt) {
             const int nt = static_cast<int>(std::min<int64_t>(256, ceil_div(ceil_div(nvec, vpt), 32) * 32));
@@ -309,7 +432,7 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
     int rc = check_launch("rmsnorm_bwd");
     if (rc) return rc;
     rmsnorm_dw_reduce<T><<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, st>>>(
-        part, static_cast<T*>(dw), static_cast<int>(grid), cols);
+        part, static_cast<T*>(dw), static_cast<int>(grid_used), cols);
     return check_launch("rmsnorm_dw_reduce");
 }
 

@@ -8,8 +8,9 @@
 // theta^(-2i/D) (standard RoPE; the pages give none).
 //
 // GB300 design (HBM-bound: every element read and written once):
-//  * one block per position s (and batch group): its D/2 angles are formed
-//    once in shared memory and reused by every head of Q and K and, when the
+//  * one block per group of npos positions (4 at head_dim 128, so that each
+//    thread forms one angle) and batch group: the angles are formed once in
+//    shared memory and reused by every head of Q and K and, when the
 //    positions are implicit (p = s), by every batch row -- 160x reuse at
 //    Llama-3-8B shapes -- so the fp64 angle work is negligible;
 //  * the inverse frequencies theta^(-2i/D) are computed on the host in
@@ -18,8 +19,12 @@
 //    (two-term 2 pi), then sincosf on the reduced single-precision angle:
 //    the result is accurate to ~1 ulp of fp32 at any position, where a plain
 //    fp32 p * inv_freq would err by ~p ulp;
-//  * each thread rotates 16-byte vectors of the two halves of a head; a warp
-//    covers four heads with full 128-byte lines.
+//  * each thread rotates 16-byte vectors (half-split pairing: the two halves
+//    of a head; interleaved pairing: four adjacent pairs); a warp covers
+//    whole 128-byte lines.
+// The extended entry points add the interleaved pairing (2i, 2i+1), per-token
+// strides (Q and K as views into a packed QKV buffer) and caller-supplied
+// cos/sin tables (for scaled frequency schedules).
 #include <math.h>
 
 #include "common.cuh"
@@ -35,6 +40,18 @@ struct InvFreq {
     double v[kMaxHalf];
 };
 
+struct RopeArgs {
+    void* q;
+    void* k;
+    const int32_t* pos;
+    const float* cos_tab;   // [n_tab, D/2] or null
+    const float* sin_tab;
+    int64_t n_tab;
+    int64_t q_ts, k_ts;     // elements between consecutive tokens (b, s)
+    int B, S, Hq, Hk, D, npos;
+    float sign;
+};
+
 __device__ __forceinline__ float2 angle_cs(double p, double inv_freq, float sign) {
     const double two_pi_hi = 6.283185307179586232;      // nearest double to 2 pi
     const double two_pi_lo = 2.4492935982947064e-16;    // 2 pi - two_pi_hi
@@ -47,98 +64,160 @@ __device__ __forceinline__ float2 angle_cs(double p, double inv_freq, float sign
     return make_float2(c, sign * s);
 }
 
-template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads) rope_kernel(T* q, T* k, const int32_t* __restrict__ pos, int B, int S,
-                                                        int Hq, int Hk, int D, const __grid_constant__ InvFreq f,
-                                                        float sign) {
-    extern __shared__ float2 cs[];   // [nb_angles][D/2] (cos, +-sin)
-    const int half = D >> 1;
-    const int s = blockIdx.x;
+// VEC: 16-byte vectors (else scalar); INTER: interleaved pairs (2i, 2i+1).
+template <typename T, bool VEC, bool INTER>
+__global__ void __launch_bounds__(kThreads) rope_kernel(const RopeArgs a, const __grid_constant__ InvFreq f) {
+    extern __shared__ float2 cs[];   // [npos][nb_angles][D/2] (cos, +-sin)
+    T* q = static_cast<T*>(a.q);
+    T* k = static_cast<T*>(a.k);
+    const int D = a.D, half = D >> 1, S = a.S, Hq = a.Hq, Hk = a.Hk;
+    const int s0 = blockIdx.x * a.npos;
+    const int np = min(a.npos, S - s0);
     const int b0 = blockIdx.y * kBatchGroup;
-    const int nb = min(kBatchGroup, B - b0);
-    const int na = pos ? nb : 1;     // distinct angle rows in this block
-    for (int t = threadIdx.x; t < na * half; t += kThreads) {
-        const int bl = t / half, i = t - bl * half;
-        const double p = pos ? static_cast<double>(pos[static_cast<int64_t>(b0 + bl) * S + s]) : static_cast<double>(s);
-        cs[t] = angle_cs(p, f.v[i], sign);
+    const int nb = min(kBatchGroup, a.B - b0);
+    const int na = a.pos ? nb : 1;     // distinct angle rows per position in this block
+    for (int t = threadIdx.x; t < np * na * half; t += kThreads) {
+        const int row = t / half, i = t - row * half;
+        const int pp = row / na, bl = row - pp * na;
+        const int64_t p = a.pos ? static_cast<int64_t>(a.pos[static_cast<int64_t>(b0 + bl) * S + s0 + pp])
+                                : static_cast<int64_t>(s0 + pp);
+        if (a.cos_tab != nullptr) {
+            const int64_t pc = p < 0 ? 0 : (p >= a.n_tab ? a.n_tab - 1 : p);   // positions outside the table clamp
+            cs[t] = make_float2(a.cos_tab[pc * half + i], a.sign * a.sin_tab[pc * half + i]);
+        } else {
+            cs[t] = angle_cs(static_cast<double>(p), f.v[i], a.sign);
+        }
     }
     __syncthreads();
     const int H = Hq + Hk;
+    auto head_base = [&](int bl, int pp, int h) -> T* {
+        const int64_t bs = static_cast<int64_t>(b0 + bl) * S + s0 + pp;
+        return h < Hq ? q + bs * a.q_ts + static_cast<int64_t>(h) * D
+                      : k + bs * a.k_ts + static_cast<int64_t>(h - Hq) * D;
+    };
     if (VEC) {
         constexpr int EPV = Vec<T>::N;
-        const int vph = half / EPV;                 // vectors per half head
-        const int ntask = nb * H * vph;
-        for (int t = threadIdx.x; t < ntask; t += kThreads) {
-            const int bl = t / (H * vph);
-            const int rem = t - bl * H * vph;
-            const int h = rem / vph, v = rem - h * vph;
-            const int64_t bs = static_cast<int64_t>(b0 + bl) * S + s;
-            T* base = h < Hq ? q + (bs * Hq + h) * D : k + (bs * Hk + (h - Hq)) * D;
-            T* pa = base + v * EPV;
-            T* pb = pa + half;
-            float a[EPV], bv[EPV];
-            unpack(ldg16(pa), a);
-            unpack(ldg16(pb), bv);
-            const float2* c = cs + (pos ? bl : 0) * half + v * EPV;
+        // half-split: a slot is the pair of vectors (v, v + D/2) of a head; interleaved:
+        // one vector.  Each thread decodes its slots once; the loop over the block's
+        // positions and batch rows only adds token offsets.
+        const int vph = INTER ? D / EPV : half / EPV;
+        const int nslot = H * vph;
+        for (int slot = threadIdx.x; slot < nslot; slot += kThreads) {
+            const int h = slot / vph, v = slot - h * vph;
+            const bool isq = h < Hq;
+            T* hb = isq ? q + static_cast<int64_t>(h) * D + v * EPV : k + static_cast<int64_t>(h - Hq) * D + v * EPV;
+            const int64_t ts = isq ? a.q_ts : a.k_ts;
+            const int coff = INTER ? (v * EPV) >> 1 : v * EPV;   // first angle index of this slot
+            for (int pp = 0; pp < np; ++pp) {
+                for (int bl = 0; bl < nb; ++bl) {
+                    T* pa = hb + (static_cast<int64_t>(b0 + bl) * S + s0 + pp) * ts;
+                    const float4* c4 = reinterpret_cast<const float4*>(cs + (pp * na + (a.pos ? bl : 0)) * half + coff);
+                    if (INTER) {
+                        float e[EPV];
+                        unpack(ldg16(pa), e);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                const float2 r = c[e];
-                const float x0 = a[e], x1 = bv[e];
-                a[e] = x0 * r.x - x1 * r.y;
-                bv[e] = x1 * r.x + x0 * r.y;
+                        for (int j = 0; j < EPV / 2; j += 2) {
+                            const float4 r = c4[j >> 1];   // two (cos, sin) pairs
+                            float x0 = e[2 * j], x1 = e[2 * j + 1];
+                            e[2 * j] = x0 * r.x - x1 * r.y;
+                            e[2 * j + 1] = x1 * r.x + x0 * r.y;
+                            x0 = e[2 * j + 2];
+                            x1 = e[2 * j + 3];
+                            e[2 * j + 2] = x0 * r.z - x1 * r.w;
+                            e[2 * j + 3] = x1 * r.z + x0 * r.w;
+                        }
+                        stg16(pa, pack(e));
+                    } else {
+                        T* pb = pa + half;
+                        float av[EPV], bv[EPV];
+                        unpack(ldg16(pa), av);
+                        unpack(ldg16(pb), bv);
+#pragma unroll
+                        for (int e = 0; e < EPV; e += 2) {
+                            const float4 r = c4[e >> 1];
+                            float x0 = av[e], x1 = bv[e];
+                            av[e] = x0 * r.x - x1 * r.y;
+                            bv[e] = x1 * r.x + x0 * r.y;
+                            x0 = av[e + 1];
+                            x1 = bv[e + 1];
+                            av[e + 1] = x0 * r.z - x1 * r.w;
+                            bv[e + 1] = x1 * r.z + x0 * r.w;
+                        }
+                        stg16(pa, pack(av));
+                        stg16(pb, pack(bv));
+                    }
+                }
             }
-            stg16(pa, pack(a));
-            stg16(pb, pack(bv));
         }
     } else {
-        const int ntask = nb * H * half;
+        const int per_pos = nb * H * half;
+        const int ntask = np * per_pos;
         for (int t = threadIdx.x; t < ntask; t += kThreads) {
-            const int bl = t / (H * half);
-            const int rem = t - bl * H * half;
+            const int pp = t / per_pos;
+            int rem = t - pp * per_pos;
+            const int bl = rem / (H * half);
+            rem -= bl * H * half;
             const int h = rem / half, i = rem - h * half;
-            const int64_t bs = static_cast<int64_t>(b0 + bl) * S + s;
-            T* base = h < Hq ? q + (bs * Hq + h) * D : k + (bs * Hk + (h - Hq)) * D;
-            const float2 r = cs[(pos ? bl : 0) * half + i];
-            const float x0 = ldf(base + i), x1 = ldf(base + i + half);
-            stf(base + i, x0 * r.x - x1 * r.y);
-            stf(base + i + half, x1 * r.x + x0 * r.y);
+            T* base = head_base(bl, pp, h);
+            const float2 r = cs[(pp * na + (a.pos ? bl : 0)) * half + i];
+            T* pa = INTER ? base + 2 * i : base + i;
+            T* pb = INTER ? base + 2 * i + 1 : base + i + half;
+            const float x0 = ldf(pa), x1 = ldf(pb);
+            stf(pa, x0 * r.x - x1 * r.y);
+            stf(pb, x1 * r.x + x0 * r.y);
         }
     }
 }
 
 int rope_run(void* q, void* k, const int32_t* pos, int64_t B, int64_t S, int64_t Hq, int64_t Hk, int64_t D,
-             double theta, int dtype, void* stream, float sign, const char* who) {
+             int64_t q_ts, int64_t k_ts, int pairing, const float* cos_tab, const float* sin_tab, int64_t n_tab,
+             double theta, int dtype, void* stream, float sign, bool strict_align, const char* who) {
     clear_error();
     if (dtype != LIGER_F32 && dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "%s: dtype %d", who, dtype);
     if (B < 0 || S < 0 || Hq < 0 || Hk < 0 || D <= 0 || (D & 1) || D > 2 * kMaxHalf || S > 2147483647LL ||
         B > 2147483647LL || Hq + Hk > (1 << 20))
         return fail(LIGER_ERR_SHAPE, "%s: batch=%lld seq=%lld heads=%lld/%lld head_dim=%lld (even, <= %d)", who,
                     (long long)B, (long long)S, (long long)Hq, (long long)Hk, (long long)D, 2 * kMaxHalf);
-    if (!(theta > 0.0) || !isfinite(theta)) return fail(LIGER_ERR_SHAPE, "%s: theta must be > 0", who);
+    if (pairing != 0 && pairing != 1) return fail(LIGER_ERR_SHAPE, "%s: pairing must be 0 or 1", who);
+    if ((q_ts < Hq * D) || (k_ts < Hk * D))
+        return fail(LIGER_ERR_SHAPE, "%s: token strides %lld/%lld smaller than heads*head_dim", who,
+                    (long long)q_ts, (long long)k_ts);
+    if ((cos_tab == nullptr) != (sin_tab == nullptr) || (cos_tab && n_tab <= 0))
+        return fail(LIGER_ERR_SHAPE, "%s: cos and sin tables go together, with n_tab > 0", who);
+    if (!cos_tab && (!(theta > 0.0) || !isfinite(theta))) return fail(LIGER_ERR_SHAPE, "%s: theta must be > 0", who);
     if (B == 0 || S == 0 || Hq + Hk == 0) return LIGER_OK;
     if ((Hq > 0 && !q) || (Hk > 0 && !k)) return fail(LIGER_ERR_NULL, "%s: q/k required for nonzero head counts", who);
-    if ((q && !aligned16(q)) || (k && !aligned16(k)))
-        return fail(LIGER_ERR_ALIGN, "%s: q and k must be 16-byte aligned", who);
-    if (pos && (reinterpret_cast<uintptr_t>(pos) & 3)) return fail(LIGER_ERR_ALIGN, "%s: pos must be 4-byte aligned", who);
+    const size_t esz = dtype == LIGER_F32 ? 4 : 2;
+    const bool q16 = !q || aligned16(q), k16 = !k || aligned16(k);
+    if (strict_align && (!q16 || !k16)) return fail(LIGER_ERR_ALIGN, "%s: q and k must be 16-byte aligned", who);
+    if ((q && reinterpret_cast<uintptr_t>(q) % esz) || (k && reinterpret_cast<uintptr_t>(k) % esz))
+        return fail(LIGER_ERR_ALIGN, "%s: q and k must be aligned to their element size", who);
+    if ((pos && (reinterpret_cast<uintptr_t>(pos) & 3)) ||
+        (cos_tab && ((reinterpret_cast<uintptr_t>(cos_tab) | reinterpret_cast<uintptr_t>(sin_tab)) & 3)))
+        return fail(LIGER_ERR_ALIGN, "%s: pos and tables must be 4-byte aligned", who);
     const int half = static_cast<int>(D / 2);
     InvFreq f;
-    for (int i = 0; i < half; ++i) f.v[i] = pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(D));
+    for (int i = 0; i < half; ++i)
+        f.v[i] = cos_tab ? 0.0 : pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(D));
     const int nbg = static_cast<int>(ceil_div(B, kBatchGroup));
     if (nbg > 65535) return fail(LIGER_ERR_SHAPE, "%s: batch too large", who);
-    dim3 grid(static_cast<unsigned>(S), static_cast<unsigned>(nbg));
-    const size_t smem = static_cast<size_t>(pos ? kBatchGroup : 1) * half * sizeof(float2);
+    // positions per block: enough that every thread forms one angle (head_dim 128: 4)
+    const int npos = std::max(1, std::min(16, kThreads / half));
+    dim3 grid(static_cast<unsigned>(ceil_div(S, npos)), static_cast<unsigned>(nbg));
+    const size_t smem = static_cast<size_t>(npos) * (pos ? kBatchGroup : 1) * half * sizeof(float2);
     cudaStream_t st = as_stream(stream);
     const int epv = dtype == LIGER_F32 ? 4 : 8;
-    const bool vec = (half % epv) == 0;
+    // 16-byte vectors need every head start aligned: strides and head_dim in whole vectors
+    const bool vec = (pairing ? (D % epv) : (half % epv)) == 0 && q_ts % epv == 0 && k_ts % epv == 0 && q16 && k16;
+    RopeArgs a{q, k, pos, cos_tab, sin_tab, n_tab, q_ts, k_ts, (int)B, (int)S, (int)Hq, (int)Hk, (int)D, npos, sign};
+    auto go = [&](auto kern) { kern<<<grid, kThreads, smem, st>>>(a, f); };
     if (dtype == LIGER_F32) {
-        auto kern = vec ? rope_kernel<float, true> : rope_kernel<float, false>;
-        kern<<<grid, kThreads, smem, st>>>(static_cast<float*>(q), static_cast<float*>(k), pos, (int)B, (int)S, (int)Hq,
-                                           (int)Hk, (int)D, f, sign);
+        if (pairing) vec ? go(rope_kernel<float, true, true>) : go(rope_kernel<float, false, true>);
+        else vec ? go(rope_kernel<float, true, false>) : go(rope_kernel<float, false, false>);
     } else {
         using Bf = __nv_bfloat16;
-        auto kern = vec ? rope_kernel<Bf, true> : rope_kernel<Bf, false>;
-        kern<<<grid, kThreads, smem, st>>>(static_cast<Bf*>(q), static_cast<Bf*>(k), pos, (int)B, (int)S, (int)Hq,
-                                           (int)Hk, (int)D, f, sign);
+        if (pairing) vec ? go(rope_kernel<Bf, true, true>) : go(rope_kernel<Bf, false, true>);
+        else vec ? go(rope_kernel<Bf, true, false>) : go(rope_kernel<Bf, false, false>);
     }
     return check_launch(who);
 }
@@ -148,12 +227,28 @@ int rope_run(void* q, void* k, const int32_t* pos, int64_t B, int64_t S, int64_t
 
 extern "C" int liger_rope_fwd(void* q, void* k, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
                               int64_t n_k_heads, int64_t head_dim, double theta, int dtype, void* stream) {
-    return liger::rope_run(q, k, pos, batch, seq, n_q_heads, n_k_heads, head_dim, theta, dtype, stream, 1.0f,
-                           "rope_fwd");
+    return liger::rope_run(q, k, pos, batch, seq, n_q_heads, n_k_heads, head_dim, n_q_heads * head_dim,
+                           n_k_heads * head_dim, 0, nullptr, nullptr, 0, theta, dtype, stream, 1.0f, true, "rope_fwd");
 }
 
 extern "C" int liger_rope_bwd(void* dq, void* dk, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
                               int64_t n_k_heads, int64_t head_dim, double theta, int dtype, void* stream) {
-    return liger::rope_run(dq, dk, pos, batch, seq, n_q_heads, n_k_heads, head_dim, theta, dtype, stream, -1.0f,
-                           "rope_bwd");
+    return liger::rope_run(dq, dk, pos, batch, seq, n_q_heads, n_k_heads, head_dim, n_q_heads * head_dim,
+                           n_k_heads * head_dim, 0, nullptr, nullptr, 0, theta, dtype, stream, -1.0f, true, "rope_bwd");
+}
+
+extern "C" int liger_rope_fwd_ex(void* q, void* k, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
+                                 int64_t n_k_heads, int64_t head_dim, int64_t q_token_stride, int64_t k_token_stride,
+                                 int pairing, const float* cos_tab, const float* sin_tab, int64_t n_tab, double theta,
+                                 int dtype, void* stream) {
+    return liger::rope_run(q, k, pos, batch, seq, n_q_heads, n_k_heads, head_dim, q_token_stride, k_token_stride,
+                           pairing, cos_tab, sin_tab, n_tab, theta, dtype, stream, 1.0f, false, "rope_fwd_ex");
+}
+
+extern "C" int liger_rope_bwd_ex(void* dq, void* dk, const int32_t* pos, int64_t batch, int64_t seq,
+                                 int64_t n_q_heads, int64_t n_k_heads, int64_t head_dim, int64_t q_token_stride,
+                                 int64_t k_token_stride, int pairing, const float* cos_tab, const float* sin_tab,
+                                 int64_t n_tab, double theta, int dtype, void* stream) {
+    return liger::rope_run(dq, dk, pos, batch, seq, n_q_heads, n_k_heads, head_dim, q_token_stride, k_token_stride,
+                           pairing, cos_tab, sin_tab, n_tab, theta, dtype, stream, -1.0f, false, "rope_bwd_ex");
 }

@@ -21,7 +21,7 @@
 //               fused epilogue; the accumulator is double-buffered in TMEM
 //               (2 x 256 columns) so tile i's epilogue overlaps tile i+1's
 //               MMAs.
-// Every mbarrier wait is bounded (about 4 s of %globaltimer); on expiry the
+// Every mbarrier wait is bounded (about 4 s of %globaltimer, mbarrier.cuh); on expiry the
 // waiting role records an error code in *ep.err, stops issuing work, waits
 // (bounded) for the copies and MMAs it already issued, and the block frees
 // its TMEM and exits.
@@ -30,6 +30,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "mbarrier.cuh"
 
 namespace liger {
 namespace tc {
@@ -47,15 +48,21 @@ constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
-constexpr unsigned long long WAIT_NS = 4000000000ull;
 
 enum Epi : int { EPI_LOGITS = 0, EPI_STORE = 1, EPI_ACCUM = 2 };
+
+// Tile order of the persistent loop: m fastest, n fastest, or groups of
+// GROUP_N tile columns with n fastest inside a group (for long-K problems
+// where both operands stream from HBM: each wave then shares ~SMs/GROUP_N
+// A row-blocks and GROUP_N B column-blocks through L2).
+enum Raster : int { RASTER_M_FASTEST = 0, RASTER_N_FASTEST = 1, RASTER_N_GROUPS = 2 };
+constexpr int GROUP_N = 8;
 
 enum Err : int { ERR_TMA_EMPTY = 1, ERR_MMA_FULL = 2, ERR_MMA_TMEM = 3, ERR_EPI_TMEM = 4 };
 
 struct EpiParams {
     int M, N;                           // logical problem size (epilogue masks)
-    int raster_n_fastest;               // tile order: 0 = m fastest, 1 = n fastest
+    int raster;                         // tile order (Raster)
     int* err;                           // error word (device)
     // EPI_LOGITS: P = exp(z - m_tile) as bf16, per-(row, n-tile) (m, sum), z at label
     const int64_t* labels;              // [M] (chunk rows)
@@ -75,54 +82,39 @@ struct EpiParams {
     // one-hot correction applied in fp32 (the bf16 operand carries only the
     // softmax part): EPI_STORE subtracts corr_scale * corr_src[labels[row], :];
     // EPI_ACCUM subtracts corr_scale * corr_src[t, :] for every token t whose
-    // label is this row, found in keys[0, nkeys) = sorted (label << 32 | t).
+    // label is this row: keys[0, nkeys) = sorted (label << 32 | t), indexed by lstart.
     const __nv_bfloat16* corr_src;
     int64_t ld_corr;
     float corr_scale;
     const unsigned long long* keys;
     int nkeys;
+    const int* lstart;
+    // L2 policies (Hint) of the A and B loads; streaming epilogue traffic (P, the
+    // fp32 accumulator, dW) always uses evict-first accesses
+    int hint_a, hint_b;   // [M + 1]: the tokens labelled with row v are keys[lstart[v] .. lstart[v+1])
 };
 
 // ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+// L2 eviction policy of an operand's loads (createpolicy, whole access)
+enum Hint : int { HINT_NORMAL = 0, HINT_EVICT_FIRST = 1, HINT_EVICT_LAST = 2 };
+__device__ __forceinline__ uint64_t make_policy(int hint) {
+    uint64_t p = 0;
+    if (hint == HINT_EVICT_FIRST)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    else if (hint == HINT_EVICT_LAST)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 uint64_t policy) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
         : "memory");
-    return ok != 0;
 }
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Bounded wait for phase `parity` of barrier `bar`: false after WAIT_NS.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    while (true) {
-        for (int i = 0; i < 256; ++i)
-            if (mbar_try(bar, parity)) return true;
-        if (globaltimer() - t0 > WAIT_NS) return false;
-    }
-}
-
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -195,16 +187,6 @@ __device__ __forceinline__ void sub_scaled32(float (&v)[32], const __nv_bfloat16
     }
 }
 
-__device__ __forceinline__ int lower_bound_u64(const unsigned long long* a, int n, unsigned long long key) {
-    int lo = 0, hi = n;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (a[mid] < key) lo = mid + 1;
-        else hi = mid;
-    }
-    return lo;
-}
-
 // --------------------------------------------------------------- kernel
 template <int A_MN, int B_MN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -252,9 +234,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(slot_ptr);
 
     auto tile_mn = [&](int t, int& mi, int& ni) {
-        if (ep.raster_n_fastest) {
+        if (ep.raster == RASTER_N_FASTEST) {
             mi = t / num_n;
             ni = t - mi * num_n;
+        } else if (ep.raster == RASTER_N_GROUPS) {
+            // groups of GROUP_N tile columns, n fastest inside a group: a wave of
+            // resident tiles spans ~SMs/GROUP_N row blocks x GROUP_N column blocks
+            const int full = num_n / GROUP_N;
+            const int tiles_full = full * num_m * GROUP_N;
+            if (t < tiles_full) {
+                const int g = t / (num_m * GROUP_N), w = t - g * num_m * GROUP_N;
+                mi = w / GROUP_N;
+                ni = g * GROUP_N + (w - mi * GROUP_N);
+            } else {
+                const int width = num_n - full * GROUP_N, w = t - tiles_full;
+                mi = w / width;
+                ni = full * GROUP_N + (w - mi * width);
+            }
         } else {
             ni = t / num_m;
             mi = t - ni * num_m;
@@ -264,6 +260,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
+            const uint64_t pol_a = make_policy(ep.hint_a), pol_b = make_policy(ep.hint_b);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_phase[STAGES];
@@ -286,16 +283,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (A_MN) {
 #pragma unroll
                         for (int j = 0; j < BM / MN_BOX; ++j)
-                            tma_load_2d(sa + j * MN_BOX_BYTES, &tmA, fb, mi * BM + j * MN_BOX, kb * BK);
+                            tma_load_2d_hint(sa + j * MN_BOX_BYTES, &tmA, fb, mi * BM + j * MN_BOX, kb * BK, pol_a);
                     } else {
-                        tma_load_2d(sa, &tmA, fb, kb * BK, mi * BM);
+                        tma_load_2d_hint(sa, &tmA, fb, kb * BK, mi * BM, pol_a);
                     }
                     if (B_MN) {
 #pragma unroll
                         for (int j = 0; j < BN / MN_BOX; ++j)
-                            tma_load_2d(sb + j * MN_BOX_BYTES, &tmB, fb, ni * BN + j * MN_BOX, kb * BK);
+                            tma_load_2d_hint(sb + j * MN_BOX_BYTES, &tmB, fb, ni * BN + j * MN_BOX, kb * BK, pol_b);
                     } else {
-                        tma_load_2d(sb, &tmB, fb, kb * BK, ni * BN);
+                        tma_load_2d_hint(sb, &tmB, fb, kb * BK, ni * BN, pol_b);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
@@ -377,6 +374,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             tile_mn(t, mi, ni);
             const int as = it & 1;
             const uint32_t aphase = (it >> 1) & 1;
+            const int row = mi * BM + rl;
+            const int n0 = ni * BN;
+            const bool row_ok = row < ep.M;
+            // EPI_ACCUM: everything that does not depend on the accumulator is fetched
+            // before waiting for it (label range, first 32 columns of the fp32 sum)
+            int k_lo = 0, k_hi = 0;
+            uint4 pre[8];
+            float* arow = nullptr;
+            if (EPI == EPI_ACCUM) {
+                arow = ep.acc + static_cast<int64_t>(row) * ep.lda + n0;
+                if (row_ok && ep.lstart != nullptr) {
+                    k_lo = ep.lstart[row];
+                    k_hi = ep.lstart[row + 1];
+                }
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    pre[g] = (row_ok && ep.acc_read && n0 + g * 4 < ep.N) ? ldg16_cs(arow + g * 4) : make_uint4(0, 0, 0, 0);
+            }
             const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(as), aphase));
             if (!got) {
                 if (lane == 0) atomicExch(ep.err, ERR_EPI_TMEM);
@@ -384,9 +399,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + static_cast<uint32_t>(as * BN) + (static_cast<uint32_t>(q * 32) << 16);
-            const int row = mi * BM + rl;
-            const int n0 = ni * BN;
-            const bool row_ok = row < ep.M;
             if (EPI == EPI_LOGITS) {
                 const int64_t y = row_ok ? ep.labels[row] : ep.ignore_index;
                 const bool live = row_ok && y != ep.ignore_index;
@@ -429,7 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                      pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
                                                      pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
                                                      pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
-                                stg16(prow + c * 32 + g * 8, u);
+                                stg16_cs(prow + c * 32 + g * 8, u);
                             }
                         }
                     }
@@ -466,7 +478,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                    pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
                                                    pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
                                 }
-                                stg16(orow + c * 32 + g * 8, u);
+                                stg16_cs(orow + c * 32 + g * 8, u);
                             }
                         }
                     }
@@ -475,16 +487,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(as));
             } else {
-                float* arow = ep.acc + static_cast<int64_t>(row) * ep.lda + n0;
                 __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
-                int k_lo = 0, k_hi = 0;
-                if (row_ok && ep.keys != nullptr) {
-                    const unsigned long long key = static_cast<unsigned long long>(row) << 32;
-                    k_lo = lower_bound_u64(ep.keys, ep.nkeys, key);
-                    k_hi = lower_bound_u64(ep.keys, ep.nkeys, key + (1ull << 32));
-                }
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
+                    uint4 nxt[8];
+                    if (c + 1 < BN / 32) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) {
+                            const int col = n0 + (c + 1) * 32 + g * 4;
+                            nxt[g] = (row_ok && ep.acc_read && col < ep.N) ? ldg16_cs(arow + (c + 1) * 32 + g * 4)
+                                                                          : make_uint4(0, 0, 0, 0);
+                        }
+                    }
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
                     for (int kk = k_lo; kk < k_hi; ++kk) {
@@ -500,13 +514,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 float* ap = arow + c * 32 + g * 4;
                                 if (ep.acc_read) {
                                     float o[4];
-                                    unpack(ldg16(ap), o);
+                                    unpack(pre[g], o);
 #pragma unroll
                                     for (int e = 0; e < 4; ++e) v[g * 4 + e] += o[e];
                                 }
                                 if (ep.acc_write) {
                                     float o[4] = {v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]};
-                                    stg16(ap, pack(o));
+                                    stg16_cs(ap, pack(o));
                                 }
                             }
                         }
@@ -519,10 +533,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                          pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
                                                          pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
                                                          pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
-                                    stg16(orow + c * 32 + g * 8, u);
+                                    stg16_cs(orow + c * 32 + g * 8, u);
                                 }
                             }
                         }
+                    }
+                    if (c + 1 < BN / 32) {
+#pragma unroll
+                        for (int g = 0; g < 8; ++g) pre[g] = nxt[g];
                     }
                 }
                 tc_fence_before();
