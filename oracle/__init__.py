@@ -55,13 +55,16 @@ def _load():
             lib.orc_rope.argtypes = [_P, ctypes.c_int, _P, _I, _I, _I, _I, _D, ctypes.c_int, _P]
             lib.orc_rope_ex.argtypes = [_P, ctypes.c_int, _P, _I, _I, _I, _I, _D, ctypes.c_int, ctypes.c_int, _P, _P,
                                         _I, _P]
+            lib.orc_linear_swiglu_fwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _I, _I, _P]
+            lib.orc_linear_swiglu_bwd.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I, _I, _I, _P, _P, _P]
             lib.orc_swiglu_fwd.argtypes = [_P, _P, ctypes.c_int, _I, _P]
             lib.orc_swiglu_bwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _P, _P]
             lib.orc_linear_ce.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
                                           _P, _P, _P, _P]
             lib.orc_linear_ce_rows.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
                                                _P, _I, _P, _P, _P]
-            for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_rope", "orc_rope_ex", "orc_swiglu_fwd", "orc_swiglu_bwd",
+            for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_rope", "orc_rope_ex", "orc_swiglu_fwd", "orc_swiglu_bwd", "orc_linear_swiglu_fwd",
+                      "orc_linear_swiglu_bwd",
                       "orc_linear_ce", "orc_linear_ce_rows"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -153,6 +156,25 @@ def swiglu_bwd(dy, g, u):
     _check(_load().orc_swiglu_bwd(pdy, pg, pu, _dt(dy, g, u), g.size, dg.ctypes.data, du.ctypes.data),
            "swiglu_bwd")
     return dg, du
+
+
+def linear_swiglu_fwd(X, Wg, Wu):
+    """FusedLinearSwiGLU forward: silu(X Wg^T) * (X Wu^T)."""
+    X, pX = _c(X); Wg, pg = _c(Wg); Wu, pu = _c(Wu)
+    T, H = X.shape; I = Wg.shape[0]
+    out = np.empty((T, I), np.float64)
+    _check(_load().orc_linear_swiglu_fwd(pX, pg, pu, _dt(X, Wg, Wu), T, H, I, out.ctypes.data), "linear_swiglu_fwd")
+    return out
+
+
+def linear_swiglu_bwd(X, Wg, Wu, dH):
+    """FusedLinearSwiGLU backward: (dX, dWg, dWu)."""
+    X, pX = _c(X); Wg, pg = _c(Wg); Wu, pu = _c(Wu); dH, pd = _c(dH)
+    T, H = X.shape; I = Wg.shape[0]
+    dX = np.empty((T, H), np.float64); dWg = np.empty((I, H), np.float64); dWu = np.empty((I, H), np.float64)
+    _check(_load().orc_linear_swiglu_bwd(pX, pg, pu, pd, _dt(X, Wg, Wu, dH), T, H, I, dX.ctypes.data,
+                                         dWg.ctypes.data, dWu.ctypes.data), "linear_swiglu_bwd")
+    return dX, dWg, dWu
 
 
 def linear_ce(X, W, labels, ignore_index=-100, reduction="mean", grad_scale=1.0, want_grads=True):

@@ -186,6 +186,51 @@ int orc_swiglu_bwd(const void* dy, const void* g, const void* u, int dt, int64_t
     return 0;
 }
 
+/* ------------------------------------------------------ linear + SwiGLU
+ * [P1] section "算子融合", FusedLinearSwiGLU paragraph: the gate and up
+ * projections of the same input, SiLU of the gate times the up branch.
+ * READING: no bias (the page's module is built with bias=False); the
+ * backward is the chain rule through the SwiGLU derivative above. */
+static double dot_row(const void* A, const void* B, int dt, int64_t a_off, int64_t b_off, int64_t n) {
+    double acc = 0.0;
+    for (int64_t h = 0; h < n; ++h) acc += ld(A, dt, a_off + h) * ld(B, dt, b_off + h);
+    return acc;
+}
+
+int orc_linear_swiglu_fwd(const void* X, const void* Wg, const void* Wu, int dt, int64_t T, int64_t H, int64_t I,
+                          double* out) {
+    if (!X || !Wg || !Wu || !out || T < 0 || H <= 0 || I <= 0 || bad_dt(dt)) return -1;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t i = 0; i < I; ++i) {
+            double g = dot_row(X, Wg, dt, t * H, i * H, H);
+            double u = dot_row(X, Wu, dt, t * H, i * H, H);
+            out[t * I + i] = g * sigmoid(g) * u;
+        }
+    return 0;
+}
+
+int orc_linear_swiglu_bwd(const void* X, const void* Wg, const void* Wu, const void* dH, int dt, int64_t T, int64_t H,
+                          int64_t I, double* dX, double* dWg, double* dWu) {
+    if (!X || !Wg || !Wu || !dH || !dX || !dWg || !dWu || T < 0 || H <= 0 || I <= 0 || bad_dt(dt)) return -1;
+    for (int64_t k = 0; k < T * H; ++k) dX[k] = 0.0;
+    for (int64_t k = 0; k < I * H; ++k) dWg[k] = dWu[k] = 0.0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t i = 0; i < I; ++i) {
+            double g = dot_row(X, Wg, dt, t * H, i * H, H);
+            double u = dot_row(X, Wu, dt, t * H, i * H, H);
+            double s = sigmoid(g), d = ld(dH, dt, t * I + i);
+            double dg = d * u * s * (1.0 + g * (1.0 - s));
+            double du = d * g * s;
+            for (int64_t h = 0; h < H; ++h) {
+                double x = ld(X, dt, t * H + h);
+                dX[t * H + h] += dg * ld(Wg, dt, i * H + h) + du * ld(Wu, dt, i * H + h);
+                dWg[i * H + h] += dg * x;
+                dWu[i * H + h] += du * x;
+            }
+        }
+    return 0;
+}
+
 /* ---------------------------------------------------------- linear + CE
  * [P1] section "算子融合", FusedCrossEntropyLoss paragraph: softmax and the
  * negative log-likelihood are one step taken straight on the classifier-head

@@ -49,6 +49,13 @@ int orc_rope_ex(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S,
 int orc_swiglu_fwd(const void* g, const void* u, int dt, int64_t n, double* y);
 int orc_swiglu_bwd(const void* dy, const void* g, const void* u, int dt, int64_t n, double* dg, double* du);
 
+/* FusedLinearSwiGLU: out = silu(X Wg^T) * (X Wu^T), X [T, H], Wg / Wu [I, H];
+ * backward from dH [T, I]: dX [T, H], dWg, dWu [I, H]. */
+int orc_linear_swiglu_fwd(const void* X, const void* Wg, const void* Wu, int dt, int64_t T, int64_t H, int64_t I,
+                          double* out);
+int orc_linear_swiglu_bwd(const void* X, const void* Wg, const void* Wu, const void* dH, int dt, int64_t T, int64_t H,
+                          int64_t I, double* dX, double* dWg, double* dWu);
+
 /* Linear cross-entropy, unchunked.  z = X W^T; lse; loss over rows with
  * label != ignore_index (mean: divided by their count; sum: not); D = scale *
  * (softmax(z) - onehot), scale = grad_scale / n_valid (mean) or grad_scale

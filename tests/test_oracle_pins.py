@@ -250,3 +250,23 @@ def test_rope_ex_table_matches_schedule_and_inverse():
     # a table that is not a rotation (scaled cos) is applied as given
     s = oracle.rope_ex(np.ones((1, 1, 1, 2)), 0.0, cos_tab=np.array([[0.5]]), sin_tab=np.array([[0.0]]))
     assert np.allclose(s[0, 0, 0], [0.5, 0.5])
+
+
+# ------------------------------------------------------- FusedLinearSwiGLU
+def test_linear_swiglu_identity_weights_golden():
+    g = golden("silu_values.json")
+    X = np.array([[1.0, -1.0, 0.0]]); E = np.eye(3)
+    out = oracle.linear_swiglu_fwd(X, E, E)                 # silu(x) * x
+    assert abs(out[0, 0] - g["silu_1"]) < 1e-15 and abs(out[0, 1] - (-g["silu_m1"])) < 1e-15 and out[0, 2] == 0.0
+    assert np.all(oracle.linear_swiglu_fwd(X, E, np.zeros((3, 3))) == 0.0)   # up = 0
+
+
+def test_linear_swiglu_bwd_finite_differences():
+    T, H, I = 3, 4, 5
+    X = RNG.standard_normal((T, H)); Wg = RNG.standard_normal((I, H)); Wu = RNG.standard_normal((I, H))
+    dH = RNG.standard_normal((T, I))
+    dX, dWg, dWu = oracle.linear_swiglu_bwd(X, Wg, Wu, dH)
+    L = lambda xx, gg, uu: float(np.sum(dH * oracle.linear_swiglu_fwd(xx, gg, uu)))
+    assert np.max(np.abs(dX - _fd(lambda v: L(v, Wg, Wu), X))) < 1e-7
+    assert np.max(np.abs(dWg - _fd(lambda v: L(X, v, Wu), Wg))) < 1e-7
+    assert np.max(np.abs(dWu - _fd(lambda v: L(X, Wg, v), Wu))) < 1e-7
