@@ -239,6 +239,38 @@ def isolated_times(chain, dev, n=10):
     return out
 
 
+def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
+    """FusedLinearSwiGLU at the pages' MLP shape (8192 tokens, hidden 4096,
+    intermediate 11008), forward and backward alone: ms and TFLOP/s
+    (forward 4*T*H*I flops; backward 12*T*H*I: recompute, dX, dW)."""
+    import torch
+    from datagen import normal
+    X = to_torch(normal(5, "mlp.X", (T, H), "bf16"), dev)
+    Wg = to_torch(normal(5, "mlp.Wg", (I, H), "bf16", 0.0, 0.02), dev)
+    Wu = to_torch(normal(5, "mlp.Wu", (I, H), "bf16", 0.0, 0.02), dev)
+    dH = to_torch(normal(5, "mlp.dH", (T, I), "bf16"), dev)
+    out = torch.empty(T, I, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(L.liger_fused_linear_swiglu_workspace(T, I), dtype=torch.uint8, device=dev)
+    dX, dWg, dWu = torch.empty_like(X), torch.empty_like(Wg), torch.empty_like(Wu)
+    res = {}
+    for name, fn, fl in (("fwd", lambda: L.liger_fused_linear_swiglu_fwd(X, Wg, Wu, out), 4 * T * H * I),
+                         ("bwd", lambda: L.liger_fused_linear_swiglu_bwd(X, Wg, Wu, dH, dX, dWg, dWu, ws),
+                          12 * T * H * I)):
+        fn()
+        fn()
+        ts = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        res[name] = {"ms": round(ms, 3), "tflops": round(fl / ms / 1e9, 1)}
+    return res
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -390,6 +422,7 @@ def native_arm(args):
     value = tokens / (ms / 1000.0)
     per_op = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
     iso = isolated_times(chain, dev)
+    mlp = fused_linear_swiglu_measure(L, dev)
     loss = float(chain.loss.item())
 
     # ---- end to end through host buffers: every step copies its inputs host -> device from
@@ -474,7 +507,11 @@ def native_arm(args):
          "data": "synthetic (seeded SplitMix64/Box-Muller, shapes and distributions of the Qwen-7B layer chain)",
          "config": workload_config(S), "roofline": roofline, "hbm_kernels": hbm,
          "hbm_peak_gbs": pk["hbm_gbs"], "cpu_baseline": cpu, "e2e": e2e,
-         "gpu_launches": chain.launches_per_step() * K, "clocks": clocks, "loss": loss}
+         "gpu_launches": chain.launches_per_step() * K, "clocks": clocks, "loss": loss,
+         "fused_linear_swiglu": dict(mlp, shape="T=8192 H=4096 I=11008 bf16 (alone, not part of the step)",
+                                     peak_tflops_burst=pk["bf16"],
+                                     frac_fwd=round(mlp["fwd"]["tflops"] / pk["bf16"], 4),
+                                     frac_bwd=round(mlp["bwd"]["tflops"] / pk["bf16"], 4))}
     emit(d)
     if dist:
         dist.destroy_process_group()

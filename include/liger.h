@@ -191,6 +191,37 @@ int liger_swiglu_fwd(const void* gate, const void* up, void* y, int64_t n, int d
 int liger_swiglu_bwd(const void* dy, const void* gate, const void* up, void* dgate, void* dup, int64_t n,
                      int dtype, void* stream);
 
+/* ---------------------------------------------- FusedLinearSwiGLU
+ * Source: the FusedLinearSwiGLU paragraph of the page "Liger-Kernel核心技术：
+ * RollingBuffer与融合算子详解", section "算子融合": x @ W_g and x @ W_u in one
+ * kernel, SiLU and the product in registers, only the result written.
+ *
+ * Forward:  h = silu(X W_g^T) * (X W_u^T)
+ *   X [T, H], W_g and W_u [I, H] (nn.Linear layout, no bias), h [T, I]; bf16
+ *   only (tcgen05 tensor cores, fp32 accumulation); H >= 64 and H, I multiples
+ *   of 8.  The gate and up products never reach device memory.
+ *   All tensors dense row-major, 16-byte aligned, device memory owned by the
+ *   caller; asynchronous on `stream`.  Errors: LIGER_ERR_DTYPE (not bf16),
+ *   LIGER_ERR_SHAPE, LIGER_ERR_NULL, LIGER_ERR_ALIGN, LIGER_ERR_CUDA.  T = 0
+ *   is a no-op (X and out may be null).
+ */
+int liger_fused_linear_swiglu_fwd(const void* X, const void* Wg, const void* Wu, void* out, int64_t T, int64_t H,
+                                  int64_t I, int dtype, void* stream);
+
+/* Bytes of workspace the backward needs: dG and dU, [T, I] bf16 each. */
+size_t liger_fused_linear_swiglu_workspace(int64_t T, int64_t I);
+
+/* Backward from dH [T, I]: g and u are recomputed (not saved by the forward);
+ * with s = sigmoid(g), dG = dH u s (1 + g (1 - s)) and dU = dH g s,
+ *     dX = dG W_g + dU W_u [T, H],  dW_g = dG^T X,  dW_u = dU^T X [I, H]
+ * (written, not accumulated).  ws: at least
+ * liger_fused_linear_swiglu_workspace(T, I) bytes, 256-byte aligned, else
+ * LIGER_ERR_WORKSPACE; other errors as the forward.  T = 0 writes zero dW_g and
+ * dW_u (X, dH, dX and ws may then be null). */
+int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, const void* Wu, const void* dH, void* dX, void* dWg,
+                                  void* dWu, void* ws, size_t ws_bytes, int64_t T, int64_t H, int64_t I, int dtype,
+                                  void* stream);
+
 /* ------------------------------------------------ fused linear + CE
  * Source: the FusedCrossEntropyLoss paragraph of the page "Liger-Kernel核心
  * 技术：RollingBuffer与融合算子详解", section "算子融合" (softmax and NLL

@@ -6,6 +6,7 @@ logits, all hand-written CUDA behind the C-ABI of ``libliger.so``
 (``include/liger.h``).  This package is the Python binding of that library:
 see ``_native`` for the functions, which carry the C entry points' names.
 """
-from ._native import (LIGER_BF16, LIGER_F32, LigerError, liger_linear_ce_fwd_bwd,  # noqa: F401
+from ._native import (LIGER_BF16, LIGER_F32, LigerError, liger_fused_linear_swiglu_bwd,  # noqa: F401
+                      liger_fused_linear_swiglu_fwd, liger_fused_linear_swiglu_workspace, liger_linear_ce_fwd_bwd,
                       liger_linear_ce_workspace, liger_rmsnorm_bwd, liger_rmsnorm_bwd_noalloc, liger_rmsnorm_bwd_workspace, liger_rmsnorm_fwd,
                       liger_rope_bwd, liger_rope_bwd_ex, liger_rope_fwd, liger_rope_fwd_ex, liger_swiglu_bwd, liger_swiglu_fwd, load)

@@ -41,6 +41,9 @@ SIGNATURES = {
                           _INT),
     "liger_swiglu_fwd": ([_P, _P, _P, _I64, _INT, _P], _INT),
     "liger_swiglu_bwd": ([_P, _P, _P, _P, _P, _I64, _INT, _P], _INT),
+    "liger_fused_linear_swiglu_fwd": ([_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
+    "liger_fused_linear_swiglu_workspace": ([_I64, _I64], _SZ),
+    "liger_fused_linear_swiglu_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _INT, _P], _INT),
     "liger_linear_ce_workspace": ([_I64, _I64, _I64, _I64, _INT], _SZ),
     "liger_linear_ce_fwd_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _I64, _INT, _P],
                                 _INT),
@@ -204,6 +207,30 @@ def liger_swiglu_bwd(dy, gate, up, dgate, dup):
     _check(load().liger_swiglu_bwd(_ptr(dy), _ptr(gate), _ptr(up), _ptr(dgate), _ptr(dup), gate.numel(),
                                    _dtype_code(gate), _stream()))
     return dgate, dup
+
+
+# -------------------------------------------------------- FusedLinearSwiGLU
+def liger_fused_linear_swiglu_fwd(X, Wg, Wu, out):
+    _dense(X, Wg, Wu, out)
+    T, H = X.shape
+    I = Wg.shape[0]
+    _check(load().liger_fused_linear_swiglu_fwd(_ptr(X), _ptr(Wg), _ptr(Wu), _ptr(out), T, H, I, _dtype_code(X),
+                                                _stream()))
+    return out
+
+
+def liger_fused_linear_swiglu_workspace(T: int, I: int) -> int:
+    return int(load().liger_fused_linear_swiglu_workspace(T, I))
+
+
+def liger_fused_linear_swiglu_bwd(X, Wg, Wu, dH, dX, dWg, dWu, ws):
+    _dense(X, Wg, Wu, dH, dX, dWg, dWu, ws)
+    T, H = X.shape
+    I = Wg.shape[0]
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().liger_fused_linear_swiglu_bwd(_ptr(X), _ptr(Wg), _ptr(Wu), _ptr(dH), _ptr(dX), _ptr(dWg),
+                                                _ptr(dWu), _ptr(ws), nbytes, T, H, I, _dtype_code(X), _stream()))
+    return dX, dWg, dWu
 
 
 # ---------------------------------------------------------------- linear CE

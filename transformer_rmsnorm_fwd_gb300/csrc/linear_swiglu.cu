@@ -1,0 +1,178 @@
+// FusedLinearSwiGLU: the gate and up projections of the MLP and the SwiGLU
+// activation in one tensor-core kernel, and its backward.
+//
+// Operator: the FusedLinearSwiGLU paragraph of the page "Liger-Kernel核心技术：
+// RollingBuffer与融合算子详解", section "算子融合": x @ W_g and x @ W_u computed
+// together, SiLU and the product taken in registers, only the result written.
+//
+//   forward:  h = silu(X W_g^T) * (X W_u^T)        X [T, H], W_g, W_u [I, H], h [T, I]
+//   backward: g = X W_g^T, u = X W_u^T (recomputed), s = sigmoid(g)
+//             dG = dh u s (1 + g (1 - s)),  dU = dh g s
+//             dX = dG W_g + dU W_u,  dW_g = dG^T X,  dW_u = dU^T X
+//
+// GB300 design (all tensor-core, tcgen05):
+//  * forward: one persistent GEMM whose 256 B rows per stage are 128 gate rows
+//    and the matching 128 up rows (two TMA boxes), so a 128 x 256 accumulator
+//    tile holds g and u for 128 output columns; the epilogue writes silu(g) u
+//    and nothing else -- g and u never reach HBM;
+//  * backward: the same GEMM recomputes g and u and its epilogue forms dG and
+//    dU from dh (the only [T, I] intermediates, in the workspace); dX is one
+//    GEMM over K = 2I that reads (dG, W_g) for the first half of its k-blocks
+//    and (dU, W_u) for the second; dW_g and dW_u are two GEMMs with both
+//    operands MN-major.
+#include "tc_gemm.cuh"
+
+namespace liger {
+namespace {
+
+// Error word of the GEMMs launched here (bounded-wait expiry codes); these
+// entry points take no workspace header, so it is a module variable.
+static __device__ int g_lsw_err;
+
+int err_word(int** out) {
+    static int* addr[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(LIGER_ERR_CUDA, "no CUDA device");
+    if (!addr[dev] && cudaGetSymbolAddress(reinterpret_cast<void**>(&addr[dev]), g_lsw_err) != cudaSuccess)
+        return check_launch("fused_linear_swiglu error word");
+    *out = addr[dev];
+    return LIGER_OK;
+}
+
+int check_shapes(int64_t T, int64_t H, int64_t I, int dtype, const char* who) {
+    if (dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "%s: bf16 only (tensor-core path)", who);
+    if (T < 0 || H < 64 || I < 8 || H % 8 || I % 8 || T > (int64_t{1} << 31) || H > (1 << 30) || I > (1 << 30))
+        return fail(LIGER_ERR_SHAPE, "%s: T=%lld H=%lld I=%lld (H >= 64, H and I multiples of 8)", who, (long long)T,
+                    (long long)H, (long long)I);
+    return LIGER_OK;
+}
+
+}  // namespace
+}  // namespace liger
+
+using namespace liger;
+using namespace liger::tc;
+
+extern "C" int liger_fused_linear_swiglu_fwd(const void* X, const void* Wg, const void* Wu, void* out, int64_t T,
+                                             int64_t H, int64_t I, int dtype, void* stream) {
+    clear_error();
+    if (int rc = check_shapes(T, H, I, dtype, "fused_linear_swiglu_fwd")) return rc;
+    if (T == 0) return LIGER_OK;
+    if (!X || !Wg || !Wu || !out) return fail(LIGER_ERR_NULL, "fused_linear_swiglu_fwd: null tensor pointer");
+    if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(out))
+        return fail(LIGER_ERR_ALIGN, "fused_linear_swiglu_fwd: tensors must be 16-byte aligned");
+    CUtensorMap mX, mG, mU;
+    int rc;
+    if ((rc = make_map(&mX, X, H, T, H, BK, BM))) return rc;
+    if ((rc = make_map(&mG, Wg, H, I, H, BK, BN / 2))) return rc;
+    if ((rc = make_map(&mU, Wu, H, I, H, BK, BN / 2))) return rc;
+    int* d_err = nullptr;
+    if ((rc = err_word(&d_err))) return rc;
+    EpiParams e{};
+    e.err = d_err;
+    e.M = static_cast<int>(T);
+    e.N = static_cast<int>(I);
+    e.out = static_cast<__nv_bfloat16*>(out);
+    e.ldo = I;
+    e.bsplit = 1;
+    e.raster = RASTER_M_FASTEST;
+    e.hint_a = HINT_EVICT_LAST;    // X: reused by every column tile
+    e.hint_b = HINT_EVICT_FIRST;   // weights: streamed once
+    const int ntile_n = static_cast<int>(ceil_div(I, BN / 2));
+    return launch_gemm<0, 0, EPI_SWIGLU>(mX, mG, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
+                                         as_stream(stream), 0, &mX, &mU);
+}
+
+extern "C" size_t liger_fused_linear_swiglu_workspace(int64_t T, int64_t I) {
+    if (T <= 0 || I <= 0) return 0;
+    return 2 * ((static_cast<size_t>(T) * static_cast<size_t>(I) * 2 + 255) & ~static_cast<size_t>(255));
+}
+
+extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, const void* Wu, const void* dH, void* dX,
+                                             void* dWg, void* dWu, void* ws, size_t ws_bytes, int64_t T, int64_t H,
+                                             int64_t I, int dtype, void* stream) {
+    clear_error();
+    if (int rc = check_shapes(T, H, I, dtype, "fused_linear_swiglu_bwd")) return rc;
+    if (!Wg || !Wu || !dWg || !dWu || (T > 0 && (!X || !dH || !dX)))
+        return fail(LIGER_ERR_NULL, "fused_linear_swiglu_bwd: null tensor pointer");
+    if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(dH) || !aligned16(dX) || !aligned16(dWg) ||
+        !aligned16(dWu))
+        return fail(LIGER_ERR_ALIGN, "fused_linear_swiglu_bwd: tensors must be 16-byte aligned");
+    const size_t need = liger_fused_linear_swiglu_workspace(T, I);
+    if (need > 0 && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)))
+        return fail(LIGER_ERR_WORKSPACE, "fused_linear_swiglu_bwd: workspace of %zu bytes (256-byte aligned) "
+                    "required, got %zu", need, ws_bytes);
+    cudaStream_t st = as_stream(stream);
+    if (T == 0) {
+        const size_t wb = static_cast<size_t>(I * H) * 2;
+        if (cudaMemsetAsync(dWg, 0, wb, st) != cudaSuccess || cudaMemsetAsync(dWu, 0, wb, st) != cudaSuccess)
+            return check_launch("fused_linear_swiglu_bwd memset");
+        return LIGER_OK;
+    }
+    int* d_err = nullptr;
+    if (int rc0 = err_word(&d_err)) return rc0;
+    __nv_bfloat16* dG = static_cast<__nv_bfloat16*>(ws);
+    __nv_bfloat16* dU = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + need / 2);
+    int rc;
+    // 1. recompute g, u; dG, dU from dh
+    CUtensorMap mX_k, mG_k, mU_k;
+    if ((rc = make_map(&mX_k, X, H, T, H, BK, BM))) return rc;
+    if ((rc = make_map(&mG_k, Wg, H, I, H, BK, BN / 2))) return rc;
+    if ((rc = make_map(&mU_k, Wu, H, I, H, BK, BN / 2))) return rc;
+    EpiParams e{};
+    e.err = d_err;
+    e.M = static_cast<int>(T);
+    e.N = static_cast<int>(I);
+    e.out = dG;
+    e.out2 = dU;
+    e.ldo = I;
+    e.src = static_cast<const __nv_bfloat16*>(dH);
+    e.lds = I;
+    e.bsplit = 1;
+    e.raster = RASTER_M_FASTEST;
+    e.hint_a = HINT_EVICT_LAST;
+    e.hint_b = HINT_EVICT_FIRST;
+    const int ntile_n = static_cast<int>(ceil_div(I, BN / 2));
+    if ((rc = launch_gemm<0, 0, EPI_SWIGLU_BWD>(mX_k, mG_k, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
+                                               st, 0, &mX_k, &mU_k)))
+        return rc;
+    // 2. dX = dG W_g + dU W_u (K = 2I: k-blocks of the second product follow those of the first)
+    CUtensorMap mdG_k, mdU_k, mG_mn, mU_mn;
+    if ((rc = make_map(&mdG_k, dG, I, T, I, BK, BM))) return rc;
+    if ((rc = make_map(&mdU_k, dU, I, T, I, BK, BM))) return rc;
+    if ((rc = make_map(&mG_mn, Wg, H, I, H, MN_BOX, BK))) return rc;
+    if ((rc = make_map(&mU_mn, Wu, H, I, H, MN_BOX, BK))) return rc;
+    const int nkb1 = static_cast<int>(ceil_div(I, BK));
+    EpiParams d{};
+    d.err = d_err;
+    d.M = static_cast<int>(T);
+    d.N = static_cast<int>(H);
+    d.out = static_cast<__nv_bfloat16*>(dX);
+    d.ldo = H;
+    d.ksplit_nkb = nkb1;
+    d.raster = RASTER_N_GROUPS;
+    if ((rc = launch_gemm<0, 1, EPI_STORE>(mdG_k, mG_mn, static_cast<int>(T), static_cast<int>(H), 2 * nkb1 * BK, d,
+                                           st, 0, &mdU_k, &mU_mn)))
+        return rc;
+    // 3. dW_g = dG^T X, dW_u = dU^T X (both operands MN-major, K = T)
+    CUtensorMap mdG_mn, mdU_mn, mX_mn;
+    if ((rc = make_map(&mdG_mn, dG, I, T, I, MN_BOX, BK))) return rc;
+    if ((rc = make_map(&mdU_mn, dU, I, T, I, MN_BOX, BK))) return rc;
+    if ((rc = make_map(&mX_mn, X, H, T, H, MN_BOX, BK))) return rc;
+    EpiParams w{};
+    w.err = d_err;
+    w.M = static_cast<int>(I);
+    w.N = static_cast<int>(H);
+    w.ldo = H;
+    w.out_write = 1;
+    w.raster = RASTER_N_FASTEST;
+    w.hint_a = HINT_EVICT_FIRST;
+    w.hint_b = HINT_EVICT_LAST;   // X: reused by every row block
+    w.out = static_cast<__nv_bfloat16*>(dWg);
+    if ((rc = launch_gemm<1, 1, EPI_ACCUM>(mdG_mn, mX_mn, static_cast<int>(I), static_cast<int>(H),
+                                           static_cast<int>(T), w, st)))
+        return rc;
+    w.out = static_cast<__nv_bfloat16*>(dWu);
+    return launch_gemm<1, 1, EPI_ACCUM>(mdU_mn, mX_mn, static_cast<int>(I), static_cast<int>(H), static_cast<int>(T), w,
+                                        st);
+}

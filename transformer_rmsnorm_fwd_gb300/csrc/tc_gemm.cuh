@@ -49,7 +49,7 @@ constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 
-enum Epi : int { EPI_LOGITS = 0, EPI_STORE = 1, EPI_ACCUM = 2 };
+enum Epi : int { EPI_LOGITS = 0, EPI_STORE = 1, EPI_ACCUM = 2, EPI_SWIGLU = 3, EPI_SWIGLU_BWD = 4 };
 
 // Tile order of the persistent loop: m fastest, n fastest, or groups of
 // GROUP_N tile columns with n fastest inside a group (for long-K problems
@@ -91,7 +91,18 @@ struct EpiParams {
     const int* lstart;
     // L2 policies (Hint) of the A and B loads; streaming epilogue traffic (P, the
     // fp32 accumulator, dW) always uses evict-first accesses
-    int hint_a, hint_b;   // [M + 1]: the tokens labelled with row v are keys[lstart[v] .. lstart[v+1])
+    int hint_a, hint_b;
+    // operand modes: bsplit -- the 256 B rows of a stage are rows [ni*128, +128) of
+    // the B map and rows [ni*128, +128) of the B2 map (gate and up weights);
+    // ksplit_nkb > 0 -- k-blocks from ksplit_nkb on come from the A2 / B2 maps,
+    // their k coordinate restarting at 0 (a sum of two products)
+    int bsplit, ksplit_nkb;
+    // EPI_SWIGLU: out[row, ni*128 + j] = silu(acc[j]) * acc[128 + j], j < 128, col < N.
+    // EPI_SWIGLU_BWD: with dh = src[row, col] recomputes g, u from the
+    // accumulator and writes out = dg (dh u s (1 + g (1 - s))), out2 = du (dh g s).
+    const __nv_bfloat16* src;
+    int64_t lds;
+    __nv_bfloat16* out2;   // [M + 1]: the tokens labelled with row v are keys[lstart[v] .. lstart[v+1])
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -188,9 +199,15 @@ __device__ __forceinline__ void sub_scaled32(float (&v)[32], const __nv_bfloat16
 }
 
 // --------------------------------------------------------------- kernel
+// The kernel and its launcher have internal linkage: every translation unit
+// that includes this header registers and configures its own copy, so a
+// one-time attribute set in one unit never stands in for another's.
+namespace {
+
 template <int A_MN, int B_MN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, int M, int N,
                    int K, EpiParams ep) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -221,6 +238,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tmA);
         prefetch_map(&tmB);
+        if (ep.bsplit || ep.ksplit_nkb > 0) {
+            prefetch_map(&tmA2);
+            prefetch_map(&tmB2);
+        }
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
@@ -280,19 +301,27 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t sb = sa + A_BYTES;
                     const uint32_t fb = full_bar(stage);
                     mbar_expect_tx(fb, STAGE_BYTES);
+                    const bool second = ep.ksplit_nkb > 0 && kb >= ep.ksplit_nkb;
+                    const CUtensorMap* mA = second ? &tmA2 : &tmA;
+                    const CUtensorMap* mB = second ? &tmB2 : &tmB;
+                    const int kc = (second ? kb - ep.ksplit_nkb : kb) * BK;
                     if (A_MN) {
 #pragma unroll
                         for (int j = 0; j < BM / MN_BOX; ++j)
-                            tma_load_2d_hint(sa + j * MN_BOX_BYTES, &tmA, fb, mi * BM + j * MN_BOX, kb * BK, pol_a);
+                            tma_load_2d_hint(sa + j * MN_BOX_BYTES, mA, fb, mi * BM + j * MN_BOX, kc, pol_a);
                     } else {
-                        tma_load_2d_hint(sa, &tmA, fb, kb * BK, mi * BM, pol_a);
+                        tma_load_2d_hint(sa, mA, fb, kc, mi * BM, pol_a);
                     }
-                    if (B_MN) {
+                    if (ep.bsplit) {
+                        // K-major B maps with 128-row boxes: gate rows, then up rows
+                        tma_load_2d_hint(sb, &tmB, fb, kc, ni * (BN / 2), pol_b);
+                        tma_load_2d_hint(sb + B_BYTES / 2, &tmB2, fb, kc, ni * (BN / 2), pol_b);
+                    } else if (B_MN) {
 #pragma unroll
                         for (int j = 0; j < BN / MN_BOX; ++j)
-                            tma_load_2d_hint(sb + j * MN_BOX_BYTES, &tmB, fb, ni * BN + j * MN_BOX, kb * BK, pol_b);
+                            tma_load_2d_hint(sb + j * MN_BOX_BYTES, mB, fb, ni * BN + j * MN_BOX, kc, pol_b);
                     } else {
-                        tma_load_2d_hint(sb, &tmB, fb, kb * BK, ni * BN, pol_b);
+                        tma_load_2d_hint(sb, mB, fb, kc, ni * BN, pol_b);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
@@ -486,6 +515,55 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(as));
+            } else if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
+                const int o0 = ni * (BN / 2);   // first output (intermediate) column of the tile
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint4 dh[4];
+                    if (EPI == EPI_SWIGLU_BWD) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int col = o0 + c * 32 + g * 8;
+                            dh[g] = (row_ok && col < ep.N) ? ldg16(ep.src + static_cast<int64_t>(row) * ep.lds + col)
+                                                          : make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                    float gv[32], uv[32];
+                    tmem_ld32(taddr + c * 32, gv);
+                    tmem_ld32(taddr + BN / 2 + c * 32, uv);
+                    if (row_ok) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int col = o0 + c * 32 + g * 8;
+                            if (col < ep.N) {
+                                float a[8], b[8];
+                                if (EPI == EPI_SWIGLU) {
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        const float x = gv[g * 8 + e];
+                                        a[e] = x * __fdividef(1.0f, 1.0f + __expf(-x)) * uv[g * 8 + e];
+                                    }
+                                    stg16(ep.out + static_cast<int64_t>(row) * ep.ldo + col, pack(a));
+                                } else {
+                                    float d[8];
+                                    unpack(dh[g], d);
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        const float x = gv[g * 8 + e], u = uv[g * 8 + e];
+                                        const float sg = __fdividef(1.0f, 1.0f + __expf(-x));
+                                        a[e] = d[e] * u * sg * (1.0f + x * (1.0f - sg));
+                                        b[e] = d[e] * (x * sg);
+                                    }
+                                    stg16(ep.out + static_cast<int64_t>(row) * ep.ldo + col, pack(a));
+                                    stg16(ep.out2 + static_cast<int64_t>(row) * ep.ldo + col, pack(b));
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(as));
             } else {
                 __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
 #pragma unroll 1
@@ -559,6 +637,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
+}  // namespace
+
 // ------------------------------------------------------------ host side
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no
 // link-time dependency on libcuda).
@@ -574,9 +654,12 @@ int make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, i
 
 // Launch C = A(M x K) * B(N x K) with the given epilogue.  A_MN / B_MN say
 // whether each operand is MN-major.  grid_limit = 0: one block per SM.
+namespace {
+
 template <int A_MN, int B_MN, int EPI>
 int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K, const EpiParams& ep,
-                cudaStream_t st, int grid_limit = 0) {
+                cudaStream_t st, int grid_limit = 0, const CUtensorMap* ma2 = nullptr,
+                const CUtensorMap* mb2 = nullptr) {
     auto kern = tc_gemm_kernel<A_MN, B_MN, EPI>;
     static bool attr_set = false;   // per instantiation; the attribute is per function
     if (!attr_set) {
@@ -588,9 +671,11 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int 
     int grid = sm_count();
     if (grid_limit > 0) grid = std::min(grid, grid_limit);
     grid = std::max(1, std::min(grid, tiles));
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, M, N, K, ep);
+    kern<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, ma2 ? *ma2 : ma, mb2 ? *mb2 : mb, M, N, K, ep);
     return check_launch("tc_gemm");
 }
+
+}  // namespace
 
 }  // namespace tc
 }  // namespace liger
