@@ -57,6 +57,8 @@ def _load():
                                         _I, _P]
             lib.orc_linear_swiglu_fwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _I, _I, _P]
             lib.orc_linear_swiglu_bwd.argtypes = [_P, _P, _P, _P, ctypes.c_int, _I, _I, _I, _P, _P, _P]
+            lib.orc_rmsnorm_qkv_rope.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _P, _P, _P, _I,
+                                                 _I, _I, _I, _I, _I, _I, _D, _D, _P, _P, _P, _P]
             lib.orc_swiglu_fwd.argtypes = [_P, _P, ctypes.c_int, _I, _P]
             lib.orc_swiglu_bwd.argtypes = [_P, _P, _P, ctypes.c_int, _I, _P, _P]
             lib.orc_linear_ce.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
@@ -141,6 +143,45 @@ def rope_ex(t, theta=1e4, sign=1, pos=None, pairing="half", cos_tab=None, sin_ta
     _check(_load().orc_rope_ex(pt, _dt(t), ppos, B, S, NH, D, float(theta), int(sign),
                                1 if pairing == "interleaved" else 0, pc, ps, n_tab, out.ctypes.data), "rope_ex")
     return out
+
+
+def rmsnorm_qkv_rope(x, w, Wq, Wk, Wv, B, S, Hq, Hk, eps, theta=1e4, bq=None, bk=None, bv=None, pos=None,
+                     cos_tab=None, sin_tab=None):
+    """Fused RMSNorm + QKV projection (+ bias) + RoPE on q and k.
+    x [B*S, H]; w [H]; Wq [Hq*D, H]; Wk, Wv [Hk*D, H]; optional biases; pos
+    [B, S] int32; optional cos/sin tables [n, D/2] indexed by position.
+    Returns q [B,S,Hq,D], k [B,S,Hk,D], v [B,S,Hk,D], rstd [B*S] in float64."""
+    x, px = _c(x); w, pw = _c(w); Wq, pq = _c(Wq); Wk, pk = _c(Wk); Wv, pv = _c(Wv)
+    H = x.shape[1]
+    D = Wq.shape[0] // Hq if Hq else Wk.shape[0] // Hk
+    arrs = [x, w, Wq, Wk, Wv]
+    pb = []
+    for b in (bq, bk, bv):
+        if b is None:
+            pb.append(None)
+        else:
+            b, p = _c(b)
+            arrs.append(b)
+            pb.append(p)
+    ppos = None
+    if pos is not None:
+        pos = np.ascontiguousarray(pos, dtype=np.int32)
+        ppos = pos.ctypes.data
+    pc = ps = None
+    n_tab = 0
+    if cos_tab is not None:
+        cos_tab = np.ascontiguousarray(cos_tab, dtype=np.float64)
+        sin_tab = np.ascontiguousarray(sin_tab, dtype=np.float64)
+        assert cos_tab.shape == sin_tab.shape and cos_tab.shape[1] == D // 2
+        pc, ps, n_tab = cos_tab.ctypes.data, sin_tab.ctypes.data, cos_tab.shape[0]
+    q = np.empty((B, S, Hq, D), np.float64)
+    k = np.empty((B, S, Hk, D), np.float64)
+    v = np.empty((B, S, Hk, D), np.float64)
+    rstd = np.empty(B * S, np.float64)
+    _check(_load().orc_rmsnorm_qkv_rope(px, pw, pq, pk, pv, pb[0], pb[1], pb[2], _dt(*arrs), ppos, pc, ps, n_tab,
+                                        B, S, H, Hq, Hk, D, float(eps), float(theta), q.ctypes.data, k.ctypes.data,
+                                        v.ctypes.data, rstd.ctypes.data), "rmsnorm_qkv_rope")
+    return q, k, v, rstd
 
 
 def swiglu_fwd(g, u):

@@ -159,6 +159,89 @@ int orc_rope_ex(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S,
     return 0;
 }
 
+/* ------------------------------------------- fused RMSNorm + QKV + RoPE
+ * [P3] section "融合内核是如何工作的？来看一段简化版实现": one kernel takes the
+ * hidden row through three steps, with nothing written in between:
+ *   1. RMSNorm of the row: inv_rms = 1/sqrt(sum_sq / H + eps), and each
+ *      normalised feature x_i * inv_rms * w_i (kept in full precision);
+ *   2. the Q, K and V projections of the normalised row, each with its bias
+ *      (the listing adds q_bias, k_bias, v_bias; NULL here means no bias);
+ *   3. RoPE on the projected q and k.
+ * READING: the listing's step 3 rotates k against v with no position term
+ * (garbled); it is read as the same RoPE as orc_rope -- pairs (i, i + D/2)
+ * within every q head and every k head, angle p * theta^(-2i/D), or the
+ * caller's cos/sin tables indexed by position -- and v is left unrotated.
+ * Weights in nn.Linear layout: Wq [Hq*D, H], Wk and Wv [Hk*D, H].  Outputs
+ * q [B,S,Hq,D], k and v [B,S,Hk,D], rstd [B*S] (the inv_rms of each row). */
+static void rope_head(double* h, int64_t D, double p, double theta, const double* cos_tab, const double* sin_tab) {
+    const int64_t half = D / 2;
+    for (int64_t i = 0; i < half; ++i) {
+        double c, sn;
+        if (cos_tab) {
+            c = cos_tab[(int64_t)p * half + i];
+            sn = sin_tab[(int64_t)p * half + i];
+        } else {
+            double phi = p * pow(theta, -2.0 * (double)i / (double)D);
+            c = cos(phi);
+            sn = sin(phi);
+        }
+        double a = h[i], b = h[i + half];
+        h[i] = a * c - b * sn;
+        h[i + half] = b * c + a * sn;
+    }
+}
+
+int orc_rmsnorm_qkv_rope(const void* x, const void* w, const void* Wq, const void* Wk, const void* Wv,
+                         const void* bq, const void* bk, const void* bv, int dt, const int32_t* pos,
+                         const double* cos_tab, const double* sin_tab, int64_t n_tab, int64_t B, int64_t S,
+                         int64_t H, int64_t Hq, int64_t Hk, int64_t D, double eps, double theta, double* q,
+                         double* k, double* v, double* rstd) {
+    if (!x || !w || !Wq || !Wk || !Wv || !q || !k || !v || B < 0 || S < 0 || H <= 0 || Hq < 0 || Hk < 0 ||
+        D <= 0 || (D % 2) || bad_dt(dt))
+        return -1;
+    if ((cos_tab == NULL) != (sin_tab == NULL) || (!cos_tab && !(theta > 0.0))) return -1;
+    const int64_t nq = Hq * D, nk = Hk * D;
+    double* xn = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!xn) return -3;
+    for (int64_t t = 0; t < B * S; ++t) {
+        const int64_t s = t % S;
+        const int64_t p = pos ? (int64_t)pos[t] : s;
+        if (cos_tab && (p < 0 || p >= n_tab)) {
+            free(xn);
+            return -2;
+        }
+        /* 1. RMSNorm */
+        double sum_sq = 0.0;
+        for (int64_t i = 0; i < H; ++i) {
+            double val = ld(x, dt, t * H + i);
+            sum_sq += val * val;
+        }
+        const double inv_rms = 1.0 / sqrt(sum_sq / (double)H + eps);
+        if (rstd) rstd[t] = inv_rms;
+        for (int64_t i = 0; i < H; ++i) xn[i] = ld(x, dt, t * H + i) * inv_rms * ld(w, dt, i);
+        /* 2. projections with bias */
+        for (int64_t f = 0; f < nq; ++f) {
+            double acc = bq ? ld(bq, dt, f) : 0.0;
+            for (int64_t i = 0; i < H; ++i) acc += xn[i] * ld(Wq, dt, f * H + i);
+            q[t * nq + f] = acc;
+        }
+        for (int64_t f = 0; f < nk; ++f) {
+            double acck = bk ? ld(bk, dt, f) : 0.0, accv = bv ? ld(bv, dt, f) : 0.0;
+            for (int64_t i = 0; i < H; ++i) {
+                acck += xn[i] * ld(Wk, dt, f * H + i);
+                accv += xn[i] * ld(Wv, dt, f * H + i);
+            }
+            k[t * nk + f] = acck;
+            v[t * nk + f] = accv;
+        }
+        /* 3. RoPE on every q head and every k head */
+        for (int64_t h = 0; h < Hq; ++h) rope_head(q + t * nq + h * D, D, (double)p, theta, cos_tab, sin_tab);
+        for (int64_t h = 0; h < Hk; ++h) rope_head(k + t * nk + h * D, D, (double)p, theta, cos_tab, sin_tab);
+    }
+    free(xn);
+    return 0;
+}
+
 /* ----------------------------------------------------------------- SwiGLU
  * [P1] section "算子融合", FusedLinearSwiGLU paragraph: the SiLU activation of
  * the gate branch times the up branch, elementwise.  silu(g) = g * sigmoid(g).

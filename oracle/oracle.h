@@ -46,6 +46,13 @@ int orc_rope_ex(const void* t, int dt, const int32_t* pos, int64_t B, int64_t S,
                 double* out);
 
 /* SwiGLU forward y = silu(g) * u and its backward. */
+/* fused RMSNorm + QKV projection (+ bias) + RoPE on q and k, fp64 outputs */
+int orc_rmsnorm_qkv_rope(const void* x, const void* w, const void* Wq, const void* Wk, const void* Wv,
+                         const void* bq, const void* bk, const void* bv, int dt, const int32_t* pos,
+                         const double* cos_tab, const double* sin_tab, int64_t n_tab, int64_t B, int64_t S,
+                         int64_t H, int64_t Hq, int64_t Hk, int64_t D, double eps, double theta, double* q,
+                         double* k, double* v, double* rstd);
+
 int orc_swiglu_fwd(const void* g, const void* u, int dt, int64_t n, double* y);
 int orc_swiglu_bwd(const void* dy, const void* g, const void* u, int dt, int64_t n, double* dg, double* du);
 

@@ -270,3 +270,69 @@ def test_linear_swiglu_bwd_finite_differences():
     assert np.max(np.abs(dX - _fd(lambda v: L(v, Wg, Wu), X))) < 1e-7
     assert np.max(np.abs(dWg - _fd(lambda v: L(X, v, Wu), Wg))) < 1e-7
     assert np.max(np.abs(dWu - _fd(lambda v: L(X, Wg, v), Wu))) < 1e-7
+
+
+# ------------------------------------------------ fused RMSNorm + QKV + RoPE
+def test_rmsnorm_qkv_rope_worked_example():
+    g = golden("rmsnorm_qkv_rope_worked.json")
+    A = lambda k: np.array(g[k], dtype=np.float64)
+    q, k, v, rstd = oracle.rmsnorm_qkv_rope(A("x"), A("w"), A("Wq"), A("Wk"), A("Wv"), 1, 2, 1, 1, 0.0,
+                                            theta=1e4, bq=A("bq"))
+    assert np.allclose(rstd, 1.0, rtol=0, atol=1e-15)
+    assert np.allclose(q[0, 0, 0], g["q_pos0"], atol=1e-14) and np.allclose(k[0, 0, 0], g["k_pos0"], atol=1e-14)
+    assert np.allclose(q[0, 1, 0], g["q_pos1"], atol=1e-14) and np.allclose(k[0, 1, 0], g["k_pos1"], atol=1e-14)
+    assert np.allclose(v[0, 0, 0], g["v"], atol=1e-14) and np.allclose(v[0, 1, 0], g["v"], atol=1e-14)
+
+
+def _qkv_case(B=2, S=5, H=24, Hq=4, Hk=2, D=8, bias=True):
+    x = RNG.standard_normal((B * S, H)); w = 1 + 0.1 * RNG.standard_normal(H)
+    Wq = RNG.standard_normal((Hq * D, H)); Wk = RNG.standard_normal((Hk * D, H)); Wv = RNG.standard_normal((Hk * D, H))
+    b = [RNG.standard_normal(n) if bias else None for n in (Hq * D, Hk * D, Hk * D)]
+    return x, w, Wq, Wk, Wv, b
+
+
+def test_rmsnorm_qkv_rope_is_the_composition_of_the_pinned_steps():
+    """Equals RMSNorm (pinned above), a library matmul plus bias, and RoPE (pinned above)
+    on q and k, with explicit positions and grouped k/v heads."""
+    B, S, Hq, Hk, D, eps, theta = 2, 5, 4, 2, 8, 1e-5, 500.0
+    x, w, Wq, Wk, Wv, (bq, bk, bv) = _qkv_case(B, S, 24, Hq, Hk, D)
+    pos = RNG.integers(0, 4096, size=(B, S)).astype(np.int32)
+    q, k, v, rstd = oracle.rmsnorm_qkv_rope(x, w, Wq, Wk, Wv, B, S, Hq, Hk, eps, theta, bq, bk, bv, pos=pos)
+    xn, r = oracle.rmsnorm_fwd(x, w, eps)
+    assert np.allclose(rstd, r, rtol=1e-15)
+    ql = (np.matmul(xn, Wq.T) + bq).reshape(B, S, Hq, D)
+    kl = (np.matmul(xn, Wk.T) + bk).reshape(B, S, Hk, D)
+    vl = (np.matmul(xn, Wv.T) + bv).reshape(B, S, Hk, D)
+    assert np.max(np.abs(q - oracle.rope(ql, theta, 1, pos))) < 1e-12
+    assert np.max(np.abs(k - oracle.rope(kl, theta, 1, pos))) < 1e-12
+    assert np.max(np.abs(v - vl)) < 1e-12
+
+
+def test_rmsnorm_qkv_rope_scale_invariance_and_relative_positions():
+    B, S, Hq, Hk, D = 1, 6, 2, 1, 16
+    x, w, Wq, Wk, Wv, _ = _qkv_case(B, S, 32, Hq, Hk, D, bias=False)
+    q0, k0, v0, r0 = oracle.rmsnorm_qkv_rope(x, w, Wq, Wk, Wv, B, S, Hq, Hk, 0.0, 1e4)
+    q1, k1, v1, r1 = oracle.rmsnorm_qkv_rope(7.5 * x, w, Wq, Wk, Wv, B, S, Hq, Hk, 0.0, 1e4)
+    assert np.max(np.abs(q1 - q0)) < 1e-12 and np.max(np.abs(v1 - v0)) < 1e-12
+    assert np.allclose(r1 * 7.5, r0, rtol=1e-14)
+    # every token the same row: <q_m, k_n> depends only on m - n (shift all positions by 1000)
+    xs = np.repeat(x[:1], S, axis=0)
+    qa, ka, _, _ = oracle.rmsnorm_qkv_rope(xs, w, Wq, Wk, Wv, B, S, Hq, Hk, 1e-6, 1e4)
+    pos = (np.arange(S) + 1000).astype(np.int32).reshape(1, S)
+    qb, kb, _, _ = oracle.rmsnorm_qkv_rope(xs, w, Wq, Wk, Wv, B, S, Hq, Hk, 1e-6, 1e4, pos=pos)
+    da = np.einsum("mhd,nd->mnh", qa[0], ka[0, :, 0]); db = np.einsum("mhd,nd->mnh", qb[0], kb[0, :, 0])
+    assert np.max(np.abs(da - db)) < 1e-9
+    assert abs(da[3, 1, 0] - da[4, 2, 0]) < 1e-9 and abs(da[3, 1, 0] - da[1, 3, 0]) > 1e-6
+
+
+def test_rmsnorm_qkv_rope_tables_from_the_schedule_equal_theta():
+    B, S, Hq, Hk, D, theta = 1, 4, 1, 1, 8, 1e4
+    x, w, Wq, Wk, Wv, (bq, bk, bv) = _qkv_case(B, S, 16, Hq, Hk, D)
+    p = np.arange(16, dtype=np.float64)[:, None]; i = np.arange(D // 2, dtype=np.float64)[None, :]
+    ang = p * theta ** (-2 * i / D)
+    pos = np.array([[3, 0, 15, 7]], np.int32)
+    b = oracle.rmsnorm_qkv_rope(x, w, Wq, Wk, Wv, B, S, Hq, Hk, 1e-6, theta, bq, bk, bv, pos=pos,
+                                cos_tab=np.cos(ang), sin_tab=np.sin(ang))
+    c = oracle.rmsnorm_qkv_rope(x, w, Wq, Wk, Wv, B, S, Hq, Hk, 1e-6, theta, bq, bk, bv, pos=pos)
+    for u, z in zip(b, c):
+        assert np.max(np.abs(u - z)) < 1e-12
