@@ -271,6 +271,83 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
     return res
 
 
+def _median_ms(fn, n):
+    import torch
+    fn()
+    fn()
+    ts = []
+    for _ in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def rmsnorm_qkv_rope_measure(L, dev, S=32768, H=HIDDEN, Hq=HEADS, Hk=HEADS, D=HEAD_DIM, n=5):
+    """Fused RMSNorm + QKV projection (+ bias) + RoPE forward at the Qwen-7B layer
+    shapes and the chain's sequence length, alone: the whole call (weight fold,
+    rstd/angle pre-pass, GEMM with the scale/bias/RoPE epilogue), the call with
+    the folded weights reused, and for comparison the unfused sequence of the
+    same work (RMSNorm kernel, cuBLAS addmm with the bias, RoPE kernel on the
+    packed QKV views).  2*T*H*N flops, N = (Hq + 2 Hk) D."""
+    import torch
+    from datagen import normal
+    T, nq, nk = S, Hq * D, Hk * D
+    N = nq + 2 * nk
+    x = to_torch(normal(6, "qkv.x", (T, H), "bf16"), dev)
+    wn = to_torch(normal(6, "qkv.w", (H,), "bf16", 1.0, 0.1), dev)
+    Wq = to_torch(normal(6, "qkv.Wq", (nq, H), "bf16", 0.0, 0.02), dev)
+    Wk = to_torch(normal(6, "qkv.Wk", (nk, H), "bf16", 0.0, 0.02), dev)
+    Wv = to_torch(normal(6, "qkv.Wv", (nk, H), "bf16", 0.0, 0.02), dev)
+    bq = to_torch(normal(6, "qkv.bq", (nq,), "bf16", 0.0, 0.1), dev)
+    bk = to_torch(normal(6, "qkv.bk", (nk,), "bf16", 0.0, 0.1), dev)
+    bv = to_torch(normal(6, "qkv.bv", (nk,), "bf16", 0.0, 0.1), dev)
+    q = torch.empty(1, S, Hq, D, dtype=torch.bfloat16, device=dev)
+    k = torch.empty(1, S, Hk, D, dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k)
+    ws = torch.empty(L.liger_rmsnorm_qkv_rope_workspace(T, H, Hq, Hk, D), dtype=torch.uint8, device=dev)
+    fl = 2.0 * T * H * N
+
+    def fused(folded):
+        return lambda: L.liger_rmsnorm_qkv_rope_fwd(x, wn, Wq, Wk, Wv, q, k, v, ws, 1, S, Hq, Hk, D, bq=bq, bk=bk,
+                                                    bv=bv, eps=EPS, theta=THETA, folded=folded)
+
+    ms_full = _median_ms(fused(False), n)
+    ms_folded = _median_ms(fused(True), n)
+    del ws
+    Wcat = torch.cat([Wq, Wk, Wv]).t()
+    bcat = torch.cat([bq, bk, bv])
+    xn = torch.empty_like(x)
+    qkv = torch.empty(T, N, dtype=torch.bfloat16, device=dev)
+
+    def unfused():
+        L.liger_rmsnorm_fwd(x, wn, xn, None, EPS)
+        torch.addmm(bcat, xn, Wcat, out=qkv)
+        L.liger_rope_fwd_ex(qkv, qkv[:, nq:], N, N, Hq, Hk, D, 1, S, theta=THETA)
+
+    ms_unf = _median_ms(unfused, n)
+    return {"ms": round(ms_full, 3), "tflops": round(fl / ms_full / 1e9, 1),
+            "ms_folded_weights": round(ms_folded, 3), "tflops_folded_weights": round(fl / ms_folded / 1e9, 1),
+            "ms_unfused_cublas": round(ms_unf, 3), "speedup_vs_unfused": round(ms_unf / ms_full, 3)}
+
+
+def linear_ce_two_pass_measure(chain, dev, n=3):
+    """The two-pass, vocabulary-chunked linear CE on the chain's own head inputs
+    (seq x 4096 x 151936), alone: ms, TFLOP/s counting its 8*S*H*V flops and the
+    operator's 6*S*H*V, and both variants' workspace bytes."""
+    import torch
+    L, i, S = chain.L, chain.inp, chain.S
+    ws = torch.empty(L.liger_linear_ce_two_pass_workspace(S, HIDDEN, VOCAB), dtype=torch.uint8, device=dev)
+    ms = _median_ms(lambda: L.liger_linear_ce_two_pass_fwd_bwd(i["X"], i["W"], i["labels"], chain.loss, chain.dX,
+                                                               chain.dW, ws), n)
+    fl = float(S) * HIDDEN * VOCAB
+    return {"ms": round(ms, 3), "tflops_8shv": round(8 * fl / ms / 1e9, 1), "tflops_6shv": round(6 * fl / ms / 1e9, 1),
+            "workspace_bytes": int(ws.numel()), "workspace_bytes_token_chunked": int(chain.ws_c.numel())}
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -423,6 +500,8 @@ def native_arm(args):
     per_op = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
     iso = isolated_times(chain, dev)
     mlp = fused_linear_swiglu_measure(L, dev)
+    qkv = rmsnorm_qkv_rope_measure(L, dev, S)
+    two_pass = linear_ce_two_pass_measure(chain, dev)
     loss = float(chain.loss.item())
 
     # ---- end to end through host buffers: every step copies its inputs host -> device from
@@ -511,7 +590,14 @@ def native_arm(args):
          "fused_linear_swiglu": dict(mlp, shape="T=8192 H=4096 I=11008 bf16 (alone, not part of the step)",
                                      peak_tflops_burst=pk["bf16"],
                                      frac_fwd=round(mlp["fwd"]["tflops"] / pk["bf16"], 4),
-                                     frac_bwd=round(mlp["bwd"]["tflops"] / pk["bf16"], 4))}
+                                     frac_bwd=round(mlp["bwd"]["tflops"] / pk["bf16"], 4)),
+         "rmsnorm_qkv_rope": dict(qkv, shape=f"T={S} H={HIDDEN} Hq=Hk={HEADS} D={HEAD_DIM} QKV bias, bf16 "
+                                             "(alone, not part of the step)",
+                                  peak_tflops_burst=pk["bf16"], frac=round(qkv["tflops"] / pk["bf16"], 4),
+                                  frac_folded_weights=round(qkv["tflops_folded_weights"] / pk["bf16"], 4)),
+         "linear_ce_two_pass": dict(two_pass, shape=f"S={S} H={HIDDEN} V={VOCAB} bf16, auto vocabulary chunk "
+                                                    "(alone, not part of the step)",
+                                    frac=round(two_pass["tflops_8shv"] / pk["bf16_sustained"], 4))}
     emit(d)
     if dist:
         dist.destroy_process_group()

@@ -19,7 +19,8 @@
  *     queued on `stream` has finished.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls queue work on it and return without waiting, except
- *     liger_linear_ce_fwd_bwd, which waits for its label scan (see there).
+ *     liger_linear_ce_fwd_bwd and liger_linear_ce_two_pass_fwd_bwd, which
+ *     wait for their label scan (see there).
  *   - `dtype` is LIGER_F32 or LIGER_BF16 and applies to every float tensor
  *     of the call except the ones documented as float (rstd, loss); all
  *     arithmetic is fp32 whatever the storage type.
@@ -191,6 +192,44 @@ int liger_swiglu_fwd(const void* gate, const void* up, void* y, int64_t n, int d
 int liger_swiglu_bwd(const void* dy, const void* gate, const void* up, void* dgate, void* dup, int64_t n,
                      int dtype, void* stream);
 
+/* ------------------------------------ fused RMSNorm + QKV projection + RoPE
+ * Source: the fused kernel on the page "Liger-Kernel底层优化：新一代内核级推理
+ * 加速引擎介绍", section "融合内核是如何工作的" (RMSNorm step, Q/K/V projection
+ * with bias, RoPE on q and k, nothing written in between).  Forward only.
+ *
+ *   r_t = 1 / sqrt(mean_i x[t,i]^2 + eps)                      (rstd, fp32 [T])
+ *   q[t] = RoPE_p(r_t (x[t] * w) Wq^T + bq)   [B, S, Hq, D]
+ *   k[t] = RoPE_p(r_t (x[t] * w) Wk^T + bk)   [B, S, Hk, D]
+ *   v[t] =        r_t (x[t] * w) Wv^T + bv    [B, S, Hk, D]
+ * with RoPE as liger_rope_fwd (pairs (i, i + D/2) in every head, angle
+ * p * theta^(-2i/D), p = pos[b, s] or s), or, given cos_tab / sin_tab
+ * ([n_tab, D/2] fp32, indexed by position, clamped to the table), those
+ * values as given.
+ *   x [B*S, H], w_norm [H], Wq [Hq*D, H], Wk and Wv [Hk*D, H] (nn.Linear
+ *   layout), biases bq [Hq*D], bk and bv [Hk*D] or NULL (no bias): all bf16,
+ *   dense row-major, 16-byte aligned (biases 2-byte).  pos: int32 [B, S] or
+ *   NULL.  rstd: fp32 [B*S] output or NULL.  hidden >= 64 and a multiple of
+ *   8; head_dim 64, 128 or 256.
+ * The norm weight is folded into the projection weights (bf16(W * w)) inside
+ * ws, so the normalised rows and the un-rotated q, k never reach device
+ * memory.  flags bit 0 set: ws already holds the folded weights and biases of
+ * an earlier call with the same w_norm, W and b (they are then not read and
+ * may be NULL).
+ * ws: liger_rmsnorm_qkv_rope_workspace(B*S, H, Hq, Hk, D) bytes, 256-byte
+ * aligned, owned by the caller (the folded weights first, so a workspace
+ * sized for more tokens can be reused).  Asynchronous on `stream`.
+ * Errors: LIGER_ERR_DTYPE (not bf16), LIGER_ERR_SHAPE, LIGER_ERR_NULL,
+ * LIGER_ERR_ALIGN, LIGER_ERR_WORKSPACE, LIGER_ERR_CUDA.  B*S = 0 is a no-op.
+ */
+size_t liger_rmsnorm_qkv_rope_workspace(int64_t tokens, int64_t hidden, int64_t n_q_heads, int64_t n_k_heads,
+                                        int64_t head_dim);
+int liger_rmsnorm_qkv_rope_fwd(const void* x, const void* w_norm, const void* Wq, const void* Wk, const void* Wv,
+                               const void* bq, const void* bk, const void* bv, const int32_t* pos,
+                               const float* cos_tab, const float* sin_tab, int64_t n_tab, void* q, void* k, void* v,
+                               float* rstd, void* ws, size_t ws_bytes, int64_t batch, int64_t seq, int64_t hidden,
+                               int64_t n_q_heads, int64_t n_k_heads, int64_t head_dim, double eps, double theta,
+                               int flags, int dtype, void* stream);
+
 /* ---------------------------------------------- FusedLinearSwiGLU
  * Source: the FusedLinearSwiGLU paragraph of the page "Liger-Kernel核心技术：
  * RollingBuffer与融合算子详解", section "算子融合": x @ W_g and x @ W_u in one
@@ -248,8 +287,9 @@ int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, const void* Wu,
  *   (T > 128).  dW is accumulated across chunks in fp32.
  *   ws: device workspace of at least liger_linear_ce_workspace(T, H, V,
  *   chunk, dtype) bytes, 256-byte aligned.  On return ws begins with
- *   float lse[T] (0 on ignored rows), followed by float loss_row[T]
- *   (lse_t - z_t[label], 0 on ignored rows).
+ *   float lse[T] (0 on ignored rows); float loss_row[T] (lse_t -
+ *   z_t[label], 0 on ignored rows) starts at byte offset 4*T rounded up to a
+ *   multiple of 256.
  *   Labels are validated on the device before any other work; the call waits
  *   for that scan (one stream synchronisation) and returns LIGER_ERR_LABEL,
  *   with nothing else queued, if a label is outside [0, V) and is not
@@ -260,6 +300,31 @@ size_t liger_linear_ce_workspace(int64_t T, int64_t H, int64_t V, int64_t chunk,
 int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H, int64_t V,
                             int64_t ignore_index, int reduction, float grad_scale, float* loss, void* dX, void* dW,
                             void* ws, size_t ws_bytes, int64_t chunk, int dtype, void* stream);
+
+/* Two-pass, vocabulary-chunked variant of the same operator (same loss, lse,
+ * dX and dW, same arguments and error behaviour), for callers that cannot
+ * hold a [chunk x V] buffer and a [V x H] fp32 accumulator: no buffer of the
+ * vocabulary's width exists at all.
+ *   pass 1: the logits GEMM keeps only per-tile (max, sum-exp) partials and
+ *           the label logit (token chunks of up to 8192 rows) -> lse, loss;
+ *   pass 2: per chunk of `vchunk` vocabulary rows (0 = automatic: 8192, at
+ *           most V), the logits of all T tokens are recomputed and the
+ *           softmax part of D for that chunk written to a [T x vchunk] bf16
+ *           buffer; dX accumulates D_c W_c in an fp32 [T x H] buffer (when
+ *           V > vchunk); the rows dW_c = D_c^T X are finished and written.
+ *   8 T H V flops (the logits twice) against 6 T H V for
+ *   liger_linear_ce_fwd_bwd; the workspace is O(T (H + vchunk)), not
+ *   O(chunk V + V H).  bf16 only (tensor cores), H >= 64 and a multiple of 8,
+ *   V >= 256, vchunk a multiple of 8.  ws: at least
+ *   liger_linear_ce_two_pass_workspace(T, H, V, vchunk) bytes, 256-byte
+ *   aligned, with float lse[T] and float loss_row[T] at the same offsets as
+ *   above. */
+size_t liger_linear_ce_two_pass_workspace(int64_t T, int64_t H, int64_t V, int64_t vchunk);
+
+int liger_linear_ce_two_pass_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H,
+                                     int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
+                                     void* dX, void* dW, void* ws, size_t ws_bytes, int64_t vchunk, int dtype,
+                                     void* stream);
 
 #ifdef __cplusplus
 }

@@ -20,7 +20,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = _native.header_functions()
-    assert len(names) == 16
+    assert len(names) == 20
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_native.SIGNATURES)
@@ -81,3 +81,24 @@ def test_workspace_sizes(lib):
     full_logits = T * V * 2
     assert n < full_logits + V * H * 4
     assert lib.liger_linear_ce_workspace(T, H, V, 0, 7) == 0
+
+
+def test_rmsnorm_qkv_rope_host_checks(lib):
+    ok = ctypes.c_void_p(0x1000)
+    r256 = lambda b: (b + 255) // 256 * 256
+    T, H, Hq, Hk, D = 300, 320, 4, 2, 64
+    N = (Hq + 2 * Hk) * D
+    need = lib.liger_rmsnorm_qkv_rope_workspace(T, H, Hq, Hk, D)
+    assert need == r256(N * H * 2) + r256(N * 4) + r256(T * 4) + 2 * r256(T * (D // 2) * 4)
+    args = lambda **kw: [kw.get("x", ok), ok, ok, ok, ok, None, None, None, None, None, None, 0, ok, ok, ok, None,
+                         kw.get("ws", ok), kw.get("ws_bytes", need), 2, 150, kw.get("H", H), Hq, Hk,
+                         kw.get("D", D), 1e-6, kw.get("theta", 1e4), kw.get("flags", 0), kw.get("dtype", 1), None]
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(dtype=0)) == -3                 # fp32: tensor-core path is bf16
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(D=96)) == -2                    # head_dim not 64/128/256
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(H=324)) == -2                   # hidden not a multiple of 8
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(theta=0.0)) == -2
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(flags=2)) == -2
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(ws_bytes=need - 1)) == -6
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(ws=ctypes.c_void_p(0x1010))) == -6
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(x=None)) == -1
+    assert lib.liger_rmsnorm_qkv_rope_fwd(*args(x=ctypes.c_void_p(0x1008))) == -4

@@ -166,7 +166,8 @@ def test_linear_ce_llama3_full_size_sampled(cuda_lib):
     cuda_lib.liger_linear_ce_fwd_bwd(tX, tW, tl, loss, dX, dW, ws)
     torch.cuda.synchronize()
     lse = ws[: 4 * T].view(torch.float32).cpu().numpy().astype(np.float64)
-    lrow = ws[4 * T: 8 * T].view(torch.float32).cpu().numpy().astype(np.float64)
+    off = (4 * T + 255) // 256 * 256          # loss_row starts at the next 256-byte boundary
+    lrow = ws[off: off + 4 * T].view(torch.float32).cpu().numpy().astype(np.float64)
     n_valid = int((lab != -100).sum())
     assert n_valid == 8192 - 819
     # the loss is the mean of the row terms

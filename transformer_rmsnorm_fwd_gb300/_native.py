@@ -44,6 +44,12 @@ SIGNATURES = {
     "liger_fused_linear_swiglu_fwd": ([_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "liger_fused_linear_swiglu_workspace": ([_I64, _I64], _SZ),
     "liger_fused_linear_swiglu_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _INT, _P], _INT),
+    "liger_rmsnorm_qkv_rope_workspace": ([_I64, _I64, _I64, _I64, _I64], _SZ),
+    "liger_rmsnorm_qkv_rope_fwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _SZ, _I64,
+                                    _I64, _I64, _I64, _I64, _I64, _D, _D, _INT, _INT, _P], _INT),
+    "liger_linear_ce_two_pass_workspace": ([_I64, _I64, _I64, _I64], _SZ),
+    "liger_linear_ce_two_pass_fwd_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _I64,
+                                          _INT, _P], _INT),
     "liger_linear_ce_workspace": ([_I64, _I64, _I64, _I64, _INT], _SZ),
     "liger_linear_ce_fwd_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _I64, _INT, _P],
                                 _INT),
@@ -233,6 +239,29 @@ def liger_fused_linear_swiglu_bwd(X, Wg, Wu, dH, dX, dWg, dWu, ws):
     return dX, dWg, dWu
 
 
+# ------------------------------------------------ fused RMSNorm + QKV + RoPE
+def liger_rmsnorm_qkv_rope_workspace(tokens: int, hidden: int, n_q_heads: int, n_k_heads: int, head_dim: int) -> int:
+    return int(load().liger_rmsnorm_qkv_rope_workspace(tokens, hidden, n_q_heads, n_k_heads, head_dim))
+
+
+def liger_rmsnorm_qkv_rope_fwd(x, w_norm, Wq, Wk, Wv, q, k, v, ws, batch, seq, n_q_heads, n_k_heads, head_dim,
+                               bq=None, bk=None, bv=None, pos=None, cos_tab=None, sin_tab=None, rstd=None,
+                               eps=1e-6, theta=1e4, folded=False):
+    """Fused RMSNorm + QKV projection + RoPE forward (see liger.h): x [B*S, H];
+    q [B,S,Hq,D], k and v [B,S,Hk,D] written; folded=True reuses the folded
+    weights already in ws."""
+    _dense(x, w_norm, Wq, Wk, Wv, bq, bk, bv, pos, cos_tab, sin_tab, q, k, v, rstd, ws)
+    H = x.shape[-1]
+    n_tab = cos_tab.shape[0] if cos_tab is not None else 0
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().liger_rmsnorm_qkv_rope_fwd(_ptr(x), _ptr(w_norm), _ptr(Wq), _ptr(Wk), _ptr(Wv), _ptr(bq), _ptr(bk),
+                                             _ptr(bv), _ptr(pos), _ptr(cos_tab), _ptr(sin_tab), n_tab, _ptr(q),
+                                             _ptr(k), _ptr(v), _ptr(rstd), _ptr(ws), nbytes, batch, seq, H,
+                                             n_q_heads, n_k_heads, head_dim, float(eps), float(theta),
+                                             1 if folded else 0, _dtype_code(x), _stream()))
+    return q, k, v
+
+
 # ---------------------------------------------------------------- linear CE
 def liger_linear_ce_workspace(T: int, H: int, V: int, chunk: int = 0, dtype: int = LIGER_BF16) -> int:
     return int(load().liger_linear_ce_workspace(T, H, V, chunk, dtype))
@@ -247,4 +276,22 @@ def liger_linear_ce_fwd_bwd(X, W, labels, loss, dX, dW, ws, ignore_index: int = 
     _check(load().liger_linear_ce_fwd_bwd(_ptr(X), _ptr(W), _ptr(labels), T, H, V, int(ignore_index),
                                           0 if reduction == "mean" else 1, float(grad_scale), _ptr(loss), _ptr(dX),
                                           _ptr(dW), _ptr(ws), nbytes, int(chunk), _dtype_code(X), _stream()))
+    return loss, dX, dW
+
+
+def liger_linear_ce_two_pass_workspace(T: int, H: int, V: int, vchunk: int = 0) -> int:
+    return int(load().liger_linear_ce_two_pass_workspace(T, H, V, vchunk))
+
+
+def liger_linear_ce_two_pass_fwd_bwd(X, W, labels, loss, dX, dW, ws, ignore_index: int = -100,
+                                     reduction: str = "mean", grad_scale: float = 1.0, vchunk: int = 0):
+    """Two-pass, vocabulary-chunked fused linear cross-entropy (see liger.h)."""
+    _dense(X, W, labels, loss, dX, dW, ws)
+    T, H = X.shape
+    V = W.shape[0]
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().liger_linear_ce_two_pass_fwd_bwd(_ptr(X), _ptr(W), _ptr(labels), T, H, V, int(ignore_index),
+                                                   0 if reduction == "mean" else 1, float(grad_scale), _ptr(loss),
+                                                   _ptr(dX), _ptr(dW), _ptr(ws), nbytes, int(vchunk), _dtype_code(X),
+                                                   _stream()))
     return loss, dX, dW

@@ -119,17 +119,19 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* sh) {
     return r;
 }
 
-// Sort the chunk's (label << 32 | row) keys (ignored rows -> ~0) in one block
-// (bitonic, in shared memory), for the one-hot correction of the dW epilogue.
+// Sort the chunk's (label << 32 | t_base + row) keys (ignored rows -> ~0) in one
+// block (bitonic, in shared memory), for the one-hot correction of the dW
+// epilogue.
 constexpr int kMaxSortKeys = 8192;
 __global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restrict__ labels, int n, int64_t ignore,
-                                                        int npow2, unsigned long long* __restrict__ out) {
+                                                        int npow2, unsigned t_base,
+                                                        unsigned long long* __restrict__ out) {
     extern __shared__ unsigned long long sk[];
     for (int i = threadIdx.x; i < npow2; i += 1024) {
         unsigned long long key = ~0ull;
         if (i < n) {
             const int64_t y = labels[i];
-            if (y != ignore) key = (static_cast<unsigned long long>(y) << 32) | static_cast<unsigned>(i);
+            if (y != ignore) key = (static_cast<unsigned long long>(y) << 32) | (t_base + static_cast<unsigned>(i));
         }
         sk[i] = key;
     }
@@ -153,9 +155,11 @@ __global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restric
     for (int i = threadIdx.x; i < n; i += 1024) out[i] = sk[i];
 }
 
-// lstart[v] = first index of label v in the sorted chunk keys, v in [0, V]
-// (so the tokens labelled v are keys[lstart[v] .. lstart[v+1])).
-__global__ void label_starts(const unsigned long long* __restrict__ keys, int n, int V, int* __restrict__ lstart) {
+// lstart[v] = base + first index of label v in the sorted chunk keys, v in
+// [0, V] (so the tokens labelled v are keys[lstart[v] .. lstart[v+1]) of the
+// array the chunk's keys start at index base of).
+__global__ void label_starts(const unsigned long long* __restrict__ keys, int n, int V, int base,
+                             int* __restrict__ lstart) {
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v <= V; v += gridDim.x * blockDim.x) {
         const unsigned long long key = static_cast<unsigned long long>(v) << 32;
         int lo = 0, hi = n;
@@ -164,13 +168,14 @@ __global__ void label_starts(const unsigned long long* __restrict__ keys, int n,
             if (keys[mid] < key) lo = mid + 1;
             else hi = mid;
         }
-        lstart[v] = lo;
+        lstart[v] = base + lo;
     }
 }
 
 // Merge the per-tile (m, s) of one chunk row into lse and rewrite P in place
 // into the softmax part of D, scale * P * exp(m_tile - lse) (the one-hot part
-// is applied exactly, in fp32, by the dX / dW GEMM epilogues).
+// is applied exactly, in fp32, by the dX / dW GEMM epilogues).  P null: lse
+// and the loss term only.
 constexpr int kRowThreads = 256;
 __global__ void __launch_bounds__(kRowThreads) dlogits_bf16(const int64_t* __restrict__ labels, int64_t ignore,
                                                             const float2* __restrict__ part, int nvt,
@@ -184,7 +189,9 @@ __global__ void __launch_bounds__(kRowThreads) dlogits_bf16(const int64_t* __res
     __nv_bfloat16* prow = P + row * ldp;
     const int nv8 = (V + 7) / 8;
     if (y == ignore) {
-        for (int k = threadIdx.x; k < nv8; k += kRowThreads) stg16(prow + static_cast<int64_t>(k) * 8, make_uint4(0, 0, 0, 0));
+        if (P != nullptr)
+            for (int k = threadIdx.x; k < nv8; k += kRowThreads)
+                stg16(prow + static_cast<int64_t>(k) * 8, make_uint4(0, 0, 0, 0));
         if (threadIdx.x == 0) {
             lse[row] = 0.f;
             lossrow[row] = 0.f;
@@ -207,6 +214,7 @@ __global__ void __launch_bounds__(kRowThreads) dlogits_bf16(const int64_t* __res
         lse[row] = l;
         lossrow[row] = l - zlab[row];
     }
+    if (P == nullptr) return;   // lse and the loss term only
     __syncthreads();
     for (int k = threadIdx.x; k < nv8; k += kRowThreads) {
         const int col = k * 8;
@@ -398,8 +406,7 @@ int run_simt(const Args& a, const Layout& L, float scale) {
     return LIGER_OK;
 }
 
-int run_tc(const Args& a, const Layout& L, float scale) {
-    using namespace tc;
+int ensure_sort_attr() {
     static bool sort_attr = false;
     if (!sort_attr) {
         if (cudaFuncSetAttribute(sort_label_keys, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -407,6 +414,12 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             return check_launch("sort_label_keys attribute");
         sort_attr = true;
     }
+    return LIGER_OK;
+}
+
+int run_tc(const Args& a, const Layout& L, float scale) {
+    using namespace tc;
+    if (int rc = ensure_sort_attr()) return rc;
     const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(a.X);
     const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(a.W);
     float* lse = reinterpret_cast<float*>(a.ws + L.lse);
@@ -475,10 +488,10 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             int npow2 = 1;
             while (npow2 < cl) npow2 <<= 1;
             sort_label_keys<<<1, 1024, sizeof(unsigned long long) * npow2, a.st>>>(a.labels + t0, cl, a.ignore, npow2,
-                                                                                    keys);
+                                                                                    0u, keys);
             if ((rc = check_launch("sort_label_keys"))) return rc;
             label_starts<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(V + 1, 256), 8 * sm_count())), 256, 0,
-                           a.st>>>(keys, cl, V, lstart);
+                           a.st>>>(keys, cl, V, 0, lstart);
             if ((rc = check_launch("label_starts"))) return rc;
             EpiParams d = e;
             d.corr_src = Xc;
@@ -506,6 +519,176 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     return LIGER_OK;
 }
 
+// --------------------------------------- two-pass (vocab-chunked) variant
+// The same loss and gradients with no [tokens x vocab] buffer at all: pass 1
+// computes only lse (the logits GEMM keeps per-tile (m, s) partials, token
+// chunk by token chunk); pass 2 recomputes the logits one vocabulary chunk of
+// Vc rows at a time for all T tokens, writes the softmax part of D for that
+// chunk ([T x Vc] bf16), accumulates dX += D_c W_c in an fp32 [T x H]
+// buffer and writes the finished rows dW_c = D_c^T X.  8 T H V flops (the
+// logits twice) against 6 T H V for the token-chunked path, and a workspace
+// of O(T (H + Vc)) instead of O(C V + V H).
+constexpr int64_t kAutoVChunk = 8192;
+
+struct Layout2 {
+    int64_t C, nvt, Vc, ldc, nvchunks, nseg;
+    size_t lse, lossrow, zlab, hdr, keys, lstart, part, dscr, acc, total;
+};
+
+Layout2 layout2(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
+    Layout2 L{};
+    L.C = std::max<int64_t>(1, std::min<int64_t>(kMaxChunkTC, T));
+    L.nvt = ceil_div(V, kVT);
+    L.Vc = std::min<int64_t>(vchunk > 0 ? vchunk : kAutoVChunk, V);
+    L.ldc = ((L.Vc + 7) / 8) * 8;
+    L.nvchunks = ceil_div(V, L.Vc);
+    L.nseg = T > 0 ? ceil_div(T, static_cast<int64_t>(kMaxSortKeys)) : 0;
+    size_t o = 0;
+    L.lse = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
+    L.lossrow = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
+    L.zlab = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
+    L.hdr = o; o = up256(o + sizeof(Hdr));
+    L.keys = o; o = up256(o + sizeof(unsigned long long) * static_cast<size_t>(T));
+    L.lstart = o; o = up256(o + sizeof(int) * static_cast<size_t>(L.nseg * (V + 1)));
+    L.part = o; o = up256(o + sizeof(float2) * static_cast<size_t>(L.C * L.nvt));
+    L.dscr = o; o = up256(o + 2 * static_cast<size_t>(T) * static_cast<size_t>(L.ldc));
+    L.acc = o; o = up256(o + (L.nvchunks > 1 ? sizeof(float) * static_cast<size_t>(T * H) : 0));
+    L.total = o;
+    return L;
+}
+
+int run_two_pass(const Args& a, const Layout2& L, float scale) {
+    using namespace tc;
+    if (int rc = ensure_sort_attr()) return rc;
+    const __nv_bfloat16* X = static_cast<const __nv_bfloat16*>(a.X);
+    const __nv_bfloat16* W = static_cast<const __nv_bfloat16*>(a.W);
+    float* lse = reinterpret_cast<float*>(a.ws + L.lse);
+    float* lossrow = reinterpret_cast<float*>(a.ws + L.lossrow);
+    float* zlab = reinterpret_cast<float*>(a.ws + L.zlab);
+    Hdr* hdr = reinterpret_cast<Hdr*>(a.ws + L.hdr);
+    float2* part = reinterpret_cast<float2*>(a.ws + L.part);
+    __nv_bfloat16* D = reinterpret_cast<__nv_bfloat16*>(a.ws + L.dscr);
+    float* acc = reinterpret_cast<float*>(a.ws + L.acc);
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(a.ws + L.keys);
+    int* lstart = reinterpret_cast<int*>(a.ws + L.lstart);
+    const int H = static_cast<int>(a.H), V = static_cast<int>(a.V), T = static_cast<int>(a.T);
+    int rc;
+    CUtensorMap mW_k;
+    if ((rc = make_map(&mW_k, W, H, V, H, BK, BN))) return rc;
+    // pass 1: lse and the loss terms, token chunk by token chunk (the chunk's X stays in L2)
+    const size_t fac_smem = sizeof(float) * static_cast<size_t>(L.nvt);
+    for (int64_t t0 = 0; t0 < a.T; t0 += L.C) {
+        const int cl = static_cast<int>(std::min(L.C, a.T - t0));
+        CUtensorMap mX_k;
+        if ((rc = make_map(&mX_k, X + t0 * H, H, cl, H, BK, BM))) return rc;
+        EpiParams e{};
+        e.err = &hdr->err;
+        e.ignore_index = a.ignore;
+        e.labels = a.labels + t0;
+        e.M = cl;
+        e.N = V;
+        e.raster = RASTER_M_FASTEST;
+        e.hint_a = HINT_EVICT_LAST;
+        e.hint_b = HINT_EVICT_FIRST;
+        e.p_out = nullptr;   // partials and the label logit only
+        e.part = part;
+        e.nvt = static_cast<int>(L.nvt);
+        e.zlab = zlab + t0;
+        if ((rc = launch_gemm<0, 0, EPI_LOGITS>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
+        dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
+                                                          zlab + t0, nullptr, 0, V, scale, lse + t0, lossrow + t0);
+        if ((rc = check_launch("dlogits_bf16"))) return rc;
+    }
+    // label keys of all tokens, sorted in segments of kMaxSortKeys, one start table per segment
+    if (a.dW) {
+        for (int64_t sg = 0; sg < L.nseg; ++sg) {
+            const int64_t b0 = sg * kMaxSortKeys;
+            const int n = static_cast<int>(std::min<int64_t>(kMaxSortKeys, a.T - b0));
+            int npow2 = 1;
+            while (npow2 < n) npow2 <<= 1;
+            sort_label_keys<<<1, 1024, sizeof(unsigned long long) * npow2, a.st>>>(
+                a.labels + b0, n, a.ignore, npow2, static_cast<unsigned>(b0), keys + b0);
+            if ((rc = check_launch("sort_label_keys"))) return rc;
+            label_starts<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(V + 1, 256), 8 * sm_count())), 256, 0,
+                           a.st>>>(keys + b0, n, V, static_cast<int>(b0), lstart + sg * (V + 1));
+            if ((rc = check_launch("label_starts"))) return rc;
+        }
+    }
+    // pass 2: per vocabulary chunk, recompute the logits, D_c, dX +=, dW_c
+    CUtensorMap mX_all, mX_mn;
+    if ((rc = make_map(&mX_all, X, H, T, H, BK, BM))) return rc;     // A of the recompute (K-major)
+    if ((rc = make_map(&mX_mn, X, H, T, H, MN_BOX, BK))) return rc;  // B of dW_c (MN-major)
+    for (int64_t c = 0; c < L.nvchunks; ++c) {
+        const int64_t c0 = c * L.Vc;
+        const int vl = static_cast<int>(std::min(L.Vc, a.V - c0));
+        const bool last = c == L.nvchunks - 1;
+        const __nv_bfloat16* Wc = W + c0 * H;
+        CUtensorMap mWc_k, mWc_mn, mD_k, mD_mn;
+        if ((rc = make_map(&mWc_k, Wc, H, vl, H, BK, BN))) return rc;
+        if ((rc = make_map(&mWc_mn, Wc, H, vl, H, MN_BOX, BK))) return rc;
+        if ((rc = make_map(&mD_k, D, vl, T, L.ldc, BK, BM))) return rc;
+        if ((rc = make_map(&mD_mn, D, vl, T, L.ldc, MN_BOX, BK))) return rc;
+        EpiParams e{};
+        e.err = &hdr->err;
+        e.ignore_index = a.ignore;
+        e.labels = a.labels;
+        // a. D_c = scale * softmax part, from the recomputed logits and lse
+        e.M = T;
+        e.N = vl;
+        e.raster = RASTER_N_FASTEST;
+        e.hint_a = HINT_EVICT_FIRST;   // X: streamed once per chunk
+        e.hint_b = HINT_EVICT_LAST;    // W_c: reused by every token block
+        e.lse = lse;
+        e.corr_scale = scale;
+        e.out = D;
+        e.ldo = L.ldc;
+        if ((rc = launch_gemm<0, 0, EPI_SOFTMAX>(mX_all, mWc_k, T, vl, H, e, a.st))) return rc;
+        // b. dX (+)= D_c W_c in fp32, the one-hot part subtracted once (first chunk)
+        if (a.dX) {
+            EpiParams d{};
+            d.err = &hdr->err;
+            d.ignore_index = a.ignore;
+            d.labels = a.labels;
+            d.corr_src = c == 0 ? W : nullptr;
+            d.ld_corr = H;
+            d.corr_scale = scale;
+            d.M = T;
+            d.N = H;
+            d.raster = RASTER_N_GROUPS;
+            d.acc = acc;
+            d.lda = H;
+            d.acc_read = c > 0 ? 1 : 0;
+            d.acc_write = last ? 0 : 1;
+            d.out_write = last ? 1 : 0;
+            d.out = static_cast<__nv_bfloat16*>(a.dX);
+            d.ldo = H;
+            if ((rc = launch_gemm<0, 1, EPI_ACCUM>(mD_k, mWc_mn, T, H, vl, d, a.st))) return rc;
+        }
+        // c. dW_c = D_c^T X, minus scale * X_t for the tokens labelled with each row
+        if (a.dW) {
+            EpiParams d{};
+            d.err = &hdr->err;
+            d.ignore_index = a.ignore;
+            d.corr_src = X;
+            d.ld_corr = H;
+            d.corr_scale = scale;
+            d.keys = keys;
+            d.nkeys = T;
+            d.lstart = lstart + c0;
+            d.nseg = static_cast<int>(L.nseg);
+            d.lstride = V + 1;
+            d.M = vl;
+            d.N = H;
+            d.raster = RASTER_N_FASTEST;
+            d.out_write = 1;
+            d.out = static_cast<__nv_bfloat16*>(a.dW) + c0 * H;
+            d.ldo = H;
+            if ((rc = launch_gemm<1, 1, EPI_ACCUM>(mD_mn, mX_mn, vl, H, T, d, a.st))) return rc;
+        }
+    }
+    return LIGER_OK;
+}
+
 }  // namespace
 }  // namespace liger
 
@@ -515,6 +698,66 @@ extern "C" size_t liger_linear_ce_workspace(int64_t T, int64_t H, int64_t V, int
     if (T < 0 || H <= 0 || V <= 0 || chunk < 0 || (dtype != LIGER_F32 && dtype != LIGER_BF16)) return 0;
     return layout(T, H, V, chunk, dtype).total;
 }
+
+namespace liger {
+namespace {
+
+struct CommonLayout {
+    size_t lse, lossrow, hdr, total;
+};
+
+// Shared tail of both entry points: pointer and workspace checks, the label
+// scan (bad labels -> LIGER_ERR_LABEL before any other work), the all-ignored
+// case, the gradient scale, the variant's GEMMs, the final loss.
+template <typename Run>
+int ce_entry(const char* who, const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H, int64_t V,
+             int64_t ignore_index, int reduction, float grad_scale, float* loss, void* dX, void* dW, void* ws,
+             size_t ws_bytes, int dtype, void* stream, const CommonLayout& CL, Run run) {
+    if (!X || !W || !loss || (T > 0 && !labels)) return fail(LIGER_ERR_NULL, "%s: X, W, labels, loss required", who);
+    if (!aligned16(X) || !aligned16(W) || (dX && !aligned16(dX)) || (dW && !aligned16(dW)) ||
+        (reinterpret_cast<uintptr_t>(loss) & 3) || (reinterpret_cast<uintptr_t>(labels) & 7))
+        return fail(LIGER_ERR_ALIGN, "%s: X, W, dX, dW must be 16-byte aligned", who);
+    if (!ws || ws_bytes < CL.total || (reinterpret_cast<uintptr_t>(ws) & 255))
+        return fail(LIGER_ERR_WORKSPACE, "%s: workspace of %zu bytes (256-byte aligned) required, got %zu", who,
+                    CL.total, ws_bytes);
+    cudaStream_t st = as_stream(stream);
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
+    Hdr* hdr = reinterpret_cast<Hdr*>(w8 + CL.hdr);
+    if (cudaMemsetAsync(hdr, 0, sizeof(Hdr), st) != cudaSuccess) return check_launch("linear_ce memset");
+    Hdr h{};
+    if (T > 0) {
+        const int grid = static_cast<int>(std::min<int64_t>(ceil_div(T, 256), 4 * sm_count()));
+        label_scan<<<grid, 256, 0, st>>>(labels, T, V, ignore_index, hdr);
+        if (int rc = check_launch("label_scan")) return rc;
+        if (cudaMemcpyAsync(&h, hdr, sizeof(Hdr), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return check_launch("linear_ce label scan");
+        if (h.bad) return fail(LIGER_ERR_LABEL, "%s: a label is outside [0, %lld) and is not %lld", who,
+                               (long long)V, (long long)ignore_index);
+    }
+    const int64_t n_valid = static_cast<int64_t>(h.n_valid);
+    const size_t esz = dtype == LIGER_F32 ? 4 : 2;
+    if (n_valid == 0) {
+        // nothing to learn from: loss 0, zero gradients (PyTorch would give NaN for the mean)
+        bool ok = cudaMemsetAsync(loss, 0, sizeof(float), st) == cudaSuccess;
+        if (dX) ok = ok && cudaMemsetAsync(dX, 0, static_cast<size_t>(T * H) * esz, st) == cudaSuccess;
+        if (dW) ok = ok && cudaMemsetAsync(dW, 0, static_cast<size_t>(V * H) * esz, st) == cudaSuccess;
+        if (T > 0) ok = ok && cudaMemsetAsync(w8 + CL.lse, 0, sizeof(float) * static_cast<size_t>(T), st) == cudaSuccess;
+        if (T > 0)
+            ok = ok && cudaMemsetAsync(w8 + CL.lossrow, 0, sizeof(float) * static_cast<size_t>(T), st) == cudaSuccess;
+        return ok ? LIGER_OK : check_launch("linear_ce memset");
+    }
+    const float scale = reduction == 0 ? static_cast<float>(static_cast<double>(grad_scale) / static_cast<double>(n_valid))
+                                       : grad_scale;
+    Args a{X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st};
+    if (int rc = run(a, scale)) return rc;
+    const double denom = reduction == 0 ? static_cast<double>(n_valid) : 1.0;
+    loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + CL.lossrow), T, denom, hdr, loss);
+    return check_launch("loss_final");
+}
+
+}  // namespace
+}  // namespace liger
 
 extern "C" int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H,
                                        int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
@@ -526,49 +769,35 @@ extern "C" int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64
         (reduction != 0 && reduction != 1))
         return fail(LIGER_ERR_SHAPE, "linear_ce: T=%lld H=%lld V=%lld chunk=%lld reduction=%d", (long long)T,
                     (long long)H, (long long)V, (long long)chunk, reduction);
-    if (!X || !W || !loss || (T > 0 && !labels)) return fail(LIGER_ERR_NULL, "linear_ce: X, W, labels, loss required");
-    if (!aligned16(X) || !aligned16(W) || (dX && !aligned16(dX)) || (dW && !aligned16(dW)) ||
-        (reinterpret_cast<uintptr_t>(loss) & 3) || (reinterpret_cast<uintptr_t>(labels) & 7))
-        return fail(LIGER_ERR_ALIGN, "linear_ce: X, W, dX, dW must be 16-byte aligned");
     const Layout L = layout(T, H, V, chunk, dtype);
-    if (!ws || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255))
-        return fail(LIGER_ERR_WORKSPACE, "linear_ce: workspace of %zu bytes (256-byte aligned) required, got %zu",
-                    L.total, ws_bytes);
-    cudaStream_t st = as_stream(stream);
-    uint8_t* w8 = static_cast<uint8_t*>(ws);
-    Hdr* hdr = reinterpret_cast<Hdr*>(w8 + L.hdr);
-    if (cudaMemsetAsync(hdr, 0, sizeof(Hdr), st) != cudaSuccess) return check_launch("linear_ce memset");
-    Hdr h{};
-    if (T > 0) {
-        const int grid = static_cast<int>(std::min<int64_t>(ceil_div(T, 256), 4 * sm_count()));
-        label_scan<<<grid, 256, 0, st>>>(labels, T, V, ignore_index, hdr);
-        if (int rc = check_launch("label_scan")) return rc;
-        if (cudaMemcpyAsync(&h, hdr, sizeof(Hdr), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-            cudaStreamSynchronize(st) != cudaSuccess)
-            return check_launch("linear_ce label scan");
-        if (h.bad) return fail(LIGER_ERR_LABEL, "linear_ce: a label is outside [0, %lld) and is not %lld", (long long)V,
-                               (long long)ignore_index);
-    }
-    const int64_t n_valid = static_cast<int64_t>(h.n_valid);
-    const size_t esz = dtype == LIGER_F32 ? 4 : 2;
-    if (n_valid == 0) {
-        // nothing to learn from: loss 0, zero gradients (PyTorch would give NaN for the mean)
-        bool ok = cudaMemsetAsync(loss, 0, sizeof(float), st) == cudaSuccess;
-        if (dX) ok = ok && cudaMemsetAsync(dX, 0, static_cast<size_t>(T * H) * esz, st) == cudaSuccess;
-        if (dW) ok = ok && cudaMemsetAsync(dW, 0, static_cast<size_t>(V * H) * esz, st) == cudaSuccess;
-        if (T > 0) ok = ok && cudaMemsetAsync(w8 + L.lse, 0, sizeof(float) * static_cast<size_t>(T), st) == cudaSuccess;
-        if (T > 0) ok = ok && cudaMemsetAsync(w8 + L.lossrow, 0, sizeof(float) * static_cast<size_t>(T), st) == cudaSuccess;
-        return ok ? LIGER_OK : check_launch("linear_ce memset");
-    }
-    const float scale = reduction == 0 ? static_cast<float>(static_cast<double>(grad_scale) / static_cast<double>(n_valid))
-                                       : grad_scale;
-    Args a{X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st};
-    int rc;
-    if (L.tc) rc = run_tc(a, L, scale);
-    else if (dtype == LIGER_F32) rc = run_simt<float>(a, L, scale);
-    else rc = run_simt<__nv_bfloat16>(a, L, scale);
-    if (rc) return rc;
-    const double denom = reduction == 0 ? static_cast<double>(n_valid) : 1.0;
-    loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + L.lossrow), T, denom, hdr, loss);
-    return check_launch("loss_final");
+    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.total};
+    return ce_entry("linear_ce", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws,
+                    ws_bytes, dtype, stream, CL, [&](const Args& a, float scale) {
+                        if (L.tc) return run_tc(a, L, scale);
+                        if (dtype == LIGER_F32) return run_simt<float>(a, L, scale);
+                        return run_simt<__nv_bfloat16>(a, L, scale);
+                    });
+}
+
+extern "C" size_t liger_linear_ce_two_pass_workspace(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
+    if (T < 0 || H <= 0 || V <= 0 || vchunk < 0) return 0;
+    return layout2(T, H, V, vchunk).total;
+}
+
+extern "C" int liger_linear_ce_two_pass_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T,
+                                                int64_t H, int64_t V, int64_t ignore_index, int reduction,
+                                                float grad_scale, float* loss, void* dX, void* dW, void* ws,
+                                                size_t ws_bytes, int64_t vchunk, int dtype, void* stream) {
+    clear_error();
+    if (dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "linear_ce_two_pass: bf16 only (tensor-core path)");
+    if (T < 0 || H < 64 || H % 8 || V < 256 || vchunk < 0 || (vchunk % 8) || H > (1 << 30) || V > (1 << 30) ||
+        T > (int64_t{1} << 31) - 1 || (reduction != 0 && reduction != 1))
+        return fail(LIGER_ERR_SHAPE, "linear_ce_two_pass: T=%lld H=%lld V=%lld vchunk=%lld reduction=%d "
+                    "(H >= 64 and a multiple of 8, V >= 256, vchunk a multiple of 8)", (long long)T, (long long)H,
+                    (long long)V, (long long)vchunk, reduction);
+    const Layout2 L = layout2(T, H, V, vchunk);
+    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.total};
+    return ce_entry("linear_ce_two_pass", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW,
+                    ws, ws_bytes, dtype, stream, CL,
+                    [&](const Args& a, float scale) { return run_two_pass(a, L, scale); });
 }

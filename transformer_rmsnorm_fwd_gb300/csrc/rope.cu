@@ -28,6 +28,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "rope_angle.cuh"
 
 namespace liger {
 namespace {
@@ -51,18 +52,6 @@ struct RopeArgs {
     int B, S, Hq, Hk, D, npos;
     float sign;
 };
-
-__device__ __forceinline__ float2 angle_cs(double p, double inv_freq, float sign) {
-    const double two_pi_hi = 6.283185307179586232;      // nearest double to 2 pi
-    const double two_pi_lo = 2.4492935982947064e-16;    // 2 pi - two_pi_hi
-    const double phi = p * inv_freq;
-    const double k = rint(phi * 0.15915494309189535);   // 1 / (2 pi)
-    double r = fma(-k, two_pi_hi, phi);
-    r = fma(-k, two_pi_lo, r);
-    float s, c;
-    sincosf(static_cast<float>(r), &s, &c);
-    return make_float2(c, sign * s);
-}
 
 // VEC: 16-byte vectors (else scalar); INTER: interleaved pairs (2i, 2i+1).
 template <typename T, bool VEC, bool INTER>

@@ -49,7 +49,15 @@ constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 
-enum Epi : int { EPI_LOGITS = 0, EPI_STORE = 1, EPI_ACCUM = 2, EPI_SWIGLU = 3, EPI_SWIGLU_BWD = 4 };
+enum Epi : int {
+    EPI_LOGITS = 0,
+    EPI_STORE = 1,
+    EPI_ACCUM = 2,
+    EPI_SWIGLU = 3,
+    EPI_SWIGLU_BWD = 4,
+    EPI_QKV_ROPE = 5,
+    EPI_SOFTMAX = 6
+};
 
 // Tile order of the persistent loop: m fastest, n fastest, or groups of
 // GROUP_N tile columns with n fastest inside a group (for long-K problems
@@ -64,7 +72,8 @@ struct EpiParams {
     int M, N;                           // logical problem size (epilogue masks)
     int raster;                         // tile order (Raster)
     int* err;                           // error word (device)
-    // EPI_LOGITS: P = exp(z - m_tile) as bf16, per-(row, n-tile) (m, sum), z at label
+    // EPI_LOGITS: P = exp(z - m_tile) as bf16 (not written if p_out is null),
+    // per-(row, n-tile) (m, sum), z at label
     const int64_t* labels;              // [M] (chunk rows)
     int64_t ignore_index;
     __nv_bfloat16* p_out;
@@ -75,7 +84,9 @@ struct EpiParams {
     // EPI_STORE: bf16 out [M, N] (ldo), rows with label == ignore_index -> +0
     __nv_bfloat16* out;
     int64_t ldo;
-    // EPI_ACCUM: fp32 accumulator acc [M, N] (lda); flags
+    // EPI_ACCUM: fp32 accumulator acc [M, N] (lda); flags.  With labels set, rows
+    // labelled ignore_index are written +0 and, if corr_src is set without keys,
+    // corr_scale * corr_src[labels[row], :] is subtracted (as EPI_STORE does).
     float* acc;
     int64_t lda;
     int acc_read, acc_write, out_write;
@@ -86,9 +97,16 @@ struct EpiParams {
     const __nv_bfloat16* corr_src;
     int64_t ld_corr;
     float corr_scale;
+    // The keys may come in nseg sorted segments with one start table each,
+    // lstride ints apart (nseg 0 counts as 1).
     const unsigned long long* keys;
     int nkeys;
     const int* lstart;
+    int nseg;
+    int64_t lstride;
+    // EPI_SOFTMAX: out[row, col] = corr_scale * exp(z - lse[row]) (bf16; +0 on rows
+    // labelled ignore_index), the softmax part of the logit gradient
+    const float* lse;
     // L2 policies (Hint) of the A and B loads; streaming epilogue traffic (P, the
     // fp32 accumulator, dW) always uses evict-first accesses
     int hint_a, hint_b;
@@ -102,7 +120,21 @@ struct EpiParams {
     // accumulator and writes out = dg (dh u s (1 + g (1 - s))), out2 = du (dh g s).
     const __nv_bfloat16* src;
     int64_t lds;
-    __nv_bfloat16* out2;   // [M + 1]: the tokens labelled with row v are keys[lstart[v] .. lstart[v+1])
+    __nv_bfloat16* out2;
+    // EPI_QKV_ROPE: y = acc * rs[row] + bias[col] over heads of hd columns (hd divides
+    // BN); heads below nq + nk (q, then k) are rotated, pairs (j, j + hd/2), by the
+    // angle row cos_t/sin_t[tr] (ld_tab floats), tr = tab_row ? clamp(tab_row[row],
+    // 0, n_tab - 1) : row % tab_mod; q -> out [M, nq], k -> out2 [M, nk],
+    // v -> out3 [M, N - nq - nk]
+    const float* rs;
+    const float* bias;
+    const float* cos_t;
+    const float* sin_t;
+    int64_t ld_tab;
+    const int32_t* tab_row;
+    int n_tab, tab_mod;
+    int hd, nq, nk;
+    __nv_bfloat16* out3;
 };
 
 // ------------------------------------------------------------ PTX wrappers
@@ -461,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         v[j] = e;
                         sum += e;
                     }
-                    if (live) {
+                    if (live && ep.p_out != nullptr) {
 #pragma unroll
                         for (int g = 0; g < 4; ++g) {
                             const int col = n0 + c * 32 + g * 8;
@@ -564,8 +596,129 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty_bar(as));
+            } else if (EPI == EPI_SOFTMAX) {
+                const int64_t y = row_ok ? ep.labels[row] : ep.ignore_index;
+                const bool live = row_ok && y != ep.ignore_index;
+                const float l2 = live ? ep.lse[row] * 1.4426950408889634f : 0.f;
+                __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(taddr + c * 32, v);
+                    if (row_ok) {
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) {
+                            const int col = n0 + c * 32 + g * 8;
+                            if (col < ep.N) {
+                                float a[8];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    a[e] = live ? ep.corr_scale * exp2f(fmaf(v[g * 8 + e], 1.4426950408889634f, -l2))
+                                                : 0.f;
+                                stg16(orow + c * 32 + g * 8, pack(a));
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(as));
+            } else if (EPI == EPI_QKV_ROPE) {
+                const float rsv = row_ok ? ep.rs[row] : 0.f;
+                int64_t tr = 0;
+                if (row_ok) {
+                    if (ep.tab_row != nullptr) {
+                        const int p = ep.tab_row[row];
+                        tr = p < 0 ? 0 : (p >= ep.n_tab ? ep.n_tab - 1 : p);
+                    } else {
+                        tr = row % ep.tab_mod;
+                    }
+                }
+                const float* crow = ep.cos_t + tr * ep.ld_tab;
+                const float* srow = ep.sin_t + tr * ep.ld_tab;
+                const int hd = ep.hd, half = hd >> 1;
+#pragma unroll 1
+                for (int h0 = 0; h0 < BN; h0 += hd) {
+                    const int gc = n0 + h0;   // first column of this head
+                    if (gc >= ep.N) break;
+                    __nv_bfloat16* dst;
+                    if (gc < ep.nq) {
+                        dst = ep.out + static_cast<int64_t>(row) * ep.nq + gc;
+                    } else if (gc < ep.nq + ep.nk) {
+                        dst = ep.out2 + static_cast<int64_t>(row) * ep.nk + (gc - ep.nq);
+                    } else {
+                        dst = ep.out3 + static_cast<int64_t>(row) * (ep.N - ep.nq - ep.nk) + (gc - ep.nq - ep.nk);
+                    }
+                    const float* bh = ep.bias + gc;
+                    if (gc < ep.nq + ep.nk) {
+#pragma unroll 1
+                        for (int j = 0; j < half; j += 32) {
+                            float a[32], b[32];
+                            tmem_ld32(taddr + h0 + j, a);
+                            tmem_ld32(taddr + h0 + half + j, b);
+                            if (row_ok) {
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) {
+                                    const int o = j + g * 8;
+                                    float cs[8], sn[8], ba[8], bb[8], y1[8], y2[8];
+                                    *reinterpret_cast<float4*>(cs) = __ldg(reinterpret_cast<const float4*>(crow + o));
+                                    *reinterpret_cast<float4*>(cs + 4) =
+                                        __ldg(reinterpret_cast<const float4*>(crow + o + 4));
+                                    *reinterpret_cast<float4*>(sn) = __ldg(reinterpret_cast<const float4*>(srow + o));
+                                    *reinterpret_cast<float4*>(sn + 4) =
+                                        __ldg(reinterpret_cast<const float4*>(srow + o + 4));
+                                    *reinterpret_cast<float4*>(ba) = __ldg(reinterpret_cast<const float4*>(bh + o));
+                                    *reinterpret_cast<float4*>(ba + 4) =
+                                        __ldg(reinterpret_cast<const float4*>(bh + o + 4));
+                                    *reinterpret_cast<float4*>(bb) =
+                                        __ldg(reinterpret_cast<const float4*>(bh + half + o));
+                                    *reinterpret_cast<float4*>(bb + 4) =
+                                        __ldg(reinterpret_cast<const float4*>(bh + half + o + 4));
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        const float x1 = fmaf(a[g * 8 + e], rsv, ba[e]);
+                                        const float x2 = fmaf(b[g * 8 + e], rsv, bb[e]);
+                                        y1[e] = x1 * cs[e] - x2 * sn[e];
+                                        y2[e] = x2 * cs[e] + x1 * sn[e];
+                                    }
+                                    stg16(dst + o, pack(y1));
+                                    stg16(dst + half + o, pack(y2));
+                                }
+                            }
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int j = 0; j < hd; j += 32) {
+                            float a[32];
+                            tmem_ld32(taddr + h0 + j, a);
+                            if (row_ok) {
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) {
+                                    const int o = j + g * 8;
+                                    float ba[8], y[8];
+                                    *reinterpret_cast<float4*>(ba) = __ldg(reinterpret_cast<const float4*>(bh + o));
+                                    *reinterpret_cast<float4*>(ba + 4) =
+                                        __ldg(reinterpret_cast<const float4*>(bh + o + 4));
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) y[e] = fmaf(a[g * 8 + e], rsv, ba[e]);
+                                    stg16(dst + o, pack(y));
+                                }
+                            }
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(as));
             } else {
                 __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
+                const int64_t ylab = (row_ok && ep.labels != nullptr) ? ep.labels[row] : ep.ignore_index;
+                const bool zero_row = ep.labels != nullptr && ylab == ep.ignore_index;
+                const __nv_bfloat16* lrow = (ep.labels != nullptr && ep.corr_src != nullptr && ep.keys == nullptr &&
+                                             row_ok && !zero_row)
+                                                ? ep.corr_src + ylab * ep.ld_corr + n0
+                                                : nullptr;
+                const int nseg = ep.nseg > 1 ? ep.nseg : 1;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint4 nxt[8];
@@ -579,10 +732,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
-                    for (int kk = k_lo; kk < k_hi; ++kk) {
-                        const int64_t t = static_cast<int64_t>(ep.keys[kk] & 0xFFFFFFFFull);
-                        sub_scaled32(v, ep.corr_src + t * ep.ld_corr + n0 + c * 32, ep.corr_scale,
-                                     ep.N - (n0 + c * 32));
+                    for (int sg = 0; sg < nseg; ++sg) {
+                        int lo = k_lo, hi = k_hi;
+                        if (sg > 0) {
+                            lo = row_ok ? ep.lstart[sg * ep.lstride + row] : 0;
+                            hi = row_ok ? ep.lstart[sg * ep.lstride + row + 1] : 0;
+                        }
+                        for (int kk = lo; kk < hi; ++kk) {
+                            const int64_t t = static_cast<int64_t>(ep.keys[kk] & 0xFFFFFFFFull);
+                            sub_scaled32(v, ep.corr_src + t * ep.ld_corr + n0 + c * 32, ep.corr_scale,
+                                         ep.N - (n0 + c * 32));
+                        }
+                    }
+                    if (lrow != nullptr) sub_scaled32(v, lrow + c * 32, ep.corr_scale, ep.N - (n0 + c * 32));
+                    if (zero_row) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
                     }
                     if (row_ok) {
 #pragma unroll
