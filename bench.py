@@ -50,6 +50,12 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--op", default="chain",
+                   choices=["chain", "linear_ce", "linear_ce_two_pass", "rmsnorm_qkv_rope", "fused_linear_swiglu",
+                            "rmsnorm", "rope", "swiglu"],
+                   help="chain: the benchmark step (default); otherwise time that one operator alone at --seq "
+                        "tokens (single-kernel profiling cases; prints a JSON line with ms per call)")
+    p.add_argument("--chunk", type=int, default=0, help="--op linear_ce: token chunk (0 = automatic)")
     return p.parse_args(argv)
 
 
@@ -604,10 +610,108 @@ def native_arm(args):
     return 0
 
 
+def single_op(args):
+    """One operator alone, W untimed + K timed calls on device-resident inputs
+    (the profiling cases: small enough for a few GB on the device)."""
+    import torch
+    import transformer_rmsnorm_fwd_gb300 as L
+    from datagen import labels, normal
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L.load()
+    S, op = args.seq, args.op
+    bf = torch.bfloat16
+    if op in ("linear_ce", "linear_ce_two_pass"):
+        X = to_torch(normal(7, "op.X", (S, HIDDEN), "bf16"), dev)
+        W = to_torch(normal(7, "op.W", (VOCAB, HIDDEN), "bf16", 0.0, 0.02), dev)
+        lab = torch.from_numpy(labels(7, "op.labels", S, VOCAB, 0.1)).to(dev)
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+        dX, dW = torch.empty_like(X), torch.empty_like(W)
+        if op == "linear_ce":
+            ws = torch.empty(L.liger_linear_ce_workspace(S, HIDDEN, VOCAB, args.chunk, L.LIGER_BF16),
+                             dtype=torch.uint8, device=dev)
+            fn = lambda: L.liger_linear_ce_fwd_bwd(X, W, lab, loss, dX, dW, ws, chunk=args.chunk)
+            flops = 6.0 * S * HIDDEN * VOCAB
+        else:
+            ws = torch.empty(L.liger_linear_ce_two_pass_workspace(S, HIDDEN, VOCAB), dtype=torch.uint8, device=dev)
+            fn = lambda: L.liger_linear_ce_two_pass_fwd_bwd(X, W, lab, loss, dX, dW, ws)
+            flops = 8.0 * S * HIDDEN * VOCAB
+    elif op == "rmsnorm_qkv_rope":
+        N = 3 * HEADS * HEAD_DIM
+        x = to_torch(normal(7, "op.x", (S, HIDDEN), "bf16"), dev)
+        wn = to_torch(normal(7, "op.w", (HIDDEN,), "bf16", 1.0, 0.1), dev)
+        Wq, Wk, Wv = (to_torch(normal(7, f"op.W{c}", (HEADS * HEAD_DIM, HIDDEN), "bf16", 0.0, 0.02), dev)
+                      for c in "qkv")
+        q = torch.empty(1, S, HEADS, HEAD_DIM, dtype=bf, device=dev)
+        k, v = torch.empty_like(q), torch.empty_like(q)
+        ws = torch.empty(L.liger_rmsnorm_qkv_rope_workspace(S, HIDDEN, HEADS, HEADS, HEAD_DIM), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: L.liger_rmsnorm_qkv_rope_fwd(x, wn, Wq, Wk, Wv, q, k, v, ws, 1, S, HEADS, HEADS, HEAD_DIM,
+                                                  eps=EPS, theta=THETA)
+        flops = 2.0 * S * HIDDEN * N
+    elif op in ("rmsnorm", "rope", "swiglu"):
+        # forward then backward, HBM-bound: report GB/s of the algorithmic bytes
+        e = 2
+        if op == "rmsnorm":
+            x = to_torch(normal(7, "op.rx", (S, HIDDEN), "bf16"), dev)
+            w = to_torch(normal(7, "op.rw", (HIDDEN,), "bf16", 1.0, 0.1), dev)
+            dy = to_torch(normal(7, "op.rdy", (S, HIDDEN), "bf16"), dev)
+            y, dx, dw = torch.empty_like(x), torch.empty_like(x), torch.empty_like(w)
+            rstd = torch.empty(S, dtype=torch.float32, device=dev)
+            wsr = torch.empty(L.liger_rmsnorm_bwd_workspace(S, HIDDEN), dtype=torch.uint8, device=dev)
+
+            def fn():
+                L.liger_rmsnorm_fwd(x, w, y, rstd, EPS)
+                L.liger_rmsnorm_bwd(dy, x, w, rstd, dx, dw, wsr)
+            nbytes = (2 * S * HIDDEN * e + 4 * S) + (3 * S * HIDDEN * e + 4 * S)
+        elif op == "rope":
+            q = to_torch(normal(7, "op.q", (1, S, HEADS, HEAD_DIM), "bf16"), dev)
+            k = to_torch(normal(7, "op.k", (1, S, HEADS, HEAD_DIM), "bf16"), dev)
+
+            def fn():
+                L.liger_rope_fwd(q, k, None, THETA)
+                L.liger_rope_bwd(q, k, None, THETA)
+            nbytes = 2 * (2 * 2 * S * HEADS * HEAD_DIM * e)
+        else:
+            g = to_torch(normal(7, "op.g", (S, INTER), "bf16"), dev)
+            u = to_torch(normal(7, "op.u", (S, INTER), "bf16"), dev)
+            dy = to_torch(normal(7, "op.sdy", (S, INTER), "bf16"), dev)
+            y, dg, du = torch.empty_like(g), torch.empty_like(g), torch.empty_like(g)
+
+            def fn():
+                L.liger_swiglu_fwd(g, u, y)
+                L.liger_swiglu_bwd(dy, g, u, dg, du)
+            nbytes = 3 * S * INTER * e + 5 * S * INTER * e
+        flops = None
+    else:
+        X = to_torch(normal(7, "op.mX", (S, HIDDEN), "bf16"), dev)
+        Wg = to_torch(normal(7, "op.Wg", (INTER, HIDDEN), "bf16", 0.0, 0.02), dev)
+        Wu = to_torch(normal(7, "op.Wu", (INTER, HIDDEN), "bf16", 0.0, 0.02), dev)
+        out = torch.empty(S, INTER, dtype=bf, device=dev)
+        fn = lambda: L.liger_fused_linear_swiglu_fwd(X, Wg, Wu, out)
+        flops = 4.0 * S * HIDDEN * INTER
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / max(1, args.steps)
+    rate = {"tflops": flops / ms / 1e9} if flops else {"gbs": nbytes / ms / 1e6}
+    emit(dict({"op": op, "seq": S, "ms_per_call": ms, "steps": args.steps, "warmup": args.warmup,
+               "note": "single operator alone (profiling case), not the benchmark step"}, **rate))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return reference_arm(args)
+    if args.op != "chain":
+        return single_op(args)
     return native_arm(args)
 
 

@@ -434,7 +434,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     const int H = static_cast<int>(a.H), V = static_cast<int>(a.V);
     int rc;
     CUtensorMap mW_k, mW_mn;
-    if ((rc = make_map(&mW_k, W, H, V, H, BK, BN))) return rc;          // B of Z = X W^T  (K-major)
+    if ((rc = make_map(&mW_k, W, H, V, H, BK, B_BOX_ROWS))) return rc;          // B of Z = X W^T  (K-major)
     if ((rc = make_map(&mW_mn, W, H, V, H, MN_BOX, BK))) return rc;     // B of dX = D W   (MN-major)
     const size_t fac_smem = sizeof(float) * static_cast<size_t>(L.nvt);
     for (int64_t c = 0; c < L.nchunks; ++c) {
@@ -463,7 +463,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
         e.part = part;
         e.nvt = static_cast<int>(L.nvt);
         e.zlab = zlab + t0;
-        if ((rc = launch_gemm<0, 0, EPI_LOGITS>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
+        if ((rc = launch_gemm<0, 0, EPI_LOGITS, 1>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
         // 2. lse, loss terms, P -> D in place
         dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
                                                           zlab + t0, P, L.ldp, V, scale, lse + t0, lossrow + t0);
@@ -481,7 +481,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             d.corr_src = W;
             d.ld_corr = H;
             d.corr_scale = scale;
-            if ((rc = launch_gemm<0, 1, EPI_STORE>(mD_k, mW_mn, cl, H, V, d, a.st))) return rc;
+            if ((rc = launch_gemm<0, 1, EPI_STORE, 1>(mD_k, mW_mn, cl, H, V, d, a.st))) return rc;
         }
         // 4. dW (+)= D^T X_c, minus scale * X_t in fp32 for each token t labelled with the row
         if (a.dW) {
@@ -513,7 +513,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             d.acc_read = first ? 0 : 1;
             d.acc_write = last ? 0 : 1;
             d.out_write = last ? 1 : 0;
-            if ((rc = launch_gemm<1, 1, EPI_ACCUM>(mD_mn, mX_mn, V, H, cl, d, a.st))) return rc;
+            if ((rc = launch_gemm<1, 1, EPI_ACCUM, 1>(mD_mn, mX_mn, V, H, cl, d, a.st))) return rc;
         }
     }
     return LIGER_OK;
@@ -574,7 +574,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
     const int H = static_cast<int>(a.H), V = static_cast<int>(a.V), T = static_cast<int>(a.T);
     int rc;
     CUtensorMap mW_k;
-    if ((rc = make_map(&mW_k, W, H, V, H, BK, BN))) return rc;
+    if ((rc = make_map(&mW_k, W, H, V, H, BK, B_BOX_ROWS))) return rc;
     // pass 1: lse and the loss terms, token chunk by token chunk (the chunk's X stays in L2)
     const size_t fac_smem = sizeof(float) * static_cast<size_t>(L.nvt);
     for (int64_t t0 = 0; t0 < a.T; t0 += L.C) {
@@ -594,7 +594,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         e.part = part;
         e.nvt = static_cast<int>(L.nvt);
         e.zlab = zlab + t0;
-        if ((rc = launch_gemm<0, 0, EPI_LOGITS>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
+        if ((rc = launch_gemm<0, 0, EPI_LOGITS, 1>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
         dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
                                                           zlab + t0, nullptr, 0, V, scale, lse + t0, lossrow + t0);
         if ((rc = check_launch("dlogits_bf16"))) return rc;
@@ -624,7 +624,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         const bool last = c == L.nvchunks - 1;
         const __nv_bfloat16* Wc = W + c0 * H;
         CUtensorMap mWc_k, mWc_mn, mD_k, mD_mn;
-        if ((rc = make_map(&mWc_k, Wc, H, vl, H, BK, BN))) return rc;
+        if ((rc = make_map(&mWc_k, Wc, H, vl, H, BK, B_BOX_ROWS))) return rc;
         if ((rc = make_map(&mWc_mn, Wc, H, vl, H, MN_BOX, BK))) return rc;
         if ((rc = make_map(&mD_k, D, vl, T, L.ldc, BK, BM))) return rc;
         if ((rc = make_map(&mD_mn, D, vl, T, L.ldc, MN_BOX, BK))) return rc;
@@ -642,7 +642,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         e.corr_scale = scale;
         e.out = D;
         e.ldo = L.ldc;
-        if ((rc = launch_gemm<0, 0, EPI_SOFTMAX>(mX_all, mWc_k, T, vl, H, e, a.st))) return rc;
+        if ((rc = launch_gemm<0, 0, EPI_SOFTMAX, 1>(mX_all, mWc_k, T, vl, H, e, a.st))) return rc;
         // b. dX (+)= D_c W_c in fp32, the one-hot part subtracted once (first chunk)
         if (a.dX) {
             EpiParams d{};
@@ -662,7 +662,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
             d.out_write = last ? 1 : 0;
             d.out = static_cast<__nv_bfloat16*>(a.dX);
             d.ldo = H;
-            if ((rc = launch_gemm<0, 1, EPI_ACCUM>(mD_k, mWc_mn, T, H, vl, d, a.st))) return rc;
+            if ((rc = launch_gemm<0, 1, EPI_ACCUM, 1>(mD_k, mWc_mn, T, H, vl, d, a.st))) return rc;
         }
         // c. dW_c = D_c^T X, minus scale * X_t for the tokens labelled with each row
         if (a.dW) {
@@ -683,7 +683,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
             d.out_write = 1;
             d.out = static_cast<__nv_bfloat16*>(a.dW) + c0 * H;
             d.ldo = H;
-            if ((rc = launch_gemm<1, 1, EPI_ACCUM>(mD_mn, mX_mn, vl, H, T, d, a.st))) return rc;
+            if ((rc = launch_gemm<1, 1, EPI_ACCUM, 1>(mD_mn, mX_mn, vl, H, T, d, a.st))) return rc;
         }
     }
     return LIGER_OK;

@@ -79,7 +79,7 @@ extern "C" int liger_fused_linear_swiglu_fwd(const void* X, const void* Wg, cons
     e.hint_a = HINT_EVICT_LAST;    // X: reused by every column tile
     e.hint_b = HINT_EVICT_FIRST;   // weights: streamed once
     const int ntile_n = static_cast<int>(ceil_div(I, BN / 2));
-    return launch_gemm<0, 0, EPI_SWIGLU>(mX, mG, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
+    return launch_gemm<0, 0, EPI_SWIGLU, 1>(mX, mG, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
                                          as_stream(stream), 0, &mX, &mU);
 }
 
@@ -133,7 +133,7 @@ extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, cons
     e.hint_a = HINT_EVICT_LAST;
     e.hint_b = HINT_EVICT_FIRST;
     const int ntile_n = static_cast<int>(ceil_div(I, BN / 2));
-    if ((rc = launch_gemm<0, 0, EPI_SWIGLU_BWD>(mX_k, mG_k, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
+    if ((rc = launch_gemm<0, 0, EPI_SWIGLU_BWD, 1>(mX_k, mG_k, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
                                                st, 0, &mX_k, &mU_k)))
         return rc;
     // 2. dX = dG W_g + dU W_u (K = 2I: k-blocks of the second product follow those of the first)
@@ -151,7 +151,7 @@ extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, cons
     d.ldo = H;
     d.ksplit_nkb = nkb1;
     d.raster = RASTER_N_GROUPS;
-    if ((rc = launch_gemm<0, 1, EPI_STORE>(mdG_k, mG_mn, static_cast<int>(T), static_cast<int>(H), 2 * nkb1 * BK, d,
+    if ((rc = launch_gemm<0, 1, EPI_STORE, 1>(mdG_k, mG_mn, static_cast<int>(T), static_cast<int>(H), 2 * nkb1 * BK, d,
                                            st, 0, &mdU_k, &mU_mn)))
         return rc;
     // 3. dW_g = dG^T X, dW_u = dU^T X (both operands MN-major, K = T)
@@ -169,10 +169,10 @@ extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, cons
     w.hint_a = HINT_EVICT_FIRST;
     w.hint_b = HINT_EVICT_LAST;   // X: reused by every row block
     w.out = static_cast<__nv_bfloat16*>(dWg);
-    if ((rc = launch_gemm<1, 1, EPI_ACCUM>(mdG_mn, mX_mn, static_cast<int>(I), static_cast<int>(H),
+    if ((rc = launch_gemm<1, 1, EPI_ACCUM, 1>(mdG_mn, mX_mn, static_cast<int>(I), static_cast<int>(H),
                                            static_cast<int>(T), w, st)))
         return rc;
     w.out = static_cast<__nv_bfloat16*>(dWu);
-    return launch_gemm<1, 1, EPI_ACCUM>(mdU_mn, mX_mn, static_cast<int>(I), static_cast<int>(H), static_cast<int>(T), w,
+    return launch_gemm<1, 1, EPI_ACCUM, 1>(mdU_mn, mX_mn, static_cast<int>(I), static_cast<int>(H), static_cast<int>(T), w,
                                         st);
 }

@@ -210,7 +210,7 @@ extern "C" int liger_rmsnorm_qkv_rope_fwd(const void* x, const void* w_norm, con
     CUtensorMap mX, mW;
     int rc;
     if ((rc = make_map(&mX, x, H, T, H, BK, BM))) return rc;
-    if ((rc = make_map(&mW, wf, H, N, H, BK, BN))) return rc;
+    if ((rc = make_map(&mW, wf, H, N, H, BK, B_BOX_ROWS))) return rc;
     int* d_err = nullptr;
     if ((rc = qkv_err_word(&d_err))) return rc;
     EpiParams e{};
@@ -245,6 +245,6 @@ extern "C" int liger_rmsnorm_qkv_rope_fwd(const void* x, const void* w_norm, con
     e.raster = RASTER_N_GROUPS;
     e.hint_a = HINT_NORMAL;
     e.hint_b = HINT_NORMAL;
-    return launch_gemm<0, 0, EPI_QKV_ROPE>(mX, mW, static_cast<int>(T), static_cast<int>(N), static_cast<int>(H), e,
+    return launch_gemm<0, 0, EPI_QKV_ROPE, 1>(mX, mW, static_cast<int>(T), static_cast<int>(N), static_cast<int>(H), e,
                                            st);
 }

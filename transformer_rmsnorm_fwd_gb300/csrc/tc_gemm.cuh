@@ -9,13 +9,19 @@
 // parameter and becomes the operand-major bits of the MMA instruction
 // descriptor and the LBO / SBO of the shared-memory descriptors.
 //
-// Block = 6 warps, one block per SM (the 4-stage ring takes ~193 KB of
-// shared memory):
-//   warp 0      TMA producer (one lane): A/B tiles into a 4-stage ring;
-//   warp 1      TMEM owner and MMA issuer (one lane): 4 x tcgen05.mma
-//               (M=128, N=256, K=16) per 64-wide k-block, tcgen05.commit
-//               frees the ring slot, a second commit hands the accumulator
-//               to the epilogue;
+// Block = 6 warps, one block per SM.  Two modes:
+//  * single CTA (PAIR = 0): 128 x 256 tiles, a 4-stage ring of 48 KB stages;
+//  * CTA pair (PAIR = 1, the one the library launches): clusters of two
+//    CTAs on neighbouring SMs share tcgen05.mma.cta_group::2 (M=256, N=256):
+//    each CTA loads 128 rows of A and 128 rows of B (32 KB per k-block
+//    instead of 48 KB, so L2->SM traffic per flop drops by a third) into a
+//    6-stage ring, both CTAs' copies complete on the leader's barrier, the
+//    leader issues the MMAs for both, and its commits are multicast to the
+//    pair's barriers; each CTA's TMEM holds its 128 x 256 half.
+//   warp 0      TMA producer (one lane);
+//   warp 1      TMEM owner and (leader) MMA issuer (one lane): 4 x tcgen05.mma
+//               (K=16) per 64-wide k-block, tcgen05.commit frees the ring
+//               slot, a second commit hands the accumulator to the epilogue;
 //   warps 2..5  epilogue: each thread owns one accumulator row (TMEM lane),
 //               reads it with tcgen05.ld 32 columns at a time and applies the
 //               fused epilogue; the accumulator is double-buffered in TMEM
@@ -48,6 +54,21 @@ constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int B_BOX_ROWS = BN / 2;   // K-major B maps: boxes of 128 rows (two per 256-row stage)
+
+// Tile geometry of one CTA (PAIR = 0) or of a CTA pair sharing one
+// cta_group::2 MMA (PAIR = 1): the pair computes a 256 x 256 tile, each CTA
+// loading 128 rows of A and 128 rows of B and holding its 128 x 256 half of
+// the accumulator, so each SM moves 32 KB instead of 48 KB per k-block.
+template <int PAIR>
+struct TileCfg {
+    static constexpr int TM = PAIR ? 2 * BM : BM;        // tile rows
+    static constexpr int BNL = PAIR ? BN / 2 : BN;       // B rows held by this CTA
+    static constexpr int B_L = BNL * BK * 2;
+    static constexpr int STAGE_L = A_BYTES + B_L;
+    static constexpr int ST = PAIR ? 6 : STAGES;         // ring depth
+    static constexpr int SMEM = 1024 + ST * STAGE_L + 256;
+};
 
 enum Epi : int {
     EPI_LOGITS = 0,
@@ -199,6 +220,51 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
+// ---- CTA-pair (cta_group::2) forms
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// address of the same shared-memory object in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t o;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(o) : "r"(addr), "r"(rank));
+    return o;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// TMA load into this CTA's shared memory completing on an mbarrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void mma_bf16_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                              uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+// arrive once on the mbarrier at this offset in both CTAs of the pair when the MMAs issued so far complete
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+    const uint16_t mask = 3;
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(mask)
+        : "memory");
+}
 // 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
@@ -236,36 +302,42 @@ __device__ __forceinline__ void sub_scaled32(float (&v)[32], const __nv_bfloat16
 // one-time attribute set in one unit never stands in for another's.
 namespace {
 
-template <int A_MN, int B_MN, int EPI>
+template <int A_MN, int B_MN, int EPI, int PAIR = 0>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, int M, int N,
                    int K, EpiParams ep) {
+    using Cfg = TileCfg<PAIR>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    const uint32_t bar0 = base + Cfg::ST * Cfg::STAGE_L;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-    const uint32_t slot = bar0 + 8u * (2 * STAGES + 4);
-    uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(gbase + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 4));
+    auto empty_bar = [&](int s) { return bar0 + 8u * (Cfg::ST + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * Cfg::ST + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * Cfg::ST + 2 + a); };
+    const uint32_t slot = bar0 + 8u * (2 * Cfg::ST + 4);
+    uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(gbase + Cfg::ST * Cfg::STAGE_L + 8 * (2 * Cfg::ST + 4));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_m = (M + BM - 1) / BM, num_n = (N + BN - 1) / BN;
+    // a CTA pair is a cluster of two consecutive blocks; rank 0 issues the MMAs
+    const uint32_t crank = PAIR ? cluster_rank() : 0u;
+    const bool leader = crank == 0;
+    const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int nunits = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    const int num_m = (M + Cfg::TM - 1) / Cfg::TM, num_n = (N + BN - 1) / BN;
     const int ntiles = num_m * num_n;
     const int nkb = (K + BK - 1) / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < Cfg::ST; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), PAIR ? 8 : 4);   // the epilogue warps of both CTAs
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tmA);
@@ -276,13 +348,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                         "r"(TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();   // both CTAs' barriers initialised before any cross-CTA arrive
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(slot_ptr);
 
@@ -316,11 +396,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t pol_a = make_policy(ep.hint_a), pol_b = make_policy(ep.hint_b);
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_phase[STAGES];
-            bool issued[STAGES];
-            for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+            uint32_t issued_phase[Cfg::ST];
+            bool issued[Cfg::ST];
+            for (int s = 0; s < Cfg::ST; ++s) issued[s] = false, issued_phase[s] = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+            const int a_row0 = static_cast<int>(crank) * BM;   // this CTA's rows within the tile
+            for (int t = unit; t < ntiles && ok; t += nunits) {
                 int mi, ni;
                 tile_mn(t, mi, ni);
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -329,35 +410,48 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    const uint32_t sa = base + stage * Cfg::STAGE_L;
                     const uint32_t sb = sa + A_BYTES;
-                    const uint32_t fb = full_bar(stage);
-                    mbar_expect_tx(fb, STAGE_BYTES);
+                    // the pair's loads all complete on the leader's full barrier
+                    const uint32_t fb = PAIR && !leader ? map_to_rank(full_bar(stage), 0) : full_bar(stage);
+                    if (leader) mbar_expect_tx(full_bar(stage), (PAIR ? 2 : 1) * Cfg::STAGE_L);
+                    auto load = [&](uint32_t dst, const CUtensorMap* m, int x, int y, uint64_t pol) {
+                        if (PAIR) tma_load_2d_pair(dst, m, fb, x, y, pol);
+                        else tma_load_2d_hint(dst, m, fb, x, y, pol);
+                    };
                     const bool second = ep.ksplit_nkb > 0 && kb >= ep.ksplit_nkb;
                     const CUtensorMap* mA = second ? &tmA2 : &tmA;
                     const CUtensorMap* mB = second ? &tmB2 : &tmB;
                     const int kc = (second ? kb - ep.ksplit_nkb : kb) * BK;
+                    const int arow = mi * Cfg::TM + a_row0;
                     if (A_MN) {
 #pragma unroll
-                        for (int j = 0; j < BM / MN_BOX; ++j)
-                            tma_load_2d_hint(sa + j * MN_BOX_BYTES, mA, fb, mi * BM + j * MN_BOX, kc, pol_a);
+                        for (int j = 0; j < BM / MN_BOX; ++j) load(sa + j * MN_BOX_BYTES, mA, arow + j * MN_BOX, kc, pol_a);
                     } else {
-                        tma_load_2d_hint(sa, mA, fb, kc, mi * BM, pol_a);
+                        load(sa, mA, kc, arow, pol_a);
                     }
                     if (ep.bsplit) {
-                        // K-major B maps with 128-row boxes: gate rows, then up rows
-                        tma_load_2d_hint(sb, &tmB, fb, kc, ni * (BN / 2), pol_b);
-                        tma_load_2d_hint(sb + B_BYTES / 2, &tmB2, fb, kc, ni * (BN / 2), pol_b);
+                        // K-major B maps with 128-row boxes: gate rows, then up rows (one each per CTA of a pair)
+                        if (PAIR) {
+                            load(sb, leader ? &tmB : &tmB2, kc, ni * (BN / 2), pol_b);
+                        } else {
+                            load(sb, &tmB, kc, ni * (BN / 2), pol_b);
+                            load(sb + B_BYTES / 2, &tmB2, kc, ni * (BN / 2), pol_b);
+                        }
                     } else if (B_MN) {
+                        const int bcol = ni * BN + static_cast<int>(crank) * Cfg::BNL;
 #pragma unroll
-                        for (int j = 0; j < BN / MN_BOX; ++j)
-                            tma_load_2d_hint(sb + j * MN_BOX_BYTES, mB, fb, ni * BN + j * MN_BOX, kc, pol_b);
+                        for (int j = 0; j < Cfg::BNL / MN_BOX; ++j)
+                            load(sb + j * MN_BOX_BYTES, mB, bcol + j * MN_BOX, kc, pol_b);
                     } else {
-                        tma_load_2d_hint(sb, mB, fb, kc, ni * BN, pol_b);
+                        const int brow = ni * BN + static_cast<int>(crank) * Cfg::BNL;
+#pragma unroll
+                        for (int j = 0; j < Cfg::BNL / B_BOX_ROWS; ++j)
+                            load(sb + j * (B_BOX_ROWS * BK * 2), mB, kc, brow + j * B_BOX_ROWS, pol_b);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
-                    if (++stage == STAGES) {
+                    if (++stage == Cfg::ST) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -365,14 +459,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) {
                 // let every copy already issued land before the block exits
-                for (int s = 0; s < STAGES; ++s)
-                    if (issued[s]) mbar_wait(full_bar(s), issued_phase[s]);
+                if (leader) {
+                    for (int s = 0; s < Cfg::ST; ++s)
+                        if (issued[s]) mbar_wait(full_bar(s), issued_phase[s]);
+                } else {
+                    // the peer's copies complete on the leader's barriers: give them time to land
+                    const uint64_t t0 = globaltimer();
+                    while (globaltimer() - t0 < 20000000ull) {
+                    }
+                }
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(BM, BN, A_MN, B_MN);
+        // ------------------------------------------------ MMA issuer (the leader of a pair)
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = make_idesc(Cfg::TM, BN, A_MN, B_MN);
             // K-major SW128: rows of 128 B, 8-row groups 1024 B apart (SBO), K step 32 B.
             // MN-major SW128: 64-element MN atoms 8 KB apart (LBO), 8-row K groups 1024 B
             // apart (SBO), K step 16 rows = 2048 B.
@@ -384,7 +485,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             int it = 0;
             bool ok = true;
             bool any = false;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++it) {
+            auto commit = [&](uint32_t bar) {
+                if (PAIR) mma_commit_pair(bar);
+                else mma_commit(bar);
+            };
+            for (int t = unit; t < ntiles && ok; t += nunits, ++it) {
                 const int as = it & 1;
                 const uint32_t aphase = (it >> 1) & 1;
                 if (!mbar_wait(tempty_bar(as), aphase ^ 1u)) {
@@ -401,27 +506,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = base + stage * STAGE_BYTES;
+                    const uint32_t sa = base + stage * Cfg::STAGE_L;
                     const uint32_t sb = sa + A_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         const uint64_t da = smem_desc(sa + k * a_kstep, a_lbo, 1024u);
                         const uint64_t db = smem_desc(sb + k * b_kstep, b_lbo, 1024u);
-                        mma_bf16(d, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+                        if (PAIR) mma_bf16_pair(d, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+                        else mma_bf16(d, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     any = true;
-                    mma_commit(empty_bar(stage));
-                    if (++stage == STAGES) {
+                    commit(empty_bar(stage));
+                    if (++stage == Cfg::ST) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(tfull_bar(as));
+                commit(tfull_bar(as));
             }
             if (!ok && any) {
                 // wait for the MMAs already issued: commit to a free barrier and wait on it
-                mma_commit(tfull_bar(it & 1));
+                commit(tfull_bar(it & 1));
                 mbar_wait(tfull_bar(it & 1), ((it >> 1) & 1));
             }
         }
@@ -429,13 +535,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int rl = q * 32 + lane;           // accumulator row of this thread
+        // hand the accumulator buffer back to the MMA issuer (the leader's barrier)
+        auto release_acc = [&](int a) {
+            if (PAIR && !leader) mbar_arrive_cluster(map_to_rank(tempty_bar(a), 0));
+            else mbar_arrive(tempty_bar(a));
+        };
         int it = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        for (int t = unit; t < ntiles; t += nunits, ++it) {
             int mi, ni;
             tile_mn(t, mi, ni);
             const int as = it & 1;
             const uint32_t aphase = (it >> 1) & 1;
-            const int row = mi * BM + rl;
+            const int row = mi * Cfg::TM + static_cast<int>(crank) * BM + rl;
             const int n0 = ni * BN;
             const bool row_ok = row < ep.M;
             // EPI_ACCUM: everything that does not depend on the accumulator is fetched
@@ -509,7 +620,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(as));
+                if (lane == 0) release_acc(as);
                 if (live) {
                     ep.part[static_cast<int64_t>(row) * ep.nvt + ni] = make_float2(m, sum);
                     if (has_lab) ep.zlab[row] = zl;
@@ -546,7 +657,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(as));
+                if (lane == 0) release_acc(as);
             } else if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
                 const int o0 = ni * (BN / 2);   // first output (intermediate) column of the tile
 #pragma unroll 1
@@ -595,7 +706,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(as));
+                if (lane == 0) release_acc(as);
             } else if (EPI == EPI_SOFTMAX) {
                 const int64_t y = row_ok ? ep.labels[row] : ep.ignore_index;
                 const bool live = row_ok && y != ep.ignore_index;
@@ -622,7 +733,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(as));
+                if (lane == 0) release_acc(as);
             } else if (EPI == EPI_QKV_ROPE) {
                 const float rsv = row_ok ? ep.rs[row] : 0.f;
                 int64_t tr = 0;
@@ -709,7 +820,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(as));
+                if (lane == 0) release_acc(as);
             } else {
                 __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
                 const int64_t ylab = (row_ok && ep.labels != nullptr) ? ep.labels[row] : ep.ignore_index;
@@ -788,17 +899,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(as));
+                if (lane == 0) release_acc(as);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();   // neither CTA exits while the pair's MMAs or copies may touch it
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
-                     : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS)
+                         : "memory");
     }
 }
 
@@ -818,25 +934,65 @@ int make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, i
              int box_outer);
 
 // Launch C = A(M x K) * B(N x K) with the given epilogue.  A_MN / B_MN say
-// whether each operand is MN-major.  grid_limit = 0: one block per SM.
+// whether each operand is MN-major.  K-major B maps have 128-row boxes
+// (B_BOX_ROWS).  PAIR = 1: clusters of two CTAs share cta_group::2 MMAs on
+// 256 x 256 tiles.  grid_limit = 0: one block per SM (pairs: as many as fit).
 namespace {
 
-template <int A_MN, int B_MN, int EPI>
+template <int A_MN, int B_MN, int EPI, int PAIR = 0>
 int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K, const EpiParams& ep,
                 cudaStream_t st, int grid_limit = 0, const CUtensorMap* ma2 = nullptr,
                 const CUtensorMap* mb2 = nullptr) {
-    auto kern = tc_gemm_kernel<A_MN, B_MN, EPI>;
+    using Cfg = TileCfg<PAIR>;
+    auto kern = tc_gemm_kernel<A_MN, B_MN, EPI, PAIR>;
     static bool attr_set = false;   // per instantiation; the attribute is per function
+    static int max_units = 0;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
             return check_launch("tc_gemm attribute");
+        if (PAIR) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (sm_count() / 2));
+            cfg.blockDim = dim3(THREADS);
+            cfg.dynamicSmemBytes = Cfg::SMEM;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0)
+                return check_launch("tc_gemm cluster occupancy");
+            max_units = n;
+        } else {
+            max_units = sm_count();
+        }
         attr_set = true;
     }
-    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    int grid = sm_count();
-    if (grid_limit > 0) grid = std::min(grid, grid_limit);
-    grid = std::max(1, std::min(grid, tiles));
-    kern<<<grid, THREADS, SMEM_BYTES, st>>>(ma, mb, ma2 ? *ma2 : ma, mb2 ? *mb2 : mb, M, N, K, ep);
+    const int tiles = ((M + Cfg::TM - 1) / Cfg::TM) * ((N + BN - 1) / BN);
+    int units = max_units;
+    if (grid_limit > 0) units = std::min(units, PAIR ? std::max(1, grid_limit / 2) : grid_limit);
+    units = std::max(1, std::min(units, tiles));
+    if (PAIR) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * units);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = Cfg::SMEM;
+        cfg.stream = st;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, ma, mb, ma2 ? *ma2 : ma, mb2 ? *mb2 : mb, M, N, K, ep) != cudaSuccess)
+            return check_launch("tc_gemm pair launch");
+        return check_launch("tc_gemm");
+    }
+    kern<<<units, THREADS, Cfg::SMEM, st>>>(ma, mb, ma2 ? *ma2 : ma, mb2 ? *mb2 : mb, M, N, K, ep);
     return check_launch("tc_gemm");
 }
 
