@@ -550,6 +550,15 @@ def native_arm(args):
 
         for ev in consumed:
             ev.record(compute)
+        # the copy alone: one step's inputs host -> device on the copy stream
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(copy_stream):
+            c0.record(copy_stream)
+            for k, t in host.items():
+                sets[1][k].copy_(t, non_blocking=True)
+            c1.record(copy_stream)
+        torch.cuda.synchronize()
+        h2d_ms = c0.elapsed_time(c1)
         run(max(1, W), K)
         if dist:
             dist.barrier()
@@ -563,7 +572,8 @@ def native_arm(args):
         e2e = {"value": tokens / (ms_e / 1000.0), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": 4, "ms_per_step": ms_e / K,
                "pipelining": "inputs of step i+1 copied on a second stream during step i (double-buffered)",
-               "resident": "parameters " + ", ".join(sorted(PARAMETERS)) + " stay on the device"}
+               "resident": "parameters " + ", ".join(sorted(PARAMETERS)) + " stay on the device",
+               "h2d_alone_ms": round(h2d_ms, 3), "h2d_alone_gbs": round(h2d / (h2d_ms / 1000.0) / 1e9, 1)}
         chain.inp = sets[0]
         del host, sets
 

@@ -69,6 +69,16 @@ __device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bf
 // 16-byte loads / stores.  ldg_nc: read-only path, only for buffers no
 // thread of the same kernel writes.
 __device__ __forceinline__ uint4 ldg16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+// 16-byte load asking L2 to fetch the whole 256-byte block around it from DRAM
+// (for a thread whose next load falls in the same 256 bytes)
+__device__ __forceinline__ uint4 ldg16_pf256(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p)
+                 : "memory");
+    return r;
+}
 __device__ __forceinline__ uint4 ldg16_nc(const void* p) {
     uint4 r;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -397,6 +397,131 @@ int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
     return check_launch("rmsnorm_fwd_generic");
 }
 
+constexpr int kBwdStagedMaxThreads = 256;
+
+// Staged backward: the same arithmetic as rmsnorm_bwd_block, with the rows
+// of dy and x brought into a ring of nst shared-memory buffers by 1-D bulk
+// copies (nst rows in flight per block whatever the SM clock).  Each thread
+// copies its column vectors of the row into registers before the row's
+// reduction barrier, so after that barrier thread 0 refills the buffer at once.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kBwdStagedMaxThreads) rmsnorm_bwd_staged(const T* dy, const T* __restrict__ x,
+                                                          const T* __restrict__ w, const float* __restrict__ rstd,
+                                                          T* dx, float* __restrict__ part, int64_t rows, int cols,
+                                                          int64_t rows_per_block, int nst) {
+    constexpr int EPV = Vec<T>::N;
+    extern __shared__ __align__(128) uint8_t sm[];
+    __shared__ float red[2][32];
+    const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, wid = tid >> 5, NW = NT >> 5;
+    const int nvec = cols / EPV;
+    const uint32_t rb = static_cast<uint32_t>(cols) * sizeof(T);   // row bytes (multiple of 16)
+    const uint32_t bars = smem_u32(sm + static_cast<size_t>(nst) * 2 * rb);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per_block;
+    const int64_t r1 = min(rows, r0 + rows_per_block);
+    if (tid == 0)
+        for (int s = 0; s < nst; ++s) mbar_init(bars + 8u * s, 1);
+    mbar_init_fence();
+    __syncthreads();
+    auto issue = [&](int64_t i) {   // row r0 + i into buffer i % nst: dy, then x
+        const int64_t r = r0 + i;
+        if (r >= r1) return;
+        const uint32_t bar = bars + 8u * static_cast<uint32_t>(i % nst);
+        uint8_t* dst = sm + static_cast<size_t>(i % nst) * 2 * rb;
+        mbar_expect_tx(bar, 2 * rb);
+        bulk_g2s(smem_u32(dst), dy + r * cols, rb, bar);
+        bulk_g2s(smem_u32(dst + rb), x + r * cols, rb, bar);
+    };
+    if (tid == 0)
+        for (int s = 0; s < nst; ++s) issue(s);
+    uint4 wv[VPT];
+    float dwa[VPT][EPV];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = j * NT + tid;
+        wv[j] = v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) dwa[j][e] = 0.f;
+    }
+    const float inv_cols = 1.0f / static_cast<float>(cols);
+    bool ok = true;
+    int64_t i = 0;
+    for (; r0 + i < r1; ++i) {
+        const int64_t r = r0 + i;
+        const int s = static_cast<int>(i % nst);
+        const bool got = mbar_wait(bars + 8u * s, static_cast<uint32_t>(i / nst) & 1u);
+        const float rs = rstd[r];
+        const uint8_t* bdy = sm + static_cast<size_t>(s) * 2 * rb;
+        const uint8_t* bx = bdy + rb;
+        uint4 cx[VPT], cdy[VPT];
+        float gx = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = j * NT + tid;
+            cx[j] = v < nvec && got ? *reinterpret_cast<const uint4*>(bx + static_cast<size_t>(v) * 16) : make_uint4(0, 0, 0, 0);
+            cdy[j] = v < nvec && got ? *reinterpret_cast<const uint4*>(bdy + static_cast<size_t>(v) * 16) : make_uint4(0, 0, 0, 0);
+            float fx[EPV], fd[EPV], fw[EPV];
+            unpack(cx[j], fx);
+            unpack(cdy[j], fd);
+            unpack(wv[j], fw);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) gx = fmaf(fd[e] * fw[e], fx[e], gx);
+        }
+        gx = warp_sum(gx);
+        if (lane == 0) red[i & 1][wid] = gx;
+        // the row's partial sums are published; every thread has its vectors of buffer s in registers
+        if (!__syncthreads_and(got ? 1 : 0)) {
+            ok = false;
+            break;
+        }
+        if (tid == 0) {
+            fence_proxy_async_smem();   // the reads of buffer s happen before the copy overwrites it
+            issue(i + nst);
+        }
+        float tot = 0.f;
+        for (int q = 0; q < NW; ++q) tot += red[i & 1][q];
+        const float c = rs * rs * rs * inv_cols * tot;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = j * NT + tid;
+            if (v < nvec) {
+                float fx[EPV], fd[EPV], fw[EPV], o[EPV];
+                unpack(cx[j], fx);
+                unpack(cdy[j], fd);
+                unpack(wv[j], fw);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    o[e] = rs * (fd[e] * fw[e]) - c * fx[e];
+                    dwa[j][e] = fmaf(fd[e] * fx[e], rs, dwa[j][e]);
+                }
+                stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, pack(o));
+            }
+        }
+    }
+    if (!ok) {
+        if (tid == 0) {
+            atomicExch(&g_stage_err, 1);
+            // copies in flight: rows i .. i+nst-1 (the refill after the failed barrier never happened)
+            for (int64_t ii = i; ii < i + nst; ++ii)
+                if (r0 + ii < r1) mbar_wait(bars + 8u * static_cast<uint32_t>(ii % nst), static_cast<uint32_t>(ii / nst) & 1u);
+        }
+        return;
+    }
+    float* pr = part + static_cast<int64_t>(blockIdx.x) * cols;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = j * NT + tid;
+        if (v < nvec) {
+#pragma unroll
+            for (int e = 0; e < EPV; e += 4) {
+                float q[4] = {dwa[j][e], dwa[j][e + 1], dwa[j][e + 2], dwa[j][e + 3]};
+                stg16(pr + static_cast<int64_t>(v) * EPV + e, pack(q));
+            }
+        }
+    }
+}
+
+inline size_t bwd_staged_smem(int rb, int nst) { return static_cast<size_t>(nst) * 2 * rb + 8u * nst; }
+
 int64_t bwd_partials(int64_t rows) {
     return std::max<int64_t>(1, std::min<int64_t>({rows, static_cast<int64_t>(sm_count()) * 2, kMaxPartials}));
 }
@@ -414,6 +539,36 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
     const T* wp = static_cast<const T*>(w);
     T* dxp = static_cast<T*>(dx);
     bool done = false;
+    const int rbytes = cols * static_cast<int>(sizeof(T));
+    if (cols % EPV == 0 && cols / EPV <= 2 * kBwdStagedMaxThreads && bwd_staged_smem(rbytes, 2) <= 100u * 1024u) {
+        // staged path: up to 4 rows in flight per block, about 3 blocks per SM at 8 KB rows
+        const int nvec = cols / EPV;
+        int nst = 4;
+        while (nst > 2 && bwd_staged_smem(rbytes, nst) > 72u * 1024u) --nst;
+        const size_t ssm = bwd_staged_smem(rbytes, nst);
+        auto go = [&](auto kern, int vpt) -> int {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm)) !=
+                cudaSuccess)
+                return check_launch("rmsnorm_bwd_staged attribute");
+            const int nt = static_cast<int>(std::min<int64_t>(kBwdStagedMaxThreads, ceil_div(ceil_div(nvec, vpt), 32) * 32));
+            int per_sm = 0;
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nt, ssm);
+            if (per_sm < 1) per_sm = 1;
+            const int64_t P2 = std::max<int64_t>(1, std::min<int64_t>({rows, static_cast<int64_t>(sm_count()) * per_sm,
+                                                                       kMaxPartials}));
+            const int64_t rpb2 = ceil_div(rows, P2);
+            grid_used = ceil_div(rows, rpb2);
+            kern<<<static_cast<unsigned>(grid_used), nt, ssm, st>>>(dyp, xp, wp, rstd, dxp, part, rows, cols, rpb2,
+                                                                    nst);
+            done = true;
+            return check_launch("rmsnorm_bwd_staged");
+        };
+        int rc0 = LIGER_OK;
+        // one column vector per thread up to kBwdStagedMaxThreads vectors (more warps per SM)
+        if (nvec <= kBwdStagedMaxThreads) rc0 = go(rmsnorm_bwd_staged<T, 1>, 1);
+        else rc0 = go(rmsnorm_bwd_staged<T, 2>, 2);
+        if (rc0) return rc0;
+    }
     if (!done && cols % EPV == 0) {
         const int nvec = cols / EPV;
         auto go = [&](auto kern, int vpt) {

@@ -18,7 +18,8 @@
 // HBM: per call the data path is
 //   1. qkv_fold   (optional): W' and the fp32 bias row           HBM-bound
 //   2. qkv_prep:  r_t per token (one read of x) and, without caller tables,
-//                 the token's cos/sin row (angle in fp64, reduced mod 2 pi)
+//                 the token's cos/sin row (angle reduced mod 2 pi in fp32 with
+//                 an exact product and a two-constant 2 pi)
 //   3. tc_gemm_kernel<EPI_QKV_ROPE>: x W'^T on tcgen05, epilogue scales by r_t,
 //                 adds the bias, rotates q and k heads in registers, writes
 //                 q, k, v in their [B, S, heads, D] layouts.
@@ -31,7 +32,9 @@ namespace {
 constexpr int kMaxHalfQkv = 128;   // head_dim <= 256
 
 struct InvFreqQkv {
-    double v[kMaxHalfQkv];
+    double v[kMaxHalfQkv];   // theta^(-2i/D)
+    float hi[kMaxHalfQkv];   // fl(v)
+    float lo[kMaxHalfQkv];   // fl(v - hi)
 };
 
 static __device__ int g_qkv_err;
@@ -119,9 +122,9 @@ __global__ void __launch_bounds__(256) qkv_prep(const __nv_bfloat16* __restrict_
     ss = warp_sum(ss);
     if (lane == 0) rstd[t] = rsqrtf(ss / static_cast<float>(H) + eps);
     if (make_tab) {
-        const double p = pos ? static_cast<double>(pos[t]) : static_cast<double>(t % S);
+        const int64_t p = pos ? static_cast<int64_t>(pos[t]) : t % S;
         for (int i = lane; i < half; i += 32) {
-            const float2 cs = angle_cs(p, f.v[i], 1.0f);
+            const float2 cs = angle_cs32(p, f.hi[i], f.lo[i], f.v[i], 1.0f);
             cos_t[t * half + i] = cs.x;
             sin_t[t * half + i] = cs.y;
         }
@@ -200,8 +203,11 @@ extern "C" int liger_rmsnorm_qkv_rope_fwd(const void* x, const void* w_norm, con
     }
     // 2. rstd per token and, without caller tables, the token's cos/sin row
     InvFreqQkv f;
-    for (int i = 0; i < half; ++i)
+    for (int i = 0; i < half; ++i) {
         f.v[i] = cos_tab ? 0.0 : pow(theta, -2.0 * static_cast<double>(i) / static_cast<double>(D));
+        f.hi[i] = static_cast<float>(f.v[i]);
+        f.lo[i] = static_cast<float>(f.v[i] - static_cast<double>(f.hi[i]));
+    }
     qkv_prep<<<static_cast<unsigned>(ceil_div(T, 8)), 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), T, H, static_cast<float>(eps), rs, pos, S, half, cos_tab ? 0 : 1,
         cos_t, sin_t, f);

@@ -119,8 +119,9 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(const RopeArgs a, const 
                     } else {
                         T* pb = pa + half;
                         float av[EPV], bv[EPV];
-                        unpack(ldg16(pa), av);
-                        unpack(ldg16(pb), bv);
+                        // the two halves of a head sit in one 256-byte block: ask L2 for all of it
+                        unpack(ldg16_pf256(pa), av);
+                        unpack(ldg16_pf256(pb), bv);
 #pragma unroll
                         for (int e = 0; e < EPV; e += 2) {
                             const float4 r = c4[e >> 1];
