@@ -215,8 +215,11 @@ class Chain:
 
 
 def isolated_times(chain, dev, n=10):
-    """Each memory-bound operator of the chain timed alone (median of n launches,
-    L2 flushed by writing 512 MB before each): ms per call."""
+    """Each memory-bound operator of the chain timed alone (median of n launches):
+    ms per call.  Before each launch L2 is flushed by writing a 512 MB buffer and
+    then reading it back, so that none of the operator's inputs is resident and
+    no other buffer's dirty lines are left for the operator to write back (the
+    state ncu's cache control leaves before a capture)."""
     import torch
     L, i = chain.L, chain.inp
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -235,6 +238,7 @@ def isolated_times(chain, dev, n=10):
         ts = []
         for _ in range(n):
             flush.zero_()
+            flush.view(torch.int32).amax()   # read back: L2 left holding clean lines of the flush buffer
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             fn()

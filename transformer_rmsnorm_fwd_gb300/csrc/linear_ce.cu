@@ -407,7 +407,10 @@ int run_simt(const Args& a, const Layout& L, float scale) {
 }
 
 int ensure_sort_attr() {
-    static bool sort_attr = false;
+    static bool done[64] = {false};   // per device: function attributes belong to each device's context
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return check_launch("sort_label_keys device");
+    bool& sort_attr = done[dev];
     if (!sort_attr) {
         if (cudaFuncSetAttribute(sort_label_keys, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(sizeof(unsigned long long) * kMaxSortKeys)) != cudaSuccess)

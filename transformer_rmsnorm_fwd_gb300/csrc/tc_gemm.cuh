@@ -945,8 +945,14 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int 
                 const CUtensorMap* mb2 = nullptr) {
     using Cfg = TileCfg<PAIR>;
     auto kern = tc_gemm_kernel<A_MN, B_MN, EPI, PAIR>;
-    static bool attr_set = false;   // per instantiation; the attribute is per function
-    static int max_units = 0;
+    // per instantiation and device: function attributes belong to each device's context
+    constexpr int kDevs = 64;
+    static bool attr_done[kDevs] = {false};
+    static int units_of[kDevs] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return check_launch("tc_gemm device");
+    bool& attr_set = attr_done[dev];
+    int& max_units = units_of[dev];
     if (!attr_set) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
             return check_launch("tc_gemm attribute");
