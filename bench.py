@@ -185,8 +185,9 @@ class Chain:
     def launches_per_step(self):
         chunk = min(self.S, 8192, max(128, (self.S + 1) // 2))
         nchunks = -(-self.S // chunk)
-        # per chunk: logits GEMM, dlogits, dX GEMM, label sort, label starts, dW GEMM
-        return 1 + 1 + 1 + (1 + 6 * nchunks + 1) + 1 + 1 + 2
+        # linear CE: label scan, label sort and start tables (once), per chunk the logits GEMM,
+        # dlogits, dX GEMM and dW GEMM, loss reduction
+        return 1 + 1 + 1 + (1 + 2 + 4 * nchunks + 1) + 1 + 1 + 2
 
     def step(self, ev=None):
         """One pass of every operator; ev: dict name -> list of (start, end) events."""

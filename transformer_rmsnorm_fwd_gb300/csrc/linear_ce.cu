@@ -75,8 +75,9 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     L.lossrow = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
     L.zlab = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
     L.hdr = o; o = up256(o + sizeof(Hdr));
-    L.keys = o; o = up256(o + (L.tc ? sizeof(unsigned long long) * static_cast<size_t>(C) : 0));
-    L.lstart = o; o = up256(o + (L.tc ? sizeof(int) * static_cast<size_t>(V + 1) : 0));
+    // every chunk's sorted label keys and start table, made in one pass before the chunks
+    L.keys = o; o = up256(o + (L.tc ? sizeof(unsigned long long) * static_cast<size_t>(std::max<int64_t>(T, 1)) : 0));
+    L.lstart = o; o = up256(o + (L.tc ? sizeof(int) * static_cast<size_t>(L.nchunks * (V + 1)) : 0));
     L.part = o; o = up256(o + (L.tc ? sizeof(float2) * static_cast<size_t>(C * L.nvt) : 0));
     L.scr = o; o = up256(o + static_cast<size_t>(C) * static_cast<size_t>(L.ldp) * (L.tc ? 2 : 4));
     const bool need_acc = L.nchunks > 1 && dtype == LIGER_BF16;
@@ -119,19 +120,26 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* sh) {
     return r;
 }
 
-// Sort the chunk's (label << 32 | t_base + row) keys (ignored rows -> ~0) in one
-// block (bitonic, in shared memory), for the one-hot correction of the dW
-// epilogue.
+// Sort the (label << 32 | token) keys of each segment of seg tokens (ignored
+// tokens -> ~0), one block per segment (bitonic, in shared memory), for the
+// one-hot correction of the dW epilogue.  Segment b covers tokens
+// [b*seg, min(n, (b+1)*seg)) and its sorted keys go to out[b*seg ...]; the
+// token index in a key is absolute (b*seg + i) or relative to the segment (i).
 constexpr int kMaxSortKeys = 8192;
-__global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restrict__ labels, int n, int64_t ignore,
-                                                        int npow2, unsigned t_base,
+__global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restrict__ labels, int64_t n, int seg,
+                                                        int64_t ignore, int absolute,
                                                         unsigned long long* __restrict__ out) {
     extern __shared__ unsigned long long sk[];
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * seg;
+    const int cnt = static_cast<int>(n - b0 < seg ? n - b0 : seg);
+    int npow2 = 1;
+    while (npow2 < cnt) npow2 <<= 1;
+    const unsigned base = absolute ? static_cast<unsigned>(b0) : 0u;
     for (int i = threadIdx.x; i < npow2; i += 1024) {
         unsigned long long key = ~0ull;
-        if (i < n) {
-            const int64_t y = labels[i];
-            if (y != ignore) key = (static_cast<unsigned long long>(y) << 32) | (t_base + static_cast<unsigned>(i));
+        if (i < cnt) {
+            const int64_t y = labels[b0 + i];
+            if (y != ignore) key = (static_cast<unsigned long long>(y) << 32) | (base + static_cast<unsigned>(i));
         }
         sk[i] = key;
     }
@@ -152,24 +160,46 @@ __global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restric
             __syncthreads();
         }
     }
-    for (int i = threadIdx.x; i < n; i += 1024) out[i] = sk[i];
+    for (int i = threadIdx.x; i < cnt; i += 1024) out[b0 + i] = sk[i];
 }
 
-// lstart[v] = base + first index of label v in the sorted chunk keys, v in
-// [0, V] (so the tokens labelled v are keys[lstart[v] .. lstart[v+1]) of the
-// array the chunk's keys start at index base of).
-__global__ void label_starts(const unsigned long long* __restrict__ keys, int n, int V, int base,
+// Start tables of every segment (blockIdx.y): lstart[s*(V+1) + v] = first index
+// of label v among segment s's sorted keys, v in [0, V], plus s*seg when the
+// indices are absolute -- so the tokens of segment s labelled v are
+// keys[lstart[v] .. lstart[v+1]) of the array the table's indices refer to.
+__global__ void label_starts(const unsigned long long* __restrict__ keys, int64_t n, int seg, int V, int absolute,
                              int* __restrict__ lstart) {
+    const int64_t b0 = static_cast<int64_t>(blockIdx.y) * seg;
+    const int cnt = static_cast<int>(n - b0 < seg ? n - b0 : seg);
+    const unsigned long long* k = keys + b0;
+    int* ls = lstart + static_cast<int64_t>(blockIdx.y) * (V + 1);
+    const int base = absolute ? static_cast<int>(b0) : 0;
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v <= V; v += gridDim.x * blockDim.x) {
         const unsigned long long key = static_cast<unsigned long long>(v) << 32;
-        int lo = 0, hi = n;
+        int lo = 0, hi = cnt;
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
-            if (keys[mid] < key) lo = mid + 1;
+            if (k[mid] < key) lo = mid + 1;
             else hi = mid;
         }
-        lstart[v] = base + lo;
+        ls[v] = base + lo;
     }
+}
+
+// Sorted keys and start tables of all nseg segments of seg tokens, in two launches.
+int sort_labels(const int64_t* labels, int64_t n, int seg, int64_t ignore, int V, bool absolute,
+                unsigned long long* keys, int* lstart, cudaStream_t st) {
+    const int64_t nseg = ceil_div(n, static_cast<int64_t>(seg));
+    if (nseg <= 0) return LIGER_OK;
+    int npow2 = 1;
+    while (npow2 < seg) npow2 <<= 1;
+    sort_label_keys<<<static_cast<unsigned>(nseg), 1024, sizeof(unsigned long long) * npow2, st>>>(
+        labels, n, seg, ignore, absolute ? 1 : 0, keys);
+    if (int rc = check_launch("sort_label_keys")) return rc;
+    const dim3 grid(static_cast<unsigned>(std::min<int64_t>(ceil_div(V + 1, 256), 2 * sm_count())),
+                    static_cast<unsigned>(nseg));
+    label_starts<<<grid, 256, 0, st>>>(keys, n, seg, V, absolute ? 1 : 0, lstart);
+    return check_launch("label_starts");
 }
 
 // Merge the per-tile (m, s) of one chunk row into lse and rewrite P in place
@@ -440,6 +470,8 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     if ((rc = make_map(&mW_k, W, H, V, H, BK, B_BOX_ROWS))) return rc;          // B of Z = X W^T  (K-major)
     if ((rc = make_map(&mW_mn, W, H, V, H, MN_BOX, BK))) return rc;     // B of dX = D W   (MN-major)
     const size_t fac_smem = sizeof(float) * static_cast<size_t>(L.nvt);
+    if (a.dW && (rc = sort_labels(a.labels, a.T, static_cast<int>(L.C), a.ignore, V, false, keys, lstart, a.st)))
+        return rc;
     for (int64_t c = 0; c < L.nchunks; ++c) {
         const int64_t t0 = c * L.C;
         const int cl = static_cast<int>(std::min(L.C, a.T - t0));
@@ -488,21 +520,13 @@ int run_tc(const Args& a, const Layout& L, float scale) {
         }
         // 4. dW (+)= D^T X_c, minus scale * X_t in fp32 for each token t labelled with the row
         if (a.dW) {
-            int npow2 = 1;
-            while (npow2 < cl) npow2 <<= 1;
-            sort_label_keys<<<1, 1024, sizeof(unsigned long long) * npow2, a.st>>>(a.labels + t0, cl, a.ignore, npow2,
-                                                                                    0u, keys);
-            if ((rc = check_launch("sort_label_keys"))) return rc;
-            label_starts<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(V + 1, 256), 8 * sm_count())), 256, 0,
-                           a.st>>>(keys, cl, V, 0, lstart);
-            if ((rc = check_launch("label_starts"))) return rc;
             EpiParams d = e;
             d.corr_src = Xc;
             d.ld_corr = H;
             d.corr_scale = scale;
-            d.keys = keys;
+            d.keys = keys + t0;                   // this chunk's keys (token indices relative to the chunk)
             d.nkeys = cl;
-            d.lstart = lstart;
+            d.lstart = lstart + c * (V + 1);
             d.M = V;
             d.N = H;
             d.raster = RASTER_N_FASTEST;
@@ -603,20 +627,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         if ((rc = check_launch("dlogits_bf16"))) return rc;
     }
     // label keys of all tokens, sorted in segments of kMaxSortKeys, one start table per segment
-    if (a.dW) {
-        for (int64_t sg = 0; sg < L.nseg; ++sg) {
-            const int64_t b0 = sg * kMaxSortKeys;
-            const int n = static_cast<int>(std::min<int64_t>(kMaxSortKeys, a.T - b0));
-            int npow2 = 1;
-            while (npow2 < n) npow2 <<= 1;
-            sort_label_keys<<<1, 1024, sizeof(unsigned long long) * npow2, a.st>>>(
-                a.labels + b0, n, a.ignore, npow2, static_cast<unsigned>(b0), keys + b0);
-            if ((rc = check_launch("sort_label_keys"))) return rc;
-            label_starts<<<static_cast<unsigned>(std::min<int64_t>(ceil_div(V + 1, 256), 8 * sm_count())), 256, 0,
-                           a.st>>>(keys + b0, n, V, static_cast<int>(b0), lstart + sg * (V + 1));
-            if ((rc = check_launch("label_starts"))) return rc;
-        }
-    }
+    if (a.dW && (rc = sort_labels(a.labels, a.T, kMaxSortKeys, a.ignore, V, true, keys, lstart, a.st))) return rc;
     // pass 2: per vocabulary chunk, recompute the logits, D_c, dX +=, dW_c
     CUtensorMap mX_all, mX_mn;
     if ((rc = make_map(&mX_all, X, H, T, H, BK, BM))) return rc;     // A of the recompute (K-major)

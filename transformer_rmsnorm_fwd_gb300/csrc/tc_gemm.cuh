@@ -15,7 +15,7 @@
 //    CTAs on neighbouring SMs share tcgen05.mma.cta_group::2 (M=256, N=256):
 //    each CTA loads 128 rows of A and 128 rows of B (32 KB per k-block
 //    instead of 48 KB, so L2->SM traffic per flop drops by a third) into a
-//    6-stage ring, both CTAs' copies complete on the leader's barrier, the
+//    5-stage ring, both CTAs' copies complete on the leader's barrier, the
 //    leader issues the MMAs for both, and its commits are multicast to the
 //    pair's barriers; each CTA's TMEM holds its 128 x 256 half.
 //   warp 0      TMA producer (one lane);
@@ -66,7 +66,7 @@ struct TileCfg {
     static constexpr int BNL = PAIR ? BN / 2 : BN;       // B rows held by this CTA
     static constexpr int B_L = BNL * BK * 2;
     static constexpr int STAGE_L = A_BYTES + B_L;
-    static constexpr int ST = PAIR ? 6 : STAGES;         // ring depth
+    static constexpr int ST = PAIR ? 5 : STAGES;         // ring depth: 5 measured fastest (3 and 4 leave the MMAs waiting; 6 and 7 were slower)
     static constexpr int SMEM = 1024 + ST * STAGE_L + 256;
 };
 
