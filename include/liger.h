@@ -4,10 +4,15 @@
  *
  * Operators (as described on the Liger-Kernel pages):
  *   - RMSNorm forward / backward, a per-row reduction;
- *   - RoPE, rotating Q and K in place;
+ *   - RoPE, rotating Q and K in place (and its variants: interleaved
+ *     pairing, strided Q/K views of a packed QKV buffer, caller tables);
  *   - the SwiGLU activation silu(gate) * up and its backward;
+ *   - FusedLinearSwiGLU: the gate and up projections and the activation in
+ *     one tensor-core GEMM, and its backward;
+ *   - the fused RMSNorm + QKV projection + RoPE forward;
  *   - a fused linear cross-entropy that never writes the full [T x V]
- *     logits to device memory.
+ *     logits to device memory (token-chunked, and a two-pass
+ *     vocabulary-chunked variant).
  *
  * Conventions shared by every entry point:
  *   - Every tensor pointer is a DEVICE pointer (cudaMalloc'd or from a
@@ -202,7 +207,9 @@ int liger_swiglu_bwd(const void* dy, const void* gate, const void* up, void* dga
  *   k[t] = RoPE_p(r_t (x[t] * w) Wk^T + bk)   [B, S, Hk, D]
  *   v[t] =        r_t (x[t] * w) Wv^T + bv    [B, S, Hk, D]
  * with RoPE as liger_rope_fwd (pairs (i, i + D/2) in every head, angle
- * p * theta^(-2i/D), p = pos[b, s] or s), or, given cos_tab / sin_tab
+ * p * theta^(-2i/D), p = pos[b, s] or s; here the angle is reduced modulo
+ * 2 pi in single precision from an exact product, within a few 1e-7 rad for
+ * positions below 2^24), or, given cos_tab / sin_tab
  * ([n_tab, D/2] fp32, indexed by position, clamped to the table), those
  * values as given.
  *   x [B*S, H], w_norm [H], Wq [Hq*D, H], Wk and Wv [Hk*D, H] (nn.Linear
