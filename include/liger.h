@@ -288,8 +288,9 @@ int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, const void* Wu,
  *   may be NULL (not computed).  Rows of dX whose label is ignore_index are
  *   written as +0.0.
  *   The tokens are processed in chunks of `chunk` rows (0 = automatic:
- *   min(T, 8192, max(128, ceil(T/2))) on the bf16 tensor-core path; a chunk
- *   larger than 8192 rows is reduced to 8192 there); per chunk the logits
+ *   min(T, 8192, max(128, ceil(T/2))) on the bf16 tensor-core path; there a
+ *   chunk above 8192 rows is rounded down to a multiple of 8192, at most
+ *   65536); per chunk the logits
  *   exist only in a [chunk x V] workspace buffer, never as a [T x V] tensor
  *   (T > 128).  dW is accumulated across chunks in fp32.
  *   ws: device workspace of at least liger_linear_ce_workspace(T, H, V,

@@ -66,7 +66,9 @@ def test_linear_ce_tiny(cuda_lib, dtype):
 
 
 @pytest.mark.parametrize("T,H,V,chunk", [(300, 320, 2037, 128), (129, 64, 256, 0), (1000, 512, 5000, 333),
-                                         (64, 128, 300, 0), (257, 136, 777, 100)])
+                                         (64, 128, 300, 0), (257, 136, 777, 100),
+                                         (9000, 64, 300, 16384),     # one chunk over two label-sort segments
+                                         (20000, 64, 260, 16384)])   # chunks of 16384 + 3616 rows
 def test_linear_ce_ragged_bf16(cuda_lib, T, H, V, chunk):
     X = datagen.normal(21, "cX", (T, H), "bf16")
     W = datagen.normal(21, "cW", (V, H), "bf16", 0.0, 0.05)

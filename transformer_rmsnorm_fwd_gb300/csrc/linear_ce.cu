@@ -38,7 +38,9 @@ namespace liger {
 namespace {
 
 constexpr int kVT = tc::BN;   // vocab tile of the (m, s) partials
-constexpr int64_t kMaxChunkTC = 8192;   // tensor-core path: rows per chunk (label sort in one block)
+constexpr int kMaxSortKeys = 8192;      // label keys sorted per block (shared memory)
+constexpr int64_t kAutoChunkTC = 8192;   // tensor-core path: most rows per chunk chosen automatically
+constexpr int64_t kMaxChunkTC = 65536;   // tensor-core path: most rows per chunk a caller may ask for
 
 struct Hdr {
     unsigned long long n_valid;
@@ -49,6 +51,7 @@ struct Hdr {
 struct Layout {
     bool tc;
     int64_t C, ldp, nvt, nchunks;
+    int seg;   // label-sort segment: the chunk (C <= 8192, indices relative to it) or 8192 tokens (absolute)
     size_t lse, lossrow, zlab, hdr, keys, lstart, part, scr, acc, total;
 };
 
@@ -61,12 +64,17 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     L.tc = use_tc(H, V, dtype);
     int64_t C;
     if (chunk > 0) C = chunk;
-    // automatic: at most half the tokens (never all T rows at once, for T > 128), at most 8192 rows
-    else if (L.tc) C = std::min<int64_t>(kMaxChunkTC, std::max<int64_t>(128, (T + 1) / 2));
+    // automatic: at most half the tokens (never all T rows at once, for T > 128), at most kAutoChunkTC rows
+    else if (L.tc) C = std::min<int64_t>(kAutoChunkTC, std::max<int64_t>(128, (T + 1) / 2));
     else C = std::max<int64_t>(128, (int64_t{1} << 26) / std::max<int64_t>(V, 1));
-    if (L.tc) C = std::min<int64_t>(C, kMaxChunkTC);
+    if (L.tc) {
+        C = std::min<int64_t>(C, kMaxChunkTC);
+        // above one label-sort block, whole blocks (the chunk's labels are sorted block by block)
+        if (C > kMaxSortKeys && C < T) C = (C / kMaxSortKeys) * kMaxSortKeys;
+    }
     C = std::max<int64_t>(1, std::min(C, std::max<int64_t>(T, 1)));
     L.C = C;
+    L.seg = static_cast<int>(std::min<int64_t>(C, kMaxSortKeys));
     L.nchunks = T > 0 ? ceil_div(T, C) : 0;
     L.ldp = L.tc ? ((V + 7) / 8) * 8 : V;
     L.nvt = ceil_div(V, kVT);
@@ -77,7 +85,7 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     L.hdr = o; o = up256(o + sizeof(Hdr));
     // every chunk's sorted label keys and start table, made in one pass before the chunks
     L.keys = o; o = up256(o + (L.tc ? sizeof(unsigned long long) * static_cast<size_t>(std::max<int64_t>(T, 1)) : 0));
-    L.lstart = o; o = up256(o + (L.tc ? sizeof(int) * static_cast<size_t>(L.nchunks * (V + 1)) : 0));
+    L.lstart = o; o = up256(o + (L.tc ? sizeof(int) * static_cast<size_t>(ceil_div(std::max<int64_t>(T, 1), L.seg) * (V + 1)) : 0));
     L.part = o; o = up256(o + (L.tc ? sizeof(float2) * static_cast<size_t>(C * L.nvt) : 0));
     L.scr = o; o = up256(o + static_cast<size_t>(C) * static_cast<size_t>(L.ldp) * (L.tc ? 2 : 4));
     const bool need_acc = L.nchunks > 1 && dtype == LIGER_BF16;
@@ -125,7 +133,6 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* sh) {
 // one-hot correction of the dW epilogue.  Segment b covers tokens
 // [b*seg, min(n, (b+1)*seg)) and its sorted keys go to out[b*seg ...]; the
 // token index in a key is absolute (b*seg + i) or relative to the segment (i).
-constexpr int kMaxSortKeys = 8192;
 __global__ void __launch_bounds__(1024) sort_label_keys(const int64_t* __restrict__ labels, int64_t n, int seg,
                                                         int64_t ignore, int absolute,
                                                         unsigned long long* __restrict__ out) {
@@ -470,8 +477,10 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     if ((rc = make_map(&mW_k, W, H, V, H, BK, B_BOX_ROWS))) return rc;          // B of Z = X W^T  (K-major)
     if ((rc = make_map(&mW_mn, W, H, V, H, MN_BOX, BK))) return rc;     // B of dX = D W   (MN-major)
     const size_t fac_smem = sizeof(float) * static_cast<size_t>(L.nvt);
-    if (a.dW && (rc = sort_labels(a.labels, a.T, static_cast<int>(L.C), a.ignore, V, false, keys, lstart, a.st)))
-        return rc;
+    // label keys: one segment per chunk (indices relative to the chunk) up to 8192 rows, else
+    // 8192-token segments with absolute indices, several per chunk
+    const bool rel = L.seg == L.C;
+    if (a.dW && (rc = sort_labels(a.labels, a.T, L.seg, a.ignore, V, !rel, keys, lstart, a.st))) return rc;
     for (int64_t c = 0; c < L.nchunks; ++c) {
         const int64_t t0 = c * L.C;
         const int cl = static_cast<int>(std::min(L.C, a.T - t0));
@@ -521,12 +530,20 @@ int run_tc(const Args& a, const Layout& L, float scale) {
         // 4. dW (+)= D^T X_c, minus scale * X_t in fp32 for each token t labelled with the row
         if (a.dW) {
             EpiParams d = e;
-            d.corr_src = Xc;
             d.ld_corr = H;
             d.corr_scale = scale;
-            d.keys = keys + t0;                   // this chunk's keys (token indices relative to the chunk)
             d.nkeys = cl;
-            d.lstart = lstart + c * (V + 1);
+            if (rel) {
+                d.corr_src = Xc;
+                d.keys = keys + t0;               // this chunk's keys (token indices relative to the chunk)
+                d.lstart = lstart + c * (V + 1);
+            } else {
+                d.corr_src = X;                   // absolute token indices
+                d.keys = keys;
+                d.lstart = lstart + (t0 / L.seg) * (V + 1);
+                d.nseg = static_cast<int>(ceil_div(static_cast<int64_t>(cl), static_cast<int64_t>(L.seg)));
+                d.lstride = V + 1;
+            }
             d.M = V;
             d.N = H;
             d.raster = RASTER_N_FASTEST;
@@ -564,7 +581,7 @@ struct Layout2 {
 
 Layout2 layout2(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
     Layout2 L{};
-    L.C = std::max<int64_t>(1, std::min<int64_t>(kMaxChunkTC, T));
+    L.C = std::max<int64_t>(1, std::min<int64_t>(kAutoChunkTC, T));
     L.nvt = ceil_div(V, kVT);
     L.Vc = std::min<int64_t>(vchunk > 0 ? vchunk : kAutoVChunk, V);
     L.ldc = ((L.Vc + 7) / 8) * 8;
