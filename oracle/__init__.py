@@ -65,9 +65,11 @@ def _load():
                                           _P, _P, _P, _P]
             lib.orc_linear_ce_rows.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
                                                _P, _I, _P, _P, _P]
+            lib.orc_linear_ce_dw_rows.argtypes = [_P, _P, ctypes.c_int, _P, _I, _I, _I, _I, ctypes.c_int, _D,
+                                                  _P, _P, _I, _P]
             for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_rope", "orc_rope_ex", "orc_swiglu_fwd", "orc_swiglu_bwd", "orc_linear_swiglu_fwd",
                       "orc_linear_swiglu_bwd",
-                      "orc_linear_ce", "orc_linear_ce_rows"):
+                      "orc_linear_ce", "orc_linear_ce_rows", "orc_linear_ce_dw_rows"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -248,6 +250,35 @@ def linear_ce_rows(X, W, labels, rows, ignore_index=-100, reduction="mean", grad
                                     lse.ctypes.data, lt.ctypes.data, dX.ctypes.data)
     _check(rc, "linear_ce_rows")
     return {"lse": lse, "loss_term": lt, "dX": dX}
+
+
+def linear_ce_rows_fwd(X, W, labels, rows, ignore_index=-100):
+    """lse and the loss term (lse - z_label, 0 if ignored) of the listed rows, without dX."""
+    X, pX = _c(X); W, pW = _c(W)
+    labels = np.ascontiguousarray(labels, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    T, H = X.shape; V = W.shape[0]
+    k = rows.size
+    lse = np.empty((k,), np.float64); lt = np.empty((k,), np.float64)
+    rc = _load().orc_linear_ce_rows(pX, pW, _dt(X, W), labels.ctypes.data, T, H, V, int(ignore_index), 0, 1.0,
+                                    rows.ctypes.data, k, lse.ctypes.data, lt.ctypes.data, None)
+    _check(rc, "linear_ce_rows_fwd")
+    return {"lse": lse, "loss_term": lt}
+
+
+def linear_ce_dw_rows(X, W, labels, lse, vrows, ignore_index=-100, reduction="mean", grad_scale=1.0):
+    """dW rows of the listed vocabulary rows, given lse [T] of every token."""
+    X, pX = _c(X); W, pW = _c(W)
+    labels = np.ascontiguousarray(labels, dtype=np.int64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    vrows = np.ascontiguousarray(vrows, dtype=np.int64)
+    T, H = X.shape; V = W.shape[0]
+    out = np.empty((vrows.size, H), np.float64)
+    rc = _load().orc_linear_ce_dw_rows(pX, pW, _dt(X, W), labels.ctypes.data, T, H, V, int(ignore_index),
+                                       0 if reduction == "mean" else 1, float(grad_scale), lse.ctypes.data,
+                                       vrows.ctypes.data, vrows.size, out.ctypes.data)
+    _check(rc, "linear_ce_dw_rows")
+    return out
 
 
 def rel_err(got, ref):

@@ -444,3 +444,49 @@ int orc_linear_ce_rows(const void* X, const void* W, int dt, const int64_t* labe
     free(z); free(xt); free(wrow);
     return 0;
 }
+
+/* The same definition restricted to the listed vocabulary rows of dW, given
+ * every token's lse (as computed above):
+ *     dW[v, :] = sum over valid t of scale * (exp(z_t[v] - lse_t) - [y_t = v]) * x_t,
+ *     z_t[v] = w_v . x_t.
+ * One pass over the tokens per listed row; n_valid (for the mean) is counted
+ * over all T labels. */
+int orc_linear_ce_dw_rows(const void* X, const void* W, int dt, const int64_t* labels, int64_t T, int64_t H,
+                          int64_t V, int64_t ignore_index, int reduction, double grad_scale, const double* lse,
+                          const int64_t* vrows, int64_t n_vrows, double* dW_rows) {
+    if (!X || !W || !labels || !lse || !vrows || !dW_rows || T < 0 || H <= 0 || V <= 0 || bad_dt(dt) ||
+        (reduction != 0 && reduction != 1))
+        return -1;
+    int bad = 0;
+    int64_t n_valid = count_valid(labels, T, V, ignore_index, &bad);
+    if (bad) return -5;
+    double scale = reduction == 0 ? (n_valid > 0 ? grad_scale / (double)n_valid : 0.0) : grad_scale;
+    double* xt = (double*)malloc(sizeof(double) * (size_t)H);
+    double* wrow = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!xt || !wrow) {
+        free(xt); free(wrow);
+        return -1;
+    }
+    for (int64_t k = 0; k < n_vrows; ++k) {
+        int64_t v = vrows[k];
+        if (v < 0 || v >= V) {
+            free(xt); free(wrow);
+            return -2;
+        }
+        widen(W, dt, v * H, H, wrow);
+        double* out = dW_rows + k * H;
+        for (int64_t h = 0; h < H; ++h) out[h] = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t y = labels[t];
+            if (y == ignore_index) continue;
+            widen(X, dt, t * H, H, xt);
+            double z = 0.0;
+            for (int64_t h = 0; h < H; ++h) z += wrow[h] * xt[h];
+            double d = scale * (exp(z - lse[t]) - (y == v ? 1.0 : 0.0));
+            for (int64_t h = 0; h < H; ++h) out[h] += d * xt[h];
+        }
+    }
+    free(xt); free(wrow);
+    return 0;
+}
+

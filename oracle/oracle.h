@@ -79,6 +79,11 @@ int orc_linear_ce_rows(const void* X, const void* W, int dt, const int64_t* labe
                        int64_t V, int64_t ignore_index, int reduction, double grad_scale,
                        const int64_t* rows, int64_t n_rows, double* lse, double* loss_term, double* dX_rows);
 
+/* Rows of dW for the listed vocabulary rows, given every token's lse. */
+int orc_linear_ce_dw_rows(const void* X, const void* W, int dt, const int64_t* labels, int64_t T, int64_t H,
+                          int64_t V, int64_t ignore_index, int reduction, double grad_scale, const double* lse,
+                          const int64_t* vrows, int64_t n_vrows, double* dW_rows);
+
 #ifdef __cplusplus
 }
 #endif

@@ -210,6 +210,22 @@ def test_ce_rows_matches_full_definition():
     assert abs(part["loss_term"][1]) == 0.0
 
 
+def test_ce_rows_fwd_and_dw_rows_match_full_definition():
+    T, H, V = 11, 5, 17
+    X = RNG.standard_normal((T, H)); W = RNG.standard_normal((V, H)); lab = RNG.integers(0, V, T)
+    lab[3] = -100; lab[7] = lab[0]                        # an ignored row, a label shared by two tokens
+    for red, gs in (("mean", 1.0), ("sum", 0.3)):
+        full = oracle.linear_ce(X, W, lab, reduction=red, grad_scale=gs)
+        fw = oracle.linear_ce_rows_fwd(X, W, lab, np.arange(T))
+        assert np.max(np.abs(fw["lse"] - full["lse"])) < 1e-15
+        valid = lab != -100
+        n = valid.sum() if red == "mean" else 1
+        assert abs(fw["loss_term"].sum() / n - full["loss"]) < 1e-14
+        vrows = np.array([lab[0], 0, V - 1, 9])
+        dw = oracle.linear_ce_dw_rows(X, W, lab, full["lse"], vrows, reduction=red, grad_scale=gs)
+        assert np.max(np.abs(dw - full["dW"][vrows])) < 1e-14
+
+
 def test_storage_widening_is_exact():
     import datagen
     b = datagen.normal(0, "w", (4, 8), "bf16"); f = datagen.bf16_bits_to_f32(b)
