@@ -19,6 +19,7 @@ import pytest
 import datagen
 import oracle
 from datagen import workloads
+from conftest import golden
 from gpu_util import LOSS_TOL_BF16, TOL, bits, dev, host
 
 pytestmark = pytest.mark.gpu
@@ -152,10 +153,12 @@ def test_linear_ce_errors_leave_outputs(cuda_lib):
 
 
 def test_linear_ce_llama3_full_size_sampled(cuda_lib):
-    """T=8192, H=4096, V=128256 bf16 (auto chunk, the benchmark's launch
-    configuration): oracle on sampled rows (lse, loss term, dX row); the loss
-    equals the mean of the sampled-consistent row terms; dW columns sum to ~0
-    over the vocabulary (each D row sums to 0); ignored rows exact zeros."""
+    """T=8192, H=4096, V=128256 bf16 (auto chunk): against the fp64 oracle's
+    lse of every token and mean loss (cached in tests/golden by
+    make_linear_ce_lse.py, the full unchunked definition), dX on sampled
+    rows, dW on sampled vocabulary rows (given the oracle's lse); the loss is the
+    mean of the row terms; dW columns sum to ~0 over the vocabulary; ignored rows
+    exact zeros."""
     import torch
     c = workloads.linear_ce_llama3()
     X, W, lab = c.make("X"), c.make("W"), c.make("labels")
@@ -184,6 +187,18 @@ def test_linear_ce_llama3_full_size_sampled(cuda_lib):
         assert abs(lse[r] - o["lse"][i]) <= 1e-5 * abs(o["lse"][i])
         assert abs(lrow[r] - o["loss_term"][i]) <= 1e-3 * abs(o["loss_term"][i])
         assert oracle.rel_err(hdX[r], o["dX"][i]) <= 2e-2
+    # the oracle's full forward: lse of every token and the mean loss
+    g = golden("linear_ce_llama3_lse.json")
+    olse = np.array(g["lse"])
+    valid = lab != -100
+    assert g["n_valid"] == n_valid
+    assert np.max(np.abs(lse[valid] - olse[valid]) / np.abs(olse[valid])) <= 1e-5
+    assert np.all(lse[~valid] == 0)
+    assert abs(float(loss.item()) - g["loss_mean"]) <= LOSS_TOL_BF16 * abs(g["loss_mean"])
+    # dW rows (each a sum over all 8192 tokens), given the oracle's lse
+    vrows = np.unique(np.concatenate([lab[:4][lab[:4] >= 0], np.random.default_rng(5).choice(V, 12, replace=False)]))
+    odW = oracle.linear_ce_dw_rows(X, W, lab, olse, vrows)
+    assert oracle.rel_err(host(dW[torch.as_tensor(vrows, device="cuda")]), odW) <= 2e-2
     # Gaussian logits z ~ N(0, 0.02^2 |x_t|^2): E[lse_t] = ln V + 0.02^2 |x_t|^2 / 2 for large V and
     # E[z_label] = 0, so the mean loss is ln V + mean_t(0.0002 |x_t|^2) to within ~0.015 (1 sigma)
     xf = datagen.to_f64(X, "bf16")
@@ -193,6 +208,45 @@ def test_linear_ce_llama3_full_size_sampled(cuda_lib):
     ign = lab == -100
     assert np.all(bits(dX)[ign] == 0)
     # sum over the vocabulary of dW rows = sum_t (sum_v D_tv) X_t = 0
-    dWh = host(dW)
-    colsum = dWh.sum(axis=0)
-    assert np.max(np.abs(colsum)) <= 2e-2 * np.max(np.abs(dWh).sum(axis=0))
+    dWd = dW.double()
+    assert float(dWd.sum(0).abs().max()) <= 2e-2 * float(dWd.abs().sum(0).max())
+
+
+def test_linear_ce_qwen_chain_seq32768(cuda_lib):
+    """The benchmark's own linear-CE call: the Qwen-7B head of the chain at seq
+    32768 (hidden 4096, vocab 151936, 10 % ignored), auto chunk (4 chunks of
+    8192 tokens): the mean loss and the lse of every 64th token against the
+    oracle's full forward (cached in tests/golden), dX on sampled rows, and the
+    properties that hold at any size."""
+    import torch
+    c = workloads.qwen_chain(32768)["linear_ce"]
+    X, W, lab = c.make("X"), c.make("W"), c.make("labels")
+    T, H = X.shape
+    V = W.shape[0]
+    tX, tW, tl = dev(X), dev(W), dev(lab)
+    ws = torch.empty(cuda_lib.liger_linear_ce_workspace(T, H, V, 0, 1), dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    dX, dW = torch.empty_like(tX), torch.empty_like(tW)
+    cuda_lib.liger_linear_ce_fwd_bwd(tX, tW, tl, loss, dX, dW, ws)
+    torch.cuda.synchronize()
+    lse = ws[: 4 * T].view(torch.float32).cpu().numpy().astype(np.float64)
+    g = golden("linear_ce_qwen32768_lse.json")
+    st = g["lse_row_stride"]
+    olse = np.array(g["lse"])
+    keep = lab[::st] != -100
+    assert g["n_valid"] == int((lab != -100).sum())
+    assert np.max(np.abs(lse[::st][keep] - olse[keep]) / np.abs(olse[keep])) <= 1e-5
+    assert abs(float(loss.item()) - g["loss_mean"]) <= LOSS_TOL_BF16 * abs(g["loss_mean"])
+    rows = np.array([1, 8191, 8192, 32766])
+    o = oracle.linear_ce_rows(X, W, lab, rows)
+    hdX = host(dX[torch.as_tensor(rows, device="cuda")])
+    for i, r in enumerate(rows):
+        if lab[r] == -100:
+            assert np.all(hdX[i] == 0)
+            continue
+        assert oracle.rel_err(hdX[i], o["dX"][i]) <= 2e-2
+    valid = torch.as_tensor(lab != -100, device="cuda")
+    assert int(torch.count_nonzero(dX[~valid])) == 0
+    dWd = dW.double()
+    assert float(dWd.sum(0).abs().max()) <= 2e-2 * float(dWd.abs().sum(0).max())
+
