@@ -12,6 +12,7 @@ import pytest
 
 import datagen
 import oracle
+from conftest import golden
 from gpu_util import LOSS_TOL_BF16, TOL, bits, dev, host
 
 pytestmark = pytest.mark.gpu
@@ -120,15 +121,24 @@ def test_linear_ce_two_pass_all_ignored_and_errors(cuda_lib):
 
 
 def test_linear_ce_two_pass_qwen7b_seq32768_sampled(cuda_lib):
-    """Qwen-7B head at seq 32768 (hidden 4096, vocab 151936, 10 % ignored), auto
-    vocabulary chunk: oracle on sampled rows (lse, loss term, dX row); the loss
-    is the mean of the row terms and close to its Gaussian-logit value; dW rows
-    sum to ~0 over the vocabulary; ignored rows exact zeros."""
-    T, H, V = 32768, 4096, 151936
-    X = datagen.normal(4, "chain.lce.X", (T, H), "bf16")
-    W = datagen.normal(4, "chain.lce.W", (V, H), "bf16", 0.0, 0.02)
-    lab = datagen.labels(4, "chain.lce.labels", T, V, 0.1)
+    """The Qwen-7B head of the benchmark's chain (seq 32768, hidden 4096, vocab
+    151936, 10 % ignored), auto vocabulary chunk: the mean loss and the lse of
+    every 64th token against the oracle's full forward (cached in tests/golden),
+    oracle on sampled rows (lse, loss term, dX row); the loss is the mean of the
+    row terms and close to its Gaussian-logit value; dW rows sum to ~0 over the
+    vocabulary; ignored rows exact zeros."""
+    from datagen import workloads
+    c = workloads.qwen_chain(32768)["linear_ce"]
+    X, W, lab = c.make("X"), c.make("W"), c.make("labels")
+    T, H = X.shape
+    V = W.shape[0]
     loss, dX, dW, lse, lrow = _run(cuda_lib, X, W, lab)
+    g = golden("linear_ce_qwen32768_lse.json")
+    st = g["lse_row_stride"]
+    olse = np.array(g["lse"])
+    keep = lab[::st] != -100
+    assert np.max(np.abs(lse[::st][keep] - olse[keep]) / np.abs(olse[keep])) <= 1e-5
+    assert abs(loss - g["loss_mean"]) <= LOSS_TOL_BF16 * abs(g["loss_mean"])
     n_valid = int((lab != -100).sum())
     assert abs(loss - lrow.sum() / n_valid) <= 1e-5 * abs(loss)
     rows = np.array([0, 8191, 8192, 32767])
