@@ -4,7 +4,7 @@ through the C-ABI.
 * tiny set (T=256, H=256, V=1024), fp32 (SIMT path) and bf16 (tcgen05 path):
   full loss, dX, dW;
 * ragged bf16 cases: rows, hidden and vocab that are not multiples of the
-  128 x 256 x 64 tensor-core tiles, several token chunks (fp32 dW
+  256 x 256 x 64 tensor-core (CTA-pair) tiles, several token chunks (fp32 dW
   accumulation across chunks), chunk-size invariance;
 * the Llama-3 lm_head shape (8192 x 4096 x 128256) in the benchmark's launch
   configuration: sampled rows of lse and dX against the oracle, and

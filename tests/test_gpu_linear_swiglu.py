@@ -1,6 +1,6 @@
 """GPU parity of FusedLinearSwiGLU (forward and backward) against the fp64
 oracle, through the C-ABI: ragged shapes whose T, H and I are not multiples
-of the 128 x 256 x 64 tensor-core tiles, and the pages' configuration (hidden
+of the 256 x 256 x 64 tensor-core (CTA-pair) tiles, and the pages' configuration (hidden
 4096, intermediate 11008, 4 x 2048 tokens) on sampled rows."""
 import numpy as np
 import pytest
