@@ -280,6 +280,27 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
             ts.append(a.elapsed_time(b))
         ms = statistics.median(ts)
         res[name] = {"ms": round(ms, 3), "tflops": round(fl / ms / 1e9, 1)}
+    # the same work in native PyTorch (two cuBLAS matmuls, silu * mul; backward by autograd),
+    # the comparison the pages quote for this fusion
+    import torch.nn.functional as F
+    Xr, Gr, Ur = X.detach().clone(), Wg.detach().clone(), Wu.detach().clone()
+
+    def torch_fwd():
+        with torch.no_grad():
+            return F.silu(Xr @ Gr.t()) * (Xr @ Ur.t())
+
+    def torch_fwd_bwd():
+        xs, gs, us = Xr.requires_grad_(True), Gr.requires_grad_(True), Ur.requires_grad_(True)
+        h = F.silu(xs @ gs.t()) * (xs @ us.t())
+        h.backward(dH)
+        xs.grad = gs.grad = us.grad = None
+
+    t_fwd = _median_ms(torch_fwd, n)
+    t_fb = _median_ms(torch_fwd_bwd, n)
+    res["torch_fwd_ms"] = round(t_fwd, 3)
+    res["torch_bwd_ms"] = round(max(t_fb - t_fwd, 1e-6), 3)
+    res["speedup_fwd_vs_torch"] = round(t_fwd / res["fwd"]["ms"], 3)
+    res["speedup_bwd_vs_torch"] = round(res["torch_bwd_ms"] / res["bwd"]["ms"], 3)
     return res
 
 
