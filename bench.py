@@ -295,12 +295,19 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
         h.backward(dH)
         xs.grad = gs.grad = us.grad = None
 
+    # the saving pair: the forward also keeps g and u, the backward does not recompute them
+    gs_, us_ = torch.empty_like(out), torch.empty_like(out)
+    res["fwd_save_ms"] = round(_median_ms(lambda: L.liger_fused_linear_swiglu_fwd_save(X, Wg, Wu, out, gs_, us_), n), 3)
+    res["bwd_saved_ms"] = round(_median_ms(
+        lambda: L.liger_fused_linear_swiglu_bwd_saved(X, Wg, Wu, dH, gs_, us_, dX, dWg, dWu, ws), n), 3)
     t_fwd = _median_ms(torch_fwd, n)
     t_fb = _median_ms(torch_fwd_bwd, n)
     res["torch_fwd_ms"] = round(t_fwd, 3)
     res["torch_bwd_ms"] = round(max(t_fb - t_fwd, 1e-6), 3)
     res["speedup_fwd_vs_torch"] = round(t_fwd / res["fwd"]["ms"], 3)
     res["speedup_bwd_vs_torch"] = round(res["torch_bwd_ms"] / res["bwd"]["ms"], 3)
+    res["speedup_fwd_bwd_vs_torch"] = round(t_fb / (res["fwd"]["ms"] + res["bwd"]["ms"]), 3)
+    res["speedup_fwd_bwd_saved_vs_torch"] = round(t_fb / (res["fwd_save_ms"] + res["bwd_saved_ms"]), 3)
     return res
 
 

@@ -268,6 +268,20 @@ int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, const void* Wu,
                                   void* dWu, void* ws, size_t ws_bytes, int64_t T, int64_t H, int64_t I, int dtype,
                                   void* stream);
 
+/* The same pair with the activations kept instead of recomputed (memory for
+ * speed): liger_fused_linear_swiglu_fwd_save also writes g = X W_g^T and
+ * u = X W_u^T ([T, I] bf16, caller-owned, 16-byte aligned; required when
+ * T > 0) from the same GEMM, and liger_fused_linear_swiglu_bwd_saved takes
+ * them back: dG, dU by the elementwise SwiGLU backward (as liger_swiglu_bwd),
+ * then dX and dW_g, dW_u as above -- 8 T H I flops instead of 12, with g and
+ * u rounded to bf16 where the recomputing backward uses them in fp32.  Same
+ * workspace, arguments and errors otherwise. */
+int liger_fused_linear_swiglu_fwd_save(const void* X, const void* Wg, const void* Wu, void* out, void* g, void* u,
+                                       int64_t T, int64_t H, int64_t I, int dtype, void* stream);
+int liger_fused_linear_swiglu_bwd_saved(const void* X, const void* Wg, const void* Wu, const void* dH, const void* g,
+                                        const void* u, void* dX, void* dWg, void* dWu, void* ws, size_t ws_bytes,
+                                        int64_t T, int64_t H, int64_t I, int dtype, void* stream);
+
 /* ------------------------------------------------ fused linear + CE
  * Source: the FusedCrossEntropyLoss paragraph of the page "Liger-Kernel核心
  * 技术：RollingBuffer与融合算子详解", section "算子融合" (softmax and NLL

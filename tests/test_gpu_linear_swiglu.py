@@ -88,3 +88,55 @@ def test_fused_linear_swiglu_errors(cuda_lib):
     with pytest.raises(cuda_lib.LigerError) as e:
         cuda_lib.liger_fused_linear_swiglu_fwd(Xb, Wb, Wb, out.bfloat16())
     assert e.value.status == -2
+
+
+def _run_saved(L, X, Wg, Wu, dH):
+    import torch
+    tX, tg, tu = dev(X), dev(Wg), dev(Wu)
+    T, H = X.shape
+    I = Wg.shape[0]
+    out = torch.empty(T, I, dtype=torch.bfloat16, device="cuda")
+    g, u = torch.empty_like(out), torch.empty_like(out)
+    L.liger_fused_linear_swiglu_fwd_save(tX, tg, tu, out, g, u)
+    ws = torch.empty(L.liger_fused_linear_swiglu_workspace(T, I), dtype=torch.uint8, device="cuda")
+    dX, dWg, dWu = torch.empty_like(tX), torch.empty_like(tg), torch.empty_like(tu)
+    L.liger_fused_linear_swiglu_bwd_saved(tX, tg, tu, dev(dH), g, u, dX, dWg, dWu, ws)
+    torch.cuda.synchronize()
+    return out, g, u, dX, dWg, dWu
+
+
+@pytest.mark.parametrize("T,H,I", [(300, 320, 688), (129, 64, 128), (64, 256, 8)])
+def test_fused_linear_swiglu_saved_ragged(cuda_lib, T, H, I):
+    """The saving forward writes h and the exact-up-to-rounding g = X Wg^T, u = X Wu^T;
+    the backward from them matches the oracle."""
+    X = datagen.normal(53, "vx", (T, H), "bf16")
+    Wg = datagen.normal(53, "vg", (I, H), "bf16", 0.0, 0.05)
+    Wu = datagen.normal(53, "vu", (I, H), "bf16", 0.0, 0.05)
+    dH = datagen.normal(53, "vd", (T, I), "bf16")
+    out, g, u, dX, dWg, dWu = _run_saved(cuda_lib, X, Wg, Wu, dH)
+    xf, gf, uf = (datagen.to_f64(a, "bf16") for a in (X, Wg, Wu))
+    assert oracle.rel_err(host(g), xf @ gf.T) <= 2e-2 and oracle.rel_err(host(u), xf @ uf.T) <= 2e-2
+    assert oracle.rel_err(host(out), oracle.linear_swiglu_fwd(X, Wg, Wu)) <= 2e-2
+    odX, odWg, odWu = oracle.linear_swiglu_bwd(X, Wg, Wu, dH)
+    assert oracle.rel_err(host(dX), odX) <= 2e-2
+    assert oracle.rel_err(host(dWg), odWg) <= 2e-2
+    assert oracle.rel_err(host(dWu), odWu) <= 2e-2
+
+
+def test_fused_linear_swiglu_saved_llama_mlp_sampled(cuda_lib):
+    """T = 4 x 2048, hidden 4096, intermediate 11008: sampled rows of h and dX,
+    sampled intermediate columns of dW_g and dW_u against the oracle."""
+    T, H, I = 8192, 4096, 11008
+    X = datagen.normal(52, "mx", (T, H), "bf16")
+    Wg = datagen.normal(52, "mg", (I, H), "bf16", 0.0, 0.02)
+    Wu = datagen.normal(52, "mu", (I, H), "bf16", 0.0, 0.02)
+    dH = datagen.normal(52, "md", (T, I), "bf16")
+    out, g, u, dX, dWg, dWu = _run_saved(cuda_lib, X, Wg, Wu, dH)
+    rows = np.array([0, 1, 4097, 8191])
+    assert oracle.rel_err(host(out)[rows], oracle.linear_swiglu_fwd(X[rows], Wg, Wu)) <= 2e-2
+    odX, _, _ = oracle.linear_swiglu_bwd(X[rows], Wg, Wu, dH[rows])
+    assert oracle.rel_err(host(dX)[rows], odX) <= 2e-2
+    cols = np.array([0, 257, 5504, 11007])
+    _, odWg, odWu = oracle.linear_swiglu_bwd(X, Wg[cols], Wu[cols], dH[:, cols])
+    assert oracle.rel_err(host(dWg)[cols], odWg) <= 2e-2
+    assert oracle.rel_err(host(dWu)[cols], odWu) <= 2e-2

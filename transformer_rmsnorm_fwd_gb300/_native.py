@@ -44,6 +44,9 @@ SIGNATURES = {
     "liger_fused_linear_swiglu_fwd": ([_P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
     "liger_fused_linear_swiglu_workspace": ([_I64, _I64], _SZ),
     "liger_fused_linear_swiglu_bwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _INT, _P], _INT),
+    "liger_fused_linear_swiglu_fwd_save": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _INT, _P], _INT),
+    "liger_fused_linear_swiglu_bwd_saved": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _I64, _INT, _P],
+                                            _INT),
     "liger_rmsnorm_qkv_rope_workspace": ([_I64, _I64, _I64, _I64, _I64], _SZ),
     "liger_rmsnorm_qkv_rope_fwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P, _SZ, _I64,
                                     _I64, _I64, _I64, _I64, _I64, _D, _D, _INT, _INT, _P], _INT),
@@ -260,6 +263,28 @@ def liger_rmsnorm_qkv_rope_fwd(x, w_norm, Wq, Wk, Wv, q, k, v, ws, batch, seq, n
                                              n_q_heads, n_k_heads, head_dim, float(eps), float(theta),
                                              1 if folded else 0, _dtype_code(x), _stream()))
     return q, k, v
+
+
+def liger_fused_linear_swiglu_fwd_save(X, Wg, Wu, out, g, u):
+    """FusedLinearSwiGLU forward that also writes g = X Wg^T and u = X Wu^T."""
+    _dense(X, Wg, Wu, out, g, u)
+    T, H = X.shape
+    I = Wg.shape[0]
+    _check(load().liger_fused_linear_swiglu_fwd_save(_ptr(X), _ptr(Wg), _ptr(Wu), _ptr(out), _ptr(g), _ptr(u), T, H, I,
+                                                     _dtype_code(X), _stream()))
+    return out, g, u
+
+
+def liger_fused_linear_swiglu_bwd_saved(X, Wg, Wu, dH, g, u, dX, dWg, dWu, ws):
+    """FusedLinearSwiGLU backward from the g, u the saving forward kept."""
+    _dense(X, Wg, Wu, dH, g, u, dX, dWg, dWu, ws)
+    T, H = X.shape
+    I = Wg.shape[0]
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().liger_fused_linear_swiglu_bwd_saved(_ptr(X), _ptr(Wg), _ptr(Wu), _ptr(dH), _ptr(g), _ptr(u), _ptr(dX),
+                                                      _ptr(dWg), _ptr(dWu), _ptr(ws), nbytes, T, H, I, _dtype_code(X),
+                                                      _stream()))
+    return dX, dWg, dWu
 
 
 # ---------------------------------------------------------------- linear CE

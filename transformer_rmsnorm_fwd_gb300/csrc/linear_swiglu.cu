@@ -53,14 +53,18 @@ int check_shapes(int64_t T, int64_t H, int64_t I, int dtype, const char* who) {
 using namespace liger;
 using namespace liger::tc;
 
-extern "C" int liger_fused_linear_swiglu_fwd(const void* X, const void* Wg, const void* Wu, void* out, int64_t T,
-                                             int64_t H, int64_t I, int dtype, void* stream) {
-    clear_error();
-    if (int rc = check_shapes(T, H, I, dtype, "fused_linear_swiglu_fwd")) return rc;
+namespace liger {
+namespace {
+
+int fwd_impl(const void* X, const void* Wg, const void* Wu, void* out, void* g_save, void* u_save, int64_t T,
+             int64_t H, int64_t I, int dtype, void* stream, const char* who) {
+    using namespace tc;
+    if (int rc = check_shapes(T, H, I, dtype, who)) return rc;
     if (T == 0) return LIGER_OK;
-    if (!X || !Wg || !Wu || !out) return fail(LIGER_ERR_NULL, "fused_linear_swiglu_fwd: null tensor pointer");
-    if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(out))
-        return fail(LIGER_ERR_ALIGN, "fused_linear_swiglu_fwd: tensors must be 16-byte aligned");
+    if (!X || !Wg || !Wu || !out) return fail(LIGER_ERR_NULL, "%s: null tensor pointer", who);
+    if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(out) || (g_save && !aligned16(g_save)) ||
+        (u_save && !aligned16(u_save)))
+        return fail(LIGER_ERR_ALIGN, "%s: tensors must be 16-byte aligned", who);
     CUtensorMap mX, mG, mU;
     int rc;
     if ((rc = make_map(&mX, X, H, T, H, BK, BM))) return rc;
@@ -73,6 +77,8 @@ extern "C" int liger_fused_linear_swiglu_fwd(const void* X, const void* Wg, cons
     e.M = static_cast<int>(T);
     e.N = static_cast<int>(I);
     e.out = static_cast<__nv_bfloat16*>(out);
+    e.out2 = static_cast<__nv_bfloat16*>(g_save);
+    e.out3 = static_cast<__nv_bfloat16*>(u_save);
     e.ldo = I;
     e.bsplit = 1;
     e.raster = RASTER_M_FASTEST;
@@ -80,7 +86,70 @@ extern "C" int liger_fused_linear_swiglu_fwd(const void* X, const void* Wg, cons
     e.hint_b = HINT_EVICT_FIRST;   // weights: streamed once
     const int ntile_n = static_cast<int>(ceil_div(I, BN / 2));
     return launch_gemm<0, 0, EPI_SWIGLU, 1>(mX, mG, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
-                                         as_stream(stream), 0, &mX, &mU);
+                                            as_stream(stream), 0, &mX, &mU);
+}
+
+// dX = dG W_g + dU W_u (one GEMM over K = 2I) and dW_g = dG^T X, dW_u = dU^T X,
+// from dG and dU [T, I] bf16.
+int grads_from_dgdu(const void* X, const void* Wg, const void* Wu, const __nv_bfloat16* dG,
+                    const __nv_bfloat16* dU, void* dX, void* dWg, void* dWu, int64_t T, int64_t H, int64_t I,
+                    int* d_err, cudaStream_t st) {
+    using namespace tc;
+    int rc;
+    CUtensorMap mdG_k, mdU_k, mG_mn, mU_mn;
+    if ((rc = make_map(&mdG_k, dG, I, T, I, BK, BM))) return rc;
+    if ((rc = make_map(&mdU_k, dU, I, T, I, BK, BM))) return rc;
+    if ((rc = make_map(&mG_mn, Wg, H, I, H, MN_BOX, BK))) return rc;
+    if ((rc = make_map(&mU_mn, Wu, H, I, H, MN_BOX, BK))) return rc;
+    const int nkb1 = static_cast<int>(ceil_div(I, BK));
+    EpiParams d{};
+    d.err = d_err;
+    d.M = static_cast<int>(T);
+    d.N = static_cast<int>(H);
+    d.out = static_cast<__nv_bfloat16*>(dX);
+    d.ldo = H;
+    d.ksplit_nkb = nkb1;
+    d.raster = RASTER_N_GROUPS;
+    if ((rc = launch_gemm<0, 1, EPI_STORE, 1>(mdG_k, mG_mn, static_cast<int>(T), static_cast<int>(H), 2 * nkb1 * BK,
+                                              d, st, 0, &mdU_k, &mU_mn)))
+        return rc;
+    CUtensorMap mdG_mn, mdU_mn, mX_mn;
+    if ((rc = make_map(&mdG_mn, dG, I, T, I, MN_BOX, BK))) return rc;
+    if ((rc = make_map(&mdU_mn, dU, I, T, I, MN_BOX, BK))) return rc;
+    if ((rc = make_map(&mX_mn, X, H, T, H, MN_BOX, BK))) return rc;
+    EpiParams w{};
+    w.err = d_err;
+    w.M = static_cast<int>(I);
+    w.N = static_cast<int>(H);
+    w.ldo = H;
+    w.out_write = 1;
+    w.raster = RASTER_N_FASTEST;
+    w.hint_a = HINT_EVICT_FIRST;
+    w.hint_b = HINT_EVICT_LAST;   // X: reused by every row block
+    w.out = static_cast<__nv_bfloat16*>(dWg);
+    if ((rc = launch_gemm<1, 1, EPI_ACCUM, 1>(mdG_mn, mX_mn, static_cast<int>(I), static_cast<int>(H),
+                                              static_cast<int>(T), w, st)))
+        return rc;
+    w.out = static_cast<__nv_bfloat16*>(dWu);
+    return launch_gemm<1, 1, EPI_ACCUM, 1>(mdU_mn, mX_mn, static_cast<int>(I), static_cast<int>(H),
+                                           static_cast<int>(T), w, st);
+}
+
+}  // namespace
+}  // namespace liger
+
+extern "C" int liger_fused_linear_swiglu_fwd(const void* X, const void* Wg, const void* Wu, void* out, int64_t T,
+                                             int64_t H, int64_t I, int dtype, void* stream) {
+    clear_error();
+    return fwd_impl(X, Wg, Wu, out, nullptr, nullptr, T, H, I, dtype, stream, "fused_linear_swiglu_fwd");
+}
+
+extern "C" int liger_fused_linear_swiglu_fwd_save(const void* X, const void* Wg, const void* Wu, void* out, void* g,
+                                                  void* u, int64_t T, int64_t H, int64_t I, int dtype,
+                                                  void* stream) {
+    clear_error();
+    if (T > 0 && (!g || !u)) return fail(LIGER_ERR_NULL, "fused_linear_swiglu_fwd_save: g and u are required");
+    return fwd_impl(X, Wg, Wu, out, g, u, T, H, I, dtype, stream, "fused_linear_swiglu_fwd_save");
 }
 
 extern "C" size_t liger_fused_linear_swiglu_workspace(int64_t T, int64_t I) {
@@ -136,43 +205,40 @@ extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, cons
     if ((rc = launch_gemm<0, 0, EPI_SWIGLU_BWD, 1>(mX_k, mG_k, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
                                                st, 0, &mX_k, &mU_k)))
         return rc;
-    // 2. dX = dG W_g + dU W_u (K = 2I: k-blocks of the second product follow those of the first)
-    CUtensorMap mdG_k, mdU_k, mG_mn, mU_mn;
-    if ((rc = make_map(&mdG_k, dG, I, T, I, BK, BM))) return rc;
-    if ((rc = make_map(&mdU_k, dU, I, T, I, BK, BM))) return rc;
-    if ((rc = make_map(&mG_mn, Wg, H, I, H, MN_BOX, BK))) return rc;
-    if ((rc = make_map(&mU_mn, Wu, H, I, H, MN_BOX, BK))) return rc;
-    const int nkb1 = static_cast<int>(ceil_div(I, BK));
-    EpiParams d{};
-    d.err = d_err;
-    d.M = static_cast<int>(T);
-    d.N = static_cast<int>(H);
-    d.out = static_cast<__nv_bfloat16*>(dX);
-    d.ldo = H;
-    d.ksplit_nkb = nkb1;
-    d.raster = RASTER_N_GROUPS;
-    if ((rc = launch_gemm<0, 1, EPI_STORE, 1>(mdG_k, mG_mn, static_cast<int>(T), static_cast<int>(H), 2 * nkb1 * BK, d,
-                                           st, 0, &mdU_k, &mU_mn)))
-        return rc;
+    // 2. dX = dG W_g + dU W_u (K = 2I: k-blocks of the second product follow those of the first);
     // 3. dW_g = dG^T X, dW_u = dU^T X (both operands MN-major, K = T)
-    CUtensorMap mdG_mn, mdU_mn, mX_mn;
-    if ((rc = make_map(&mdG_mn, dG, I, T, I, MN_BOX, BK))) return rc;
-    if ((rc = make_map(&mdU_mn, dU, I, T, I, MN_BOX, BK))) return rc;
-    if ((rc = make_map(&mX_mn, X, H, T, H, MN_BOX, BK))) return rc;
-    EpiParams w{};
-    w.err = d_err;
-    w.M = static_cast<int>(I);
-    w.N = static_cast<int>(H);
-    w.ldo = H;
-    w.out_write = 1;
-    w.raster = RASTER_N_FASTEST;
-    w.hint_a = HINT_EVICT_FIRST;
-    w.hint_b = HINT_EVICT_LAST;   // X: reused by every row block
-    w.out = static_cast<__nv_bfloat16*>(dWg);
-    if ((rc = launch_gemm<1, 1, EPI_ACCUM, 1>(mdG_mn, mX_mn, static_cast<int>(I), static_cast<int>(H),
-                                           static_cast<int>(T), w, st)))
-        return rc;
-    w.out = static_cast<__nv_bfloat16*>(dWu);
-    return launch_gemm<1, 1, EPI_ACCUM, 1>(mdU_mn, mX_mn, static_cast<int>(I), static_cast<int>(H), static_cast<int>(T), w,
-                                        st);
+    return grads_from_dgdu(X, Wg, Wu, dG, dU, dX, dWg, dWu, T, H, I, d_err, st);
+}
+
+extern "C" int liger_fused_linear_swiglu_bwd_saved(const void* X, const void* Wg, const void* Wu, const void* dH,
+                                                   const void* g, const void* u, void* dX, void* dWg, void* dWu,
+                                                   void* ws, size_t ws_bytes, int64_t T, int64_t H, int64_t I,
+                                                   int dtype, void* stream) {
+    clear_error();
+    const char* who = "fused_linear_swiglu_bwd_saved";
+    if (int rc = check_shapes(T, H, I, dtype, who)) return rc;
+    if (!Wg || !Wu || !dWg || !dWu || (T > 0 && (!X || !dH || !g || !u || !dX)))
+        return fail(LIGER_ERR_NULL, "%s: null tensor pointer", who);
+    if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(dH) || !aligned16(g) || !aligned16(u) ||
+        !aligned16(dX) || !aligned16(dWg) || !aligned16(dWu))
+        return fail(LIGER_ERR_ALIGN, "%s: tensors must be 16-byte aligned", who);
+    const size_t need = liger_fused_linear_swiglu_workspace(T, I);
+    if (need > 0 && (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255)))
+        return fail(LIGER_ERR_WORKSPACE, "%s: workspace of %zu bytes (256-byte aligned) required, got %zu", who, need,
+                    ws_bytes);
+    cudaStream_t st = as_stream(stream);
+    if (T == 0) {
+        const size_t wb = static_cast<size_t>(I * H) * 2;
+        if (cudaMemsetAsync(dWg, 0, wb, st) != cudaSuccess || cudaMemsetAsync(dWu, 0, wb, st) != cudaSuccess)
+            return check_launch("fused_linear_swiglu_bwd_saved memset");
+        return LIGER_OK;
+    }
+    int* d_err = nullptr;
+    if (int rc0 = err_word(&d_err)) return rc0;
+    __nv_bfloat16* dG = static_cast<__nv_bfloat16*>(ws);
+    __nv_bfloat16* dU = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + need / 2);
+    // 1. dG, dU from dh and the saved g, u (the elementwise SwiGLU backward)
+    if (int rc = liger_swiglu_bwd(dH, g, u, dG, dU, T * I, LIGER_BF16, stream)) return rc;
+    // 2-3. as in the backward with recompute
+    return grads_from_dgdu(X, Wg, Wu, dG, dU, dX, dWg, dWu, T, H, I, d_err, st);
 }

@@ -136,7 +136,8 @@ struct EpiParams {
     // ksplit_nkb > 0 -- k-blocks from ksplit_nkb on come from the A2 / B2 maps,
     // their k coordinate restarting at 0 (a sum of two products)
     int bsplit, ksplit_nkb;
-    // EPI_SWIGLU: out[row, ni*128 + j] = silu(acc[j]) * acc[128 + j], j < 128, col < N.
+    // EPI_SWIGLU: out[row, ni*128 + j] = silu(acc[j]) * acc[128 + j], j < 128, col < N; with
+    // out2 set, g = acc[j] and u = acc[128 + j] also go to out2 and out3 (bf16, same layout).
     // EPI_SWIGLU_BWD: with dh = src[row, col] recomputes g, u from the
     // accumulator and writes out = dg (dh u s (1 + g (1 - s))), out2 = du (dh g s).
     const __nv_bfloat16* src;
@@ -687,6 +688,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         a[e] = x * __fdividef(1.0f, 1.0f + __expf(-x)) * uv[g * 8 + e];
                                     }
                                     stg16(ep.out + static_cast<int64_t>(row) * ep.ldo + col, pack(a));
+                                    if (ep.out2 != nullptr) {   // keep g and u for a backward without recompute
+                                        float gg[8], uu[8];
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e) {
+                                            gg[e] = gv[g * 8 + e];
+                                            uu[e] = uv[g * 8 + e];
+                                        }
+                                        stg16(ep.out2 + static_cast<int64_t>(row) * ep.ldo + col, pack(gg));
+                                        stg16(ep.out3 + static_cast<int64_t>(row) * ep.ldo + col, pack(uu));
+                                    }
                                 } else {
                                     float d[8];
                                     unpack(dh[g], d);
