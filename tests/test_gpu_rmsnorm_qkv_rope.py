@@ -60,6 +60,8 @@ def _check(got, want):
     (1, 300, 256, 2, 2, 128, False),    # no bias
     (1, 129, 520, 1, 1, 256, True),     # head_dim 256, hidden not a multiple of 64
     (3, 17, 64, 3, 1, 128, True),       # odd head counts: q and k share a tile, N = 640 ends in a half tile
+    (1, 40, 64, 0, 2, 64, True),        # no q heads
+    (1, 40, 64, 2, 0, 64, True),        # no k / v heads
 ])
 def test_rmsnorm_qkv_rope_ragged(cuda_lib, B, S, H, Hq, Hk, D, bias):
     x, w, Wq, Wk, Wv, b = _inputs(61, B, S, H, Hq, Hk, D, bias)
