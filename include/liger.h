@@ -119,9 +119,11 @@ int liger_rmsnorm_bwd(const void* dy, const void* x, const void* w, const float*
  *     Nothing in it needs to start at zero: a call writes every partial sum it
  *     reads.  Calls whose work can overlap on the GPU (several streams,
  *     several host threads) race on the array: the caller must order them.
- *   - Partial rows: min(rows, 2 x SMs, 1024, 16 MiB / (4 * cols)).  When the
- *     last term is the smallest, fewer partials are summed than by
- *     liger_rmsnorm_bwd, so dw may differ from it by rounding only.
+ *   - Partial rows: min(rows, 2 x SMs, 1024, 16 MiB / (4 * cols)).
+ *     liger_rmsnorm_bwd may split the rows into a different number of
+ *     partials (it sizes its grid by the resident blocks per SM), so dw may
+ *     differ from it by rounding only (dx too: its row sums may be reduced
+ *     in another order).
  *   - cols above 16 MiB / 4 = 4194304 does not fit one partial row: the call
  *     returns LIGER_ERR_WORKSPACE and queues nothing.
  */
