@@ -26,7 +26,9 @@
 //               reads it with tcgen05.ld 32 columns at a time and applies the
 //               fused epilogue; the accumulator is double-buffered in TMEM
 //               (2 x 256 columns) so tile i's epilogue overlaps tile i+1's
-//               MMAs.
+//               MMAs.  Each warp moves its 32 rows to and from global memory
+//               through an 8 KB staging buffer as whole row runs (see
+//               store_block), not one 16-byte piece of 32 rows at a time.
 // Every mbarrier wait is bounded (about 4 s of %globaltimer, mbarrier.cuh); on expiry the
 // waiting role records an error code in *ep.err, stops issuing work, waits
 // (bounded) for the copies and MMAs it already issued, and the block frees
@@ -53,7 +55,6 @@ constexpr int MN_BOX = 64;      // MN-major TMA box: 64 (MN) x 64 (K) = 8 KB
 constexpr int MN_BOX_BYTES = MN_BOX * BK * 2;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
 constexpr int B_BOX_ROWS = BN / 2;   // K-major B maps: boxes of 128 rows (two per 256-row stage)
 
 // Tile geometry of one CTA (PAIR = 0) or of a CTA pair sharing one
@@ -67,7 +68,8 @@ struct TileCfg {
     static constexpr int B_L = BNL * BK * 2;
     static constexpr int STAGE_L = A_BYTES + B_L;
     static constexpr int ST = PAIR ? 5 : STAGES;         // ring depth: 5 measured fastest (3 and 4 leave the MMAs waiting; 6 and 7 were slower)
-    static constexpr int SMEM = 1024 + ST * STAGE_L + 256;
+    static constexpr int EPI_STAGE = 4 * 8192;           // the epilogue warps' staging buffers (8 KB each)
+    static constexpr int SMEM = 1024 + ST * STAGE_L + 256 + EPI_STAGE;
 };
 
 enum Epi : int {
@@ -295,6 +297,89 @@ __device__ __forceinline__ void sub_scaled32(float (&v)[32], const __nv_bfloat16
             for (int e = 0; e < 8; ++e) v[g * 8 + e] = fmaf(-s, f[e], v[g * 8 + e]);
         }
     }
+}
+
+// ---- row-run epilogue stores through a warp-private staging buffer
+// An epilogue thread owns one accumulator row, so a direct 16-byte store from
+// every lane touches 32 rows: 32 half-filled sectors per warp instruction.
+// Instead each lane writes its row's block of NCH 16-byte chunks (NCH = 4:
+// 32 bf16 columns, NCH = 8: 32 fp32 columns) into the warp's buffer, and the
+// warp moves the block to global memory as whole row runs, 32 / NCH rows per
+// instruction (full sectors, 4 or 8 lines).  Loads of a block (the fp32 sum,
+// the upstream gradient) take the reverse path.  Chunk j of row r sits in the
+// 16-byte slot j ^ swz(r) of the row, which spreads both the per-row accesses
+// and the row-run accesses of each quarter warp over all 32 banks.
+__device__ __forceinline__ void sts16(uint32_t a, const uint4& v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 lds16(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a)
+                 : "memory");
+    return v;
+}
+template <int NCH>
+__device__ __forceinline__ uint32_t stage_slot(int r, int j) {
+    return NCH == 8 ? static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4))
+                    : static_cast<uint32_t>(r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+}
+// number of 16-byte chunks (epc elements each) of a block starting at column c0 that start below n
+__device__ __forceinline__ int chunks_below(int c0, int n, int epc, int nch) {
+    const int k = n > c0 ? (n - c0 + epc - 1) / epc : 0;
+    return k < nch ? k : nch;
+}
+// this lane's row of the block, to and from the buffer
+template <int NCH>
+__device__ __forceinline__ void stage_row(uint32_t buf, int lane, const uint4 (&v)[NCH]) {
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) sts16(buf + stage_slot<NCH>(lane, j), v[j]);
+}
+template <int NCH>
+__device__ __forceinline__ void unstage_row(uint32_t buf, int lane, uint4 (&v)[NCH]) {
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) v[j] = lds16(buf + stage_slot<NCH>(lane, j));
+}
+// The block whose row 0, chunk 0 is at blk (rows ld bytes apart) as row runs:
+// only rows whose bit is set in `rows` and chunks below nch are written.
+// Every lane of the warp calls it, after a __syncwarp that follows the staging.
+template <int NCH, bool CS>
+__device__ __forceinline__ void store_block(uint32_t buf, int lane, uint8_t* blk, int64_t ld, uint32_t rows, int nch) {
+    constexpr int RPI = 32 / NCH;
+    const int j = lane % NCH, r0 = lane / NCH;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int r = i * RPI + r0;
+        const uint4 v = lds16(buf + stage_slot<NCH>(r, j));
+        if (((rows >> r) & 1u) && j < nch) {
+            if (CS) stg16_cs(blk + r * ld + j * 16, v);
+            else stg16(blk + r * ld + j * 16, v);
+        }
+    }
+}
+// Row runs of a block from global memory into registers (zero where masked) ...
+template <int NCH, bool CS>
+__device__ __forceinline__ void load_block(int lane, const uint8_t* blk, int64_t ld, uint32_t rows, int nch,
+                                           uint4 (&v)[NCH]) {
+    constexpr int RPI = 32 / NCH;
+    const int j = lane % NCH, r0 = lane / NCH;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int r = i * RPI + r0;
+        v[i] = make_uint4(0, 0, 0, 0);
+        if (((rows >> r) & 1u) && j < nch) v[i] = CS ? ldg16_cs(blk + r * ld + j * 16) : ldg16(blk + r * ld + j * 16);
+    }
+}
+// ... and from those registers into the buffer (then __syncwarp and unstage_row)
+template <int NCH>
+__device__ __forceinline__ void stage_block(uint32_t buf, int lane, const uint4 (&v)[NCH]) {
+    constexpr int RPI = 32 / NCH;
+    const int j = lane % NCH, r0 = lane / NCH;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) sts16(buf + stage_slot<NCH>(i * RPI + r0, j), v[i]);
+}
+__device__ __forceinline__ uint4 pack_bf8(const float* f) {
+    return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
 }
 
 // --------------------------------------------------------------- kernel
@@ -536,6 +621,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;                 // TMEM lane quarter this warp may access
         const int rl = q * 32 + lane;           // accumulator row of this thread
+        // this warp's 8 KB staging buffer, after the ring and the barriers
+        const uint32_t sbuf = base + Cfg::ST * Cfg::STAGE_L + 256 + static_cast<uint32_t>(warp - 2) * 8192u;
         // hand the accumulator buffer back to the MMA issuer (the leader's barrier)
         auto release_acc = [&](int a) {
             if (PAIR && !leader) mbar_arrive_cluster(map_to_rank(tempty_bar(a), 0));
@@ -554,16 +641,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             // before waiting for it (label range, first 32 columns of the fp32 sum)
             int k_lo = 0, k_hi = 0;
             uint4 pre[8];
-            float* arow = nullptr;
+            const uint32_t rows = __ballot_sync(0xffffffffu, row_ok);   // bit r: row - lane + r is in range
+            uint8_t* ablk = nullptr;
             if (EPI == EPI_ACCUM) {
-                arow = ep.acc + static_cast<int64_t>(row) * ep.lda + n0;
+                ablk = reinterpret_cast<uint8_t*>(ep.acc + static_cast<int64_t>(row - lane) * ep.lda + n0);
                 if (row_ok && ep.lstart != nullptr) {
                     k_lo = ep.lstart[row];
                     k_hi = ep.lstart[row + 1];
                 }
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    pre[g] = (row_ok && ep.acc_read && n0 + g * 4 < ep.N) ? ldg16_cs(arow + g * 4) : make_uint4(0, 0, 0, 0);
+                load_block<8, true>(lane, ablk, ep.lda * 4, ep.acc_read ? rows : 0u, chunks_below(n0, ep.N, 4, 8), pre);
             }
             const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(as), aphase));
             if (!got) {
@@ -593,7 +679,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 const float ml = m * 1.4426950408889634f;
                 float sum = 0.f;
-                __nv_bfloat16* prow = ep.p_out + static_cast<int64_t>(row) * ep.ldp + n0;
+                // P rows of labelled tokens, as row runs
+                const uint32_t prows = __ballot_sync(0xffffffffu, live);
+                uint8_t* pblk = ep.p_out != nullptr
+                                    ? reinterpret_cast<uint8_t*>(ep.p_out + static_cast<int64_t>(row - lane) * ep.ldp + n0)
+                                    : nullptr;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
@@ -605,18 +695,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         v[j] = e;
                         sum += e;
                     }
-                    if (live && ep.p_out != nullptr) {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int col = n0 + c * 32 + g * 8;
-                            if (col < ep.N) {
-                                uint4 u = make_uint4(pack_bf2(v[g * 8 + 0], v[g * 8 + 1]),
-                                                     pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
-                                                     pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
-                                                     pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
-                                stg16_cs(prow + c * 32 + g * 8, u);
-                            }
-                        }
+                    if (pblk != nullptr) {
+                        const uint4 u[4] = {pack_bf8(v), pack_bf8(v + 8), pack_bf8(v + 16), pack_bf8(v + 24)};
+                        __syncwarp();   // the previous block's row runs have been read
+                        stage_row<4>(sbuf, lane, u);
+                        __syncwarp();
+                        store_block<4, true>(sbuf, lane, pblk + c * 64, ep.ldp * 2, prows,
+                                             chunks_below(n0 + c * 32, ep.N, 8, 4));
                     }
                 }
                 tc_fence_before();
@@ -631,89 +716,86 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool zero = !row_ok || (ep.labels != nullptr && y == ep.ignore_index);
                 const __nv_bfloat16* crow =
                     (ep.corr_src != nullptr && !zero) ? ep.corr_src + y * ep.ld_corr + n0 : nullptr;
-                __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
+                uint8_t* oblk = reinterpret_cast<uint8_t*>(ep.out + static_cast<int64_t>(row - lane) * ep.ldo + n0);
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
                     if (crow != nullptr) sub_scaled32(v, crow + c * 32, ep.corr_scale, ep.N - (n0 + c * 32));
-                    if (row_ok) {
+                    uint4 u[4] = {pack_bf8(v), pack_bf8(v + 8), pack_bf8(v + 16), pack_bf8(v + 24)};
+                    if (zero) {
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int col = n0 + c * 32 + g * 8;
-                            if (col < ep.N) {
-                                uint4 u;
-                                if (zero) {
-                                    u = make_uint4(0, 0, 0, 0);
-                                } else {
-                                    u = make_uint4(pack_bf2(v[g * 8 + 0], v[g * 8 + 1]),
-                                                   pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
-                                                   pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
-                                                   pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
-                                }
-                                stg16_cs(orow + c * 32 + g * 8, u);
-                            }
-                        }
+                        for (int g = 0; g < 4; ++g) u[g] = make_uint4(0, 0, 0, 0);
                     }
+                    __syncwarp();   // the previous block's row runs have been read
+                    stage_row<4>(sbuf, lane, u);
+                    __syncwarp();
+                    store_block<4, true>(sbuf, lane, oblk + c * 64, ep.ldo * 2, rows,
+                                         chunks_below(n0 + c * 32, ep.N, 8, 4));
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(as);
             } else if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
                 const int o0 = ni * (BN / 2);   // first output (intermediate) column of the tile
+                const int64_t orow0 = static_cast<int64_t>(row - lane) * ep.ldo + o0;
+                // staging: out at +0, out2 at +2 KB, out3 at +4 KB, the dh block at +6 KB
+                const uint32_t s_out = sbuf, s_out2 = sbuf + 2048u, s_out3 = sbuf + 4096u, s_dh = sbuf + 6144u;
 #pragma unroll 1
                 for (int c = 0; c < BN / 64; ++c) {
+                    const int nch = chunks_below(o0 + c * 32, ep.N, 8, 4);
                     uint4 dh[4];
-                    if (EPI == EPI_SWIGLU_BWD) {
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int col = o0 + c * 32 + g * 8;
-                            dh[g] = (row_ok && col < ep.N) ? ldg16(ep.src + static_cast<int64_t>(row) * ep.lds + col)
-                                                          : make_uint4(0, 0, 0, 0);
-                        }
-                    }
+                    if (EPI == EPI_SWIGLU_BWD)
+                        load_block<4, false>(lane,
+                                             reinterpret_cast<const uint8_t*>(
+                                                 ep.src + static_cast<int64_t>(row - lane) * ep.lds + o0 + c * 32),
+                                             ep.lds * 2, rows, nch, dh);
                     float gv[32], uv[32];
                     tmem_ld32(taddr + c * 32, gv);
                     tmem_ld32(taddr + BN / 2 + c * 32, uv);
-                    if (row_ok) {
+                    __syncwarp();   // the previous block's row runs have been read
+                    if (EPI == EPI_SWIGLU_BWD) {
+                        stage_block<4>(s_dh, lane, dh);
+                        __syncwarp();
+                        unstage_row<4>(s_dh, lane, dh);   // now this lane's row
+                    }
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int col = o0 + c * 32 + g * 8;
-                            if (col < ep.N) {
-                                float a[8], b[8];
-                                if (EPI == EPI_SWIGLU) {
+                    for (int g = 0; g < 4; ++g) {
+                        float a[8], b[8];
+                        if (EPI == EPI_SWIGLU) {
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        const float x = gv[g * 8 + e];
-                                        a[e] = x * __fdividef(1.0f, 1.0f + __expf(-x)) * uv[g * 8 + e];
-                                    }
-                                    stg16(ep.out + static_cast<int64_t>(row) * ep.ldo + col, pack(a));
-                                    if (ep.out2 != nullptr) {   // keep g and u for a backward without recompute
-                                        float gg[8], uu[8];
-#pragma unroll
-                                        for (int e = 0; e < 8; ++e) {
-                                            gg[e] = gv[g * 8 + e];
-                                            uu[e] = uv[g * 8 + e];
-                                        }
-                                        stg16(ep.out2 + static_cast<int64_t>(row) * ep.ldo + col, pack(gg));
-                                        stg16(ep.out3 + static_cast<int64_t>(row) * ep.ldo + col, pack(uu));
-                                    }
-                                } else {
-                                    float d[8];
-                                    unpack(dh[g], d);
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        const float x = gv[g * 8 + e], u = uv[g * 8 + e];
-                                        const float sg = __fdividef(1.0f, 1.0f + __expf(-x));
-                                        a[e] = d[e] * u * sg * (1.0f + x * (1.0f - sg));
-                                        b[e] = d[e] * (x * sg);
-                                    }
-                                    stg16(ep.out + static_cast<int64_t>(row) * ep.ldo + col, pack(a));
-                                    stg16(ep.out2 + static_cast<int64_t>(row) * ep.ldo + col, pack(b));
-                                }
+                            for (int e = 0; e < 8; ++e) {
+                                const float x = gv[g * 8 + e];
+                                a[e] = x * __fdividef(1.0f, 1.0f + __expf(-x)) * uv[g * 8 + e];
                             }
+                            sts16(s_out + stage_slot<4>(lane, g), pack(a));
+                            if (ep.out2 != nullptr) {   // keep g and u for a backward without recompute
+                                sts16(s_out2 + stage_slot<4>(lane, g), pack_bf8(gv + g * 8));
+                                sts16(s_out3 + stage_slot<4>(lane, g), pack_bf8(uv + g * 8));
+                            }
+                        } else {
+                            float d[8];
+                            unpack(dh[g], d);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float x = gv[g * 8 + e], u = uv[g * 8 + e];
+                                const float sg = __fdividef(1.0f, 1.0f + __expf(-x));
+                                a[e] = d[e] * u * sg * (1.0f + x * (1.0f - sg));
+                                b[e] = d[e] * (x * sg);
+                            }
+                            sts16(s_out + stage_slot<4>(lane, g), pack(a));
+                            sts16(s_out2 + stage_slot<4>(lane, g), pack(b));
                         }
                     }
+                    __syncwarp();
+                    store_block<4, false>(s_out, lane, reinterpret_cast<uint8_t*>(ep.out + orow0 + c * 32), ep.ldo * 2,
+                                          rows, nch);
+                    if (EPI == EPI_SWIGLU_BWD || ep.out2 != nullptr)
+                        store_block<4, false>(s_out2, lane, reinterpret_cast<uint8_t*>(ep.out2 + orow0 + c * 32),
+                                              ep.ldo * 2, rows, nch);
+                    if (EPI == EPI_SWIGLU && ep.out2 != nullptr)
+                        store_block<4, false>(s_out3, lane, reinterpret_cast<uint8_t*>(ep.out3 + orow0 + c * 32),
+                                              ep.ldo * 2, rows, nch);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -722,25 +804,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t y = row_ok ? ep.labels[row] : ep.ignore_index;
                 const bool live = row_ok && y != ep.ignore_index;
                 const float l2 = live ? ep.lse[row] * 1.4426950408889634f : 0.f;
-                __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
+                uint8_t* oblk = reinterpret_cast<uint8_t*>(ep.out + static_cast<int64_t>(row - lane) * ep.ldo + n0);
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
-                    if (row_ok) {
+                    __syncwarp();   // the previous block's row runs have been read
 #pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            const int col = n0 + c * 32 + g * 8;
-                            if (col < ep.N) {
-                                float a[8];
+                    for (int g = 0; g < 4; ++g) {
+                        float a[8];
 #pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    a[e] = live ? ep.corr_scale * exp2f(fmaf(v[g * 8 + e], 1.4426950408889634f, -l2))
-                                                : 0.f;
-                                stg16(orow + c * 32 + g * 8, pack(a));
-                            }
-                        }
+                        for (int e = 0; e < 8; ++e)
+                            a[e] = live ? ep.corr_scale * exp2f(fmaf(v[g * 8 + e], 1.4426950408889634f, -l2)) : 0.f;
+                        sts16(sbuf + stage_slot<4>(lane, g), pack(a));
                     }
+                    __syncwarp();
+                    store_block<4, false>(sbuf, lane, oblk + c * 64, ep.ldo * 2, rows,
+                                          chunks_below(n0 + c * 32, ep.N, 8, 4));
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -833,7 +913,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) release_acc(as);
             } else {
-                __nv_bfloat16* orow = ep.out + static_cast<int64_t>(row) * ep.ldo + n0;
+                uint8_t* oblk = ep.out != nullptr
+                                    ? reinterpret_cast<uint8_t*>(ep.out + static_cast<int64_t>(row - lane) * ep.ldo + n0)
+                                    : nullptr;
                 const int64_t ylab = (row_ok && ep.labels != nullptr) ? ep.labels[row] : ep.ignore_index;
                 const bool zero_row = ep.labels != nullptr && ylab == ep.ignore_index;
                 const __nv_bfloat16* lrow = (ep.labels != nullptr && ep.corr_src != nullptr && ep.keys == nullptr &&
@@ -841,16 +923,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                                                 ? ep.corr_src + ylab * ep.ld_corr + n0
                                                 : nullptr;
                 const int nseg = ep.nseg > 1 ? ep.nseg : 1;
+                // staging: the fp32 block at +0 (4 KB), the bf16 block at +4 KB
+                const uint32_t s_acc = sbuf, s_out = sbuf + 4096u;
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
-                    uint4 nxt[8];
-                    if (c + 1 < BN / 32) {
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            const int col = n0 + (c + 1) * 32 + g * 4;
-                            nxt[g] = (row_ok && ep.acc_read && col < ep.N) ? ldg16_cs(arow + (c + 1) * 32 + g * 4)
-                                                                          : make_uint4(0, 0, 0, 0);
-                        }
+                    __syncwarp();   // the previous block's row runs have been read
+                    if (ep.acc_read) {
+                        stage_block<8>(s_acc, lane, pre);   // block c, fetched one block ahead
+                        if (c + 1 < BN / 32)
+                            load_block<8, true>(lane, ablk + (c + 1) * 128, ep.lda * 4, rows,
+                                                chunks_below(n0 + (c + 1) * 32, ep.N, 4, 8), pre);
                     }
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
@@ -871,42 +953,38 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = 0.f;
                     }
-                    if (row_ok) {
+                    if (ep.acc_read) {
+                        __syncwarp();
+                        uint4 o[8];
+                        unstage_row<8>(s_acc, lane, o);
 #pragma unroll
                         for (int g = 0; g < 8; ++g) {
-                            const int col = n0 + c * 32 + g * 4;
-                            if (col < ep.N) {
-                                float* ap = arow + c * 32 + g * 4;
-                                if (ep.acc_read) {
-                                    float o[4];
-                                    unpack(pre[g], o);
+                            float f[4];
+                            unpack(o[g], f);
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e) v[g * 4 + e] += o[e];
-                                }
-                                if (ep.acc_write) {
-                                    float o[4] = {v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]};
-                                    stg16_cs(ap, pack(o));
-                                }
-                            }
-                        }
-                        if (ep.out_write) {
-#pragma unroll
-                            for (int g = 0; g < 4; ++g) {
-                                const int col = n0 + c * 32 + g * 8;
-                                if (col < ep.N) {
-                                    uint4 u = make_uint4(pack_bf2(v[g * 8 + 0], v[g * 8 + 1]),
-                                                         pack_bf2(v[g * 8 + 2], v[g * 8 + 3]),
-                                                         pack_bf2(v[g * 8 + 4], v[g * 8 + 5]),
-                                                         pack_bf2(v[g * 8 + 6], v[g * 8 + 7]));
-                                    stg16_cs(orow + c * 32 + g * 8, u);
-                                }
-                            }
+                            for (int e = 0; e < 4; ++e) v[g * 4 + e] += f[e];
                         }
                     }
-                    if (c + 1 < BN / 32) {
+                    if (ep.acc_write) {   // this lane's row only: no other lane reads it before the next barrier
+                        uint4 w[8];
 #pragma unroll
-                        for (int g = 0; g < 8; ++g) pre[g] = nxt[g];
+                        for (int g = 0; g < 8; ++g) {
+                            const float f[4] = {v[g * 4 + 0], v[g * 4 + 1], v[g * 4 + 2], v[g * 4 + 3]};
+                            w[g] = pack(f);
+                        }
+                        stage_row<8>(s_acc, lane, w);
                     }
+                    if (ep.out_write) {
+                        const uint4 u[4] = {pack_bf8(v), pack_bf8(v + 8), pack_bf8(v + 16), pack_bf8(v + 24)};
+                        stage_row<4>(s_out, lane, u);
+                    }
+                    __syncwarp();
+                    if (ep.acc_write)
+                        store_block<8, true>(s_acc, lane, ablk + c * 128, ep.lda * 4, rows,
+                                             chunks_below(n0 + c * 32, ep.N, 4, 8));
+                    if (ep.out_write)
+                        store_block<4, true>(s_out, lane, oblk + c * 64, ep.ldo * 2, rows,
+                                             chunks_below(n0 + c * 32, ep.N, 8, 4));
                 }
                 tc_fence_before();
                 __syncwarp();
