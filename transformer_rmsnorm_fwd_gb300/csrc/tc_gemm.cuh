@@ -286,6 +286,52 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// The same load split in two, so that the next chunk's load is in flight while
+// this one is used: issue, then wait.  The wait names the destination
+// registers as operands, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+// t[k] for a run-time k in [0, 32) by a select tree on the bits of k (keeps t in registers)
+__device__ __forceinline__ float select32(const float (&t)[32], int k) {
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a[i] = (k & 16) ? t[i + 16] : t[i];
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1) {
+        const bool hi = (k & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) a[i] = hi ? a[i + w] : a[i];
+    }
+    return a[0];
+}
+// 2^x by the hardware approximation (PTX ex2.approx.ftz.f32: relative error
+// near 2^-22, results below the normal range flushed to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // v[0..32) -= s * src[0..32) over the 8-column groups that start below n_left
 __device__ __forceinline__ void sub_scaled32(float (&v)[32], const __nv_bfloat16* src, float s, int n_left) {
 #pragma unroll
@@ -640,7 +686,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // EPI_ACCUM: everything that does not depend on the accumulator is fetched
             // before waiting for it (label range, first 32 columns of the fp32 sum)
             int k_lo = 0, k_hi = 0;
-            uint4 pre[8];
+            uint4 pre[8], pre2[8];   // EPI_ACCUM: fp32 sum blocks c and c + 1, in flight
             const uint32_t rows = __ballot_sync(0xffffffffu, row_ok);   // bit r: row - lane + r is in range
             uint8_t* ablk = nullptr;
             if (EPI == EPI_ACCUM) {
@@ -650,6 +696,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     k_hi = ep.lstart[row + 1];
                 }
                 load_block<8, true>(lane, ablk, ep.lda * 4, ep.acc_read ? rows : 0u, chunks_below(n0, ep.N, 4, 8), pre);
+                load_block<8, true>(lane, ablk + 128, ep.lda * 4, ep.acc_read ? rows : 0u, chunks_below(n0 + 32, ep.N, 4, 8),
+                                    pre2);
             }
             const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(as), aphase));
             if (!got) {
@@ -661,49 +709,75 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (EPI == EPI_LOGITS) {
                 const int64_t y = row_ok ? ep.labels[row] : ep.ignore_index;
                 const bool live = row_ok && y != ep.ignore_index;
+                const bool full = n0 + BN <= ep.N;   // no column of this tile is masked
+                const int64_t jy = y - n0;           // the label's column in the tile, if in [0, BN)
                 float m = -INFINITY, zl = 0.f;
                 bool has_lab = false;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(taddr + c * 32, v);
+                // Two passes over the tile's TMEM row, each with the next 32 columns'
+                // load in flight while the current ones are used.  Pass 1: row max
+                // (a tree per 32 columns; max is exact in any order) and z at the label.
+                uint32_t ra[32], rb[32];
+                auto max_chunk = [&](int c, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
+                    if (c + 1 < BN / 32) tmem_ld32_issue(taddr + (c + 1) * 32, nxt);
+                    float t[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = n0 + c * 32 + j;
-                        if (col < ep.N) m = fmaxf(m, v[j]);
-                        if (col == y) {
-                            zl = v[j];
-                            has_lab = true;
-                        }
+                    for (int j = 0; j < 32; ++j)
+                        t[j] = (full || n0 + c * 32 + j < ep.N) ? __uint_as_float(cur[j]) : -INFINITY;
+                    if (jy >= c * 32 && jy < c * 32 + 32) {
+                        zl = select32(t, static_cast<int>(jy - c * 32));
+                        has_lab = true;
                     }
+#pragma unroll
+                    for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+                        for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+                    }
+                    m = fmaxf(m, t[0]);
+                    if (c + 1 < BN / 32) tmem_ld_wait(nxt);
+                };
+                tmem_ld32_issue(taddr, ra);
+                tmem_ld_wait(ra);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c += 2) {
+                    max_chunk(c, ra, rb);
+                    max_chunk(c + 1, rb, ra);
                 }
+                // Pass 2: P = exp(z - m) (bf16 row runs for labelled rows) and its sum,
+                // kept as 8 partial sums so the adds do not form one serial chain.
                 const float ml = m * 1.4426950408889634f;
-                float sum = 0.f;
-                // P rows of labelled tokens, as row runs
+                float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 const uint32_t prows = __ballot_sync(0xffffffffu, live);
                 uint8_t* pblk = ep.p_out != nullptr
                                     ? reinterpret_cast<uint8_t*>(ep.p_out + static_cast<int64_t>(row - lane) * ep.ldp + n0)
                                     : nullptr;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(taddr + c * 32, v);
+                auto exp_chunk = [&](int c, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
+                    if (c + 1 < BN / 32) tmem_ld32_issue(taddr + (c + 1) * 32, nxt);
+                    float e[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const int col = n0 + c * 32 + j;
-                        const float e = col < ep.N ? exp2f(fmaf(v[j], 1.4426950408889634f, -ml)) : 0.f;
-                        v[j] = e;
-                        sum += e;
+                        e[j] = (full || n0 + c * 32 + j < ep.N)
+                                   ? ex2_approx(fmaf(__uint_as_float(cur[j]), 1.4426950408889634f, -ml))
+                                   : 0.f;
+                        ps[j & 7] += e[j];
                     }
                     if (pblk != nullptr) {
-                        const uint4 u[4] = {pack_bf8(v), pack_bf8(v + 8), pack_bf8(v + 16), pack_bf8(v + 24)};
+                        const uint4 u[4] = {pack_bf8(e), pack_bf8(e + 8), pack_bf8(e + 16), pack_bf8(e + 24)};
                         __syncwarp();   // the previous block's row runs have been read
                         stage_row<4>(sbuf, lane, u);
                         __syncwarp();
                         store_block<4, true>(sbuf, lane, pblk + c * 64, ep.ldp * 2, prows,
                                              chunks_below(n0 + c * 32, ep.N, 8, 4));
                     }
+                    if (c + 1 < BN / 32) tmem_ld_wait(nxt);
+                };
+                tmem_ld32_issue(taddr, ra);
+                tmem_ld_wait(ra);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c += 2) {
+                    exp_chunk(c, ra, rb);
+                    exp_chunk(c + 1, rb, ra);
                 }
+                const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) release_acc(as);
@@ -925,14 +999,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int nseg = ep.nseg > 1 ? ep.nseg : 1;
                 // staging: the fp32 block at +0 (4 KB), the bf16 block at +4 KB
                 const uint32_t s_acc = sbuf, s_out = sbuf + 4096u;
-#pragma unroll 1
+#pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {
                     __syncwarp();   // the previous block's row runs have been read
                     if (ep.acc_read) {
-                        stage_block<8>(s_acc, lane, pre);   // block c, fetched one block ahead
-                        if (c + 1 < BN / 32)
-                            load_block<8, true>(lane, ablk + (c + 1) * 128, ep.lda * 4, rows,
-                                                chunks_below(n0 + (c + 1) * 32, ep.N, 4, 8), pre);
+                        uint4(&cur)[8] = (c & 1) ? pre2 : pre;
+                        stage_block<8>(s_acc, lane, cur);   // block c, fetched two blocks ahead
+                        if (c + 2 < BN / 32)
+                            load_block<8, true>(lane, ablk + (c + 2) * 128, ep.lda * 4, rows,
+                                                chunks_below(n0 + (c + 2) * 32, ep.N, 4, 8), cur);
                     }
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
