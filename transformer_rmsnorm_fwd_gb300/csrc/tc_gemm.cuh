@@ -879,22 +879,32 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool live = row_ok && y != ep.ignore_index;
                 const float l2 = live ? ep.lse[row] * 1.4426950408889634f : 0.f;
                 uint8_t* oblk = reinterpret_cast<uint8_t*>(ep.out + static_cast<int64_t>(row - lane) * ep.ldo + n0);
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    float v[32];
-                    tmem_ld32(taddr + c * 32, v);
+                // the next 32 TMEM columns load while the current ones are used
+                uint32_t ra[32], rb[32];
+                auto softmax_chunk = [&](int c, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
+                    if (c + 1 < BN / 32) tmem_ld32_issue(taddr + (c + 1) * 32, nxt);
                     __syncwarp();   // the previous block's row runs have been read
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         float a[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            a[e] = live ? ep.corr_scale * exp2f(fmaf(v[g * 8 + e], 1.4426950408889634f, -l2)) : 0.f;
+                            a[e] = live ? ep.corr_scale *
+                                              ex2_approx(fmaf(__uint_as_float(cur[g * 8 + e]), 1.4426950408889634f, -l2))
+                                        : 0.f;
                         sts16(sbuf + stage_slot<4>(lane, g), pack(a));
                     }
                     __syncwarp();
                     store_block<4, false>(sbuf, lane, oblk + c * 64, ep.ldo * 2, rows,
                                           chunks_below(n0 + c * 32, ep.N, 8, 4));
+                    if (c + 1 < BN / 32) tmem_ld_wait(nxt);
+                };
+                tmem_ld32_issue(taddr, ra);
+                tmem_ld_wait(ra);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c += 2) {
+                    softmax_chunk(c, ra, rb);
+                    softmax_chunk(c + 1, rb, ra);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -913,18 +923,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const float* crow = ep.cos_t + tr * ep.ld_tab;
                 const float* srow = ep.sin_t + tr * ep.ld_tab;
                 const int hd = ep.hd, half = hd >> 1;
+                // staging: the two 32-column output blocks of a rotated pair at +0 and +2 KB
+                const uint32_t s_y1 = sbuf, s_y2 = sbuf + 2048u;
 #pragma unroll 1
                 for (int h0 = 0; h0 < BN; h0 += hd) {
                     const int gc = n0 + h0;   // first column of this head
                     if (gc >= ep.N) break;
-                    __nv_bfloat16* dst;
+                    __nv_bfloat16* hbase;
+                    int64_t ldh;
                     if (gc < ep.nq) {
-                        dst = ep.out + static_cast<int64_t>(row) * ep.nq + gc;
+                        hbase = ep.out + gc;
+                        ldh = ep.nq;
                     } else if (gc < ep.nq + ep.nk) {
-                        dst = ep.out2 + static_cast<int64_t>(row) * ep.nk + (gc - ep.nq);
+                        hbase = ep.out2 + (gc - ep.nq);
+                        ldh = ep.nk;
                     } else {
-                        dst = ep.out3 + static_cast<int64_t>(row) * (ep.N - ep.nq - ep.nk) + (gc - ep.nq - ep.nk);
+                        hbase = ep.out3 + (gc - ep.nq - ep.nk);
+                        ldh = ep.N - ep.nq - ep.nk;
                     }
+                    // this head's columns of the warp's 32 rows
+                    uint8_t* hblk = reinterpret_cast<uint8_t*>(hbase + static_cast<int64_t>(row - lane) * ldh);
                     const float* bh = ep.bias + gc;
                     if (gc < ep.nq + ep.nk) {
 #pragma unroll 1
@@ -932,7 +950,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             float a[32], b[32];
                             tmem_ld32(taddr + h0 + j, a);
                             tmem_ld32(taddr + h0 + half + j, b);
-                            if (row_ok) {
+                            __syncwarp();   // the previous blocks' row runs have been read
+                            {
 #pragma unroll
                                 for (int g = 0; g < 4; ++g) {
                                     const int o = j + g * 8;
@@ -957,17 +976,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         y1[e] = x1 * cs[e] - x2 * sn[e];
                                         y2[e] = x2 * cs[e] + x1 * sn[e];
                                     }
-                                    stg16(dst + o, pack(y1));
-                                    stg16(dst + half + o, pack(y2));
+                                    sts16(s_y1 + stage_slot<4>(lane, g), pack(y1));
+                                    sts16(s_y2 + stage_slot<4>(lane, g), pack(y2));
                                 }
                             }
+                            __syncwarp();
+                            store_block<4, false>(s_y1, lane, hblk + j * 2, ldh * 2, rows, 4);
+                            store_block<4, false>(s_y2, lane, hblk + (half + j) * 2, ldh * 2, rows, 4);
                         }
                     } else {
 #pragma unroll 1
                         for (int j = 0; j < hd; j += 32) {
                             float a[32];
                             tmem_ld32(taddr + h0 + j, a);
-                            if (row_ok) {
+                            __syncwarp();   // the previous block's row runs have been read
+                            {
 #pragma unroll
                                 for (int g = 0; g < 4; ++g) {
                                     const int o = j + g * 8;
@@ -977,9 +1000,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                                         __ldg(reinterpret_cast<const float4*>(bh + o + 4));
 #pragma unroll
                                     for (int e = 0; e < 8; ++e) y[e] = fmaf(a[g * 8 + e], rsv, ba[e]);
-                                    stg16(dst + o, pack(y));
+                                    sts16(s_y1 + stage_slot<4>(lane, g), pack(y));
                                 }
                             }
+                            __syncwarp();
+                            store_block<4, false>(s_y1, lane, hblk + j * 2, ldh * 2, rows, 4);
                         }
                     }
                 }
