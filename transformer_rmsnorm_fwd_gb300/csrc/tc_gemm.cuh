@@ -416,6 +416,18 @@ __device__ __forceinline__ void load_block(int lane, const uint8_t* blk, int64_t
         if (((rows >> r) & 1u) && j < nch) v[i] = CS ? ldg16_cs(blk + r * ld + j * 16) : ldg16(blk + r * ld + j * 16);
     }
 }
+// Row runs of a block gathered from rows of a table: row r of the block is
+// table row idx of lane r (every lane passes an in-range idx).
+template <int NCH>
+__device__ __forceinline__ void gather_block(int lane, const uint8_t* base, int64_t ld, int idx, uint4 (&v)[NCH]) {
+    constexpr int RPI = 32 / NCH;
+    const int j = lane % NCH, r0 = lane / NCH;
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        const int tr = __shfl_sync(0xffffffffu, idx, i * RPI + r0);
+        v[i] = ldg16(base + static_cast<int64_t>(tr) * ld + j * 16);
+    }
+}
 // ... and from those registers into the buffer (then __syncwarp and unstage_row)
 template <int NCH>
 __device__ __forceinline__ void stage_block(uint32_t buf, int lane, const uint4 (&v)[NCH]) {
@@ -920,11 +932,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         tr = row % ep.tab_mod;
                     }
                 }
-                const float* crow = ep.cos_t + tr * ep.ld_tab;
-                const float* srow = ep.sin_t + tr * ep.ld_tab;
+                const int tr32 = static_cast<int>(tr);   // table row of this lane's token (n_tab < 2^31)
                 const int hd = ep.hd, half = hd >> 1;
-                // staging: the two 32-column output blocks of a rotated pair at +0 and +2 KB
-                const uint32_t s_y1 = sbuf, s_y2 = sbuf + 2048u;
+                // staging: the two 32-column output blocks of a rotated pair at +0 and +2 KB,
+                // 16 columns of cos and of sin at +4 and +6 KB
+                const uint32_t s_y1 = sbuf, s_y2 = sbuf + 2048u, s_cos = sbuf + 4096u, s_sin = sbuf + 6144u;
 #pragma unroll 1
                 for (int h0 = 0; h0 < BN; h0 += hd) {
                     const int gc = n0 + h0;   // first column of this head
@@ -950,18 +962,39 @@ __global__ void __launch_bounds__(THREADS, 1)
                             float a[32], b[32];
                             tmem_ld32(taddr + h0 + j, a);
                             tmem_ld32(taddr + h0 + half + j, b);
-                            __syncwarp();   // the previous blocks' row runs have been read
-                            {
+                            // cos / sin of 16 pairs at a time: the warp's 32 table rows
+                            // gathered as row runs into the buffer, then each lane's own row
 #pragma unroll
-                                for (int g = 0; g < 4; ++g) {
+                            for (int hh = 0; hh < 2; ++hh) {
+                                const int o0 = j + hh * 16;
+                                uint4 gc4[4], gs4[4];
+                                gather_block<4>(lane, reinterpret_cast<const uint8_t*>(ep.cos_t + o0), ep.ld_tab * 4,
+                                                tr32, gc4);
+                                gather_block<4>(lane, reinterpret_cast<const uint8_t*>(ep.sin_t + o0), ep.ld_tab * 4,
+                                                tr32, gs4);
+                                __syncwarp();   // the buffers' previous contents have been read
+                                stage_block<4>(s_cos, lane, gc4);
+                                stage_block<4>(s_sin, lane, gs4);
+                                __syncwarp();
+                                unstage_row<4>(s_cos, lane, gc4);
+                                unstage_row<4>(s_sin, lane, gs4);
+#pragma unroll
+                                for (int g2 = 0; g2 < 2; ++g2) {
+                                    const int g = hh * 2 + g2;   // 8 pairs: columns j + 8 g
                                     const int o = j + g * 8;
                                     float cs[8], sn[8], ba[8], bb[8], y1[8], y2[8];
-                                    *reinterpret_cast<float4*>(cs) = __ldg(reinterpret_cast<const float4*>(crow + o));
-                                    *reinterpret_cast<float4*>(cs + 4) =
-                                        __ldg(reinterpret_cast<const float4*>(crow + o + 4));
-                                    *reinterpret_cast<float4*>(sn) = __ldg(reinterpret_cast<const float4*>(srow + o));
-                                    *reinterpret_cast<float4*>(sn + 4) =
-                                        __ldg(reinterpret_cast<const float4*>(srow + o + 4));
+#pragma unroll
+                                    for (int h = 0; h < 2; ++h) {
+                                        const uint4 c4 = gc4[g2 * 2 + h], s4 = gs4[g2 * 2 + h];
+                                        cs[h * 4 + 0] = __uint_as_float(c4.x);
+                                        cs[h * 4 + 1] = __uint_as_float(c4.y);
+                                        cs[h * 4 + 2] = __uint_as_float(c4.z);
+                                        cs[h * 4 + 3] = __uint_as_float(c4.w);
+                                        sn[h * 4 + 0] = __uint_as_float(s4.x);
+                                        sn[h * 4 + 1] = __uint_as_float(s4.y);
+                                        sn[h * 4 + 2] = __uint_as_float(s4.z);
+                                        sn[h * 4 + 3] = __uint_as_float(s4.w);
+                                    }
                                     *reinterpret_cast<float4*>(ba) = __ldg(reinterpret_cast<const float4*>(bh + o));
                                     *reinterpret_cast<float4*>(ba + 4) =
                                         __ldg(reinterpret_cast<const float4*>(bh + o + 4));
