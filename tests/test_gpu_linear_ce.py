@@ -250,3 +250,30 @@ def test_linear_ce_qwen_chain_seq32768(cuda_lib):
     dWd = dW.double()
     assert float(dWd.sum(0).abs().max()) <= 2e-2 * float(dWd.abs().sum(0).max())
 
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_linear_ce_token_shards_compose_to_mean(cuda_lib, dtype):
+    """Data-parallel use on one GPU: the batch split into two token shards with
+    different numbers of ignored rows, each shard called in sum mode with
+    grad_scale = 1 / n_valid of the whole batch; the shard losses summed and
+    divided by n_valid, the shard dW summed, the shard dX concatenated equal
+    the oracle's mean over the unsharded batch (the exchanges of a
+    token-sharded step: n_valid, then loss and dW)."""
+    T, H, V = 600, 256, 3000
+    X = datagen.normal(41, "shX", (T, H), dtype)
+    W = datagen.normal(41, "shW", (V, H), dtype, 0.0, 0.05)
+    lab = datagen.labels(41, "shl", T, V, 0.1)
+    lab[:40] = -100                               # the first shard holds more ignored rows
+    n = int((lab != -100).sum())
+    h = 256                                       # shard 0: 256 rows, shard 1: 344 rows
+    parts = [_run(cuda_lib, X[a:b], W, lab[a:b], dtype, reduction="sum", grad_scale=1.0 / n)
+             for a, b in ((0, h), (h, T))]
+    o = oracle.linear_ce(X, W, lab)
+    loss = sum(p[0] for p in parts) / n
+    ltol = 1e-5 if dtype == "f32" else LOSS_TOL_BF16
+    assert abs(loss - o["loss"]) <= ltol * abs(o["loss"])
+    dW = host(parts[0][2]) + host(parts[1][2])
+    dX = np.concatenate([host(parts[0][1]), host(parts[1][1])])
+    assert oracle.rel_err(dW, o["dW"]) <= TOL[dtype]
+    assert oracle.rel_err(dX, o["dX"]) <= TOL[dtype]
