@@ -476,6 +476,23 @@ def cpu_oracle_sample(S, inputs, n_rows=32, n_tokens=1):
     return 1.0 / per_token, desc, per_token
 
 
+def host_cpu():
+    """The host the oracle ran on: logical CPUs and the CPU model (from
+    /proc/cpuinfo where it names one, else the machine type)."""
+    import platform
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                if k.strip().lower() in ("model name", "cpu model", "processor name") and v.strip():
+                    model = v.strip()
+                    break
+    except OSError:
+        pass
+    return {"host_nproc": os.cpu_count(), "host_cpu": model or platform.machine()}
+
+
 def emit(d):
     print(json.dumps(d), flush=True)
 
@@ -496,7 +513,7 @@ def reference_arm(args):
     d = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * S / value, "higher_is_better": True,
          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(S),
-         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc, **host_cpu()},
          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     emit(d)
     return 0
@@ -633,7 +650,7 @@ def native_arm(args):
     cpu = None
     if not args.no_cpu:
         v, desc, _ = cpu_oracle_sample(S, inputs)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc, **host_cpu()}
     d = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
          "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
          "data": "synthetic (seeded SplitMix64/Box-Muller, shapes and distributions of the Qwen-7B layer chain)",
