@@ -277,3 +277,29 @@ def test_linear_ce_token_shards_compose_to_mean(cuda_lib, dtype):
     dX = np.concatenate([host(parts[0][1]), host(parts[1][1])])
     assert oracle.rel_err(dW, o["dW"]) <= TOL[dtype]
     assert oracle.rel_err(dX, o["dX"]) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("V", [300, 512])
+def test_linear_ce_labels_at_tile_edges(cuda_lib, V):
+    """Labels on the first and last column of 32-column chunks and of 256-wide
+    vocabulary tiles, in a full tile and (V = 300) in the ragged last tile: the
+    logits epilogue picks z at the label for lse - z and the one-hot part of
+    D in both its full-tile and masked paths; token-chunked and two-pass."""
+    import torch
+    T, H = 64, 128
+    X = datagen.normal(43, "teX", (T, H), "bf16")
+    W = datagen.normal(43, "teW", (V, H), "bf16", 0.0, 0.05)
+    edges = [0, 1, 31, 32, 63, 64, 127, 128, 224, 255, 256, 257, 287, 288, V - 2, V - 1]
+    lab = datagen.labels(43, "tel", T, V, 0.0)
+    lab[: len(edges)] = edges
+    lab[len(edges) + 1] = -100
+    loss, dX, dW, lse = _run(cuda_lib, X, W, lab, "bf16")
+    _check_full(X, W, lab, "bf16", loss, dX, dW, lse)
+    tX, tW = dev(X), dev(W)
+    ws = torch.empty(cuda_lib.liger_linear_ce_two_pass_workspace(T, H, V, 256), dtype=torch.uint8, device="cuda")
+    l2 = torch.empty(1, dtype=torch.float32, device="cuda")
+    dX2, dW2 = torch.empty_like(tX), torch.empty_like(tW)
+    cuda_lib.liger_linear_ce_two_pass_fwd_bwd(tX, tW, dev(lab), l2, dX2, dW2, ws, -100, "mean", 1.0, 256)
+    torch.cuda.synchronize()
+    lse2 = ws[: 4 * T].view(torch.float32).cpu().numpy().astype(np.float64)
+    _check_full(X, W, lab, "bf16", float(l2.item()), dX2, dW2, lse2)
