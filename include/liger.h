@@ -36,6 +36,11 @@
  *     queues nothing and leaves every output untouched.
  *     liger_last_error() then describes the failure (per calling thread).
  *   - The current CUDA device is the one the pointers belong to.
+ *   - Calls may come from several host threads at once, on any streams and
+ *     devices, as long as they do not share output or workspace buffers
+ *     (liger_rmsnorm_bwd_noalloc shares its scratch array: see there).  The
+ *     library's own per-device state (kernel attributes, occupancy, the
+ *     tensor-map encoder) is set up on first use and safe to race.
  */
 #ifndef LIGER_H
 #define LIGER_H

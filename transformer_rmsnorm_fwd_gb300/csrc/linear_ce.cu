@@ -31,6 +31,8 @@
 // tensor cores would miss the 1e-5 fp32 tolerance, so fp32 stays on FMA.
 #include <math.h>
 
+#include <atomic>
+
 #include "tc_gemm.cuh"
 
 namespace liger {
@@ -444,15 +446,15 @@ int run_simt(const Args& a, const Layout& L, float scale) {
 }
 
 int ensure_sort_attr() {
-    static bool done[64] = {false};   // per device: function attributes belong to each device's context
+    // per device: function attributes belong to each device's context (racing threads set the same value)
+    static std::atomic<bool> done[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return check_launch("sort_label_keys device");
-    bool& sort_attr = done[dev];
-    if (!sort_attr) {
+    if (!done[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(sort_label_keys, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(sizeof(unsigned long long) * kMaxSortKeys)) != cudaSuccess)
             return check_launch("sort_label_keys attribute");
-        sort_attr = true;
+        done[dev].store(true, std::memory_order_release);
     }
     return LIGER_OK;
 }

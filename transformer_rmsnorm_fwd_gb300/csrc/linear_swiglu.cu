@@ -20,6 +20,8 @@
 //    GEMM over K = 2I that reads (dG, W_g) for the first half of its k-blocks
 //    and (dU, W_u) for the second; dW_g and dW_u are two GEMMs with both
 //    operands MN-major.
+#include <atomic>
+
 #include "tc_gemm.cuh"
 
 namespace liger {
@@ -30,12 +32,16 @@ namespace {
 static __device__ int g_lsw_err;
 
 int err_word(int** out) {
-    static int* addr[64] = {nullptr};
+    static std::atomic<int*> addr[64];   // per device; racing threads store the same address
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(LIGER_ERR_CUDA, "no CUDA device");
-    if (!addr[dev] && cudaGetSymbolAddress(reinterpret_cast<void**>(&addr[dev]), g_lsw_err) != cudaSuccess)
-        return check_launch("fused_linear_swiglu error word");
-    *out = addr[dev];
+    int* a = addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&a), g_lsw_err) != cudaSuccess)
+            return check_launch("fused_linear_swiglu error word");
+        addr[dev].store(a, std::memory_order_release);
+    }
+    *out = a;
     return LIGER_OK;
 }
 

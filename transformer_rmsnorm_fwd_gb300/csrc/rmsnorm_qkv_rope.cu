@@ -40,12 +40,16 @@ struct InvFreqQkv {
 static __device__ int g_qkv_err;
 
 int qkv_err_word(int** out) {
-    static int* addr[64] = {nullptr};
+    static std::atomic<int*> addr[64];   // per device; racing threads store the same address
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(LIGER_ERR_CUDA, "no CUDA device");
-    if (!addr[dev] && cudaGetSymbolAddress(reinterpret_cast<void**>(&addr[dev]), g_qkv_err) != cudaSuccess)
-        return check_launch("rmsnorm_qkv_rope error word");
-    *out = addr[dev];
+    int* a = addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&a), g_qkv_err) != cudaSuccess)
+            return check_launch("rmsnorm_qkv_rope error word");
+        addr[dev].store(a, std::memory_order_release);
+    }
+    *out = a;
     return LIGER_OK;
 }
 

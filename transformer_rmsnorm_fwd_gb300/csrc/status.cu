@@ -2,6 +2,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace liger {
@@ -25,8 +27,9 @@ int check_launch(const char* what) {
 }
 
 static constexpr int kMaxDev = 64;
-static int g_sms[kMaxDev] = {0};
-static int g_smem[kMaxDev] = {0};
+// 0 = not yet read; racing threads store the same value
+static std::atomic<int> g_sms[kMaxDev];
+static std::atomic<int> g_smem[kMaxDev];
 
 int sm_count() {
     int dev = 0;
@@ -36,23 +39,23 @@ int sm_count() {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         return n > 0 ? n : 148;
     }
-    if (g_sms[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-        g_sms[dev] = n;
+    int v = g_sms[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 148;
+        g_sms[dev].store(v, std::memory_order_relaxed);
     }
-    return g_sms[dev];
+    return v;
 }
 
 int max_smem_optin() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-    if (g_smem[dev] == 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) n = 0;
-        g_smem[dev] = n;
+    int v = g_smem[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) v = 0;
+        g_smem[dev].store(v, std::memory_order_relaxed);
     }
-    return g_smem[dev];
+    return v;
 }
 
 }  // namespace liger

@@ -37,6 +37,8 @@
 
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "mbarrier.cuh"
 
@@ -1167,15 +1169,15 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int 
                 const CUtensorMap* mb2 = nullptr) {
     using Cfg = TileCfg<PAIR>;
     auto kern = tc_gemm_kernel<A_MN, B_MN, EPI, PAIR>;
-    // per instantiation and device: function attributes belong to each device's context
+    // per instantiation and device: function attributes belong to each device's context.
+    // units_of[dev] = 0 until the attribute is set; threads that race here all set the
+    // same attribute and store the same count (published with release / acquire).
     constexpr int kDevs = 64;
-    static bool attr_done[kDevs] = {false};
-    static int units_of[kDevs] = {0};
+    static std::atomic<int> units_of[kDevs];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return check_launch("tc_gemm device");
-    bool& attr_set = attr_done[dev];
-    int& max_units = units_of[dev];
-    if (!attr_set) {
+    int max_units = units_of[dev].load(std::memory_order_acquire);
+    if (max_units == 0) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) != cudaSuccess)
             return check_launch("tc_gemm attribute");
         if (PAIR) {
@@ -1197,7 +1199,7 @@ int launch_gemm(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int 
         } else {
             max_units = sm_count();
         }
-        attr_set = true;
+        units_of[dev].store(max_units, std::memory_order_release);
     }
     const int tiles = ((M + Cfg::TM - 1) / Cfg::TM) * ((N + BN - 1) / BN);
     int units = max_units;
