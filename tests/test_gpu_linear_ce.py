@@ -259,7 +259,8 @@ def test_linear_ce_token_shards_compose_to_mean(cuda_lib, dtype):
     grad_scale = 1 / n_valid of the whole batch; the shard losses summed and
     divided by n_valid, the shard dW summed, the shard dX concatenated equal
     the oracle's mean over the unsharded batch (the exchanges of a
-    token-sharded step: n_valid, then loss and dW)."""
+    token-sharded step: n_valid, then loss and dW); the summed dW within
+    the two shards' own error bounds, each shard rounded on its own."""
     T, H, V = 600, 256, 3000
     X = datagen.normal(41, "shX", (T, H), dtype)
     W = datagen.normal(41, "shW", (V, H), dtype, 0.0, 0.05)
@@ -273,10 +274,19 @@ def test_linear_ce_token_shards_compose_to_mean(cuda_lib, dtype):
     loss = sum(p[0] for p in parts) / n
     ltol = 1e-5 if dtype == "f32" else LOSS_TOL_BF16
     assert abs(loss - o["loss"]) <= ltol * abs(o["loss"])
-    dW = host(parts[0][2]) + host(parts[1][2])
     dX = np.concatenate([host(parts[0][1]), host(parts[1][1])])
-    assert oracle.rel_err(dW, o["dW"]) <= TOL[dtype]
     assert oracle.rel_err(dX, o["dX"]) <= TOL[dtype]
+    # dW: each shard's output is rounded to the storage type on its own, so the
+    # summed result is bounded by the two shards' allowed errors (where the
+    # shards nearly cancel, that is large next to the sum itself)
+    os_ = [oracle.linear_ce(X[a:b], W, lab[a:b], reduction="sum", grad_scale=1.0 / n) for a, b in ((0, h), (h, T))]
+    assert np.max(np.abs(os_[0]["dW"] + os_[1]["dW"] - o["dW"])) <= 1e-12 * np.max(np.abs(o["dW"]))
+    allow = np.zeros_like(o["dW"])
+    for p, q in zip(parts, os_):
+        g = host(p[2])
+        assert oracle.rel_err(g, q["dW"]) <= TOL[dtype]
+        allow += TOL[dtype] * np.maximum(np.abs(q["dW"]), np.sqrt(np.mean(q["dW"] ** 2)))
+    assert np.all(np.abs(host(parts[0][2]) + host(parts[1][2]) - o["dW"]) <= allow)
 
 
 @pytest.mark.parametrize("V", [300, 512])
