@@ -215,15 +215,20 @@ class Chain:
                                                        self.ws_r))
 
 
-def isolated_times(chain, dev, n=10):
-    """Each memory-bound operator of the chain timed alone (median of n launches):
-    ms per call.  Before each launch L2 is flushed by writing a 512 MB buffer and
-    then reading it back, so that none of the operator's inputs is resident and
-    no other buffer's dirty lines are left for the operator to write back (the
-    state ncu's cache control leaves before a capture)."""
+def isolated_times(chain, dev):
+    """Each memory-bound operator of the chain timed alone: median ms per call
+    (timed_median).  Before each launch L2 is flushed by writing a 512 MB buffer
+    and then reading it back, so that none of the operator's inputs is resident
+    and no other buffer's dirty lines are left for the operator to write back
+    (the state ncu's cache control leaves before a capture)."""
     import torch
     L, i = chain.L, chain.inp
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush.view(torch.int32).amax()   # read back: L2 left holding clean lines of the flush buffer
+
     ops = {
         "rmsnorm_fwd": lambda: L.liger_rmsnorm_fwd(i["x"], i["w"], chain.y, chain.rstd, EPS),
         "rmsnorm_bwd": lambda: L.liger_rmsnorm_bwd(i["dy_r"], i["x"], i["w"], chain.rstd, chain.dx, chain.dw,
@@ -233,25 +238,12 @@ def isolated_times(chain, dev, n=10):
         "swiglu_fwd": lambda: L.liger_swiglu_fwd(i["gate"], i["up"], chain.ys),
         "swiglu_bwd": lambda: L.liger_swiglu_bwd(i["dy_s"], i["gate"], i["up"], chain.dg, chain.du),
     }
-    out = {}
-    for name, fn in ops.items():
-        fn()
-        ts = []
-        for _ in range(n):
-            flush.zero_()
-            flush.view(torch.int32).amax()   # read back: L2 left holding clean lines of the flush buffer
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        out[name] = statistics.median(ts)
+    out = {name: timed_median(fn, pre=flush_l2) for name, fn in ops.items()}
     del flush
     return out
 
 
-def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
+def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER):
     """FusedLinearSwiGLU at the pages' MLP shape (8192 tokens, hidden 4096,
     intermediate 11008), forward and backward alone: ms and TFLOP/s
     (forward 4*T*H*I flops; backward 12*T*H*I: recompute, dX, dW)."""
@@ -268,17 +260,7 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
     for name, fn, fl in (("fwd", lambda: L.liger_fused_linear_swiglu_fwd(X, Wg, Wu, out), 4 * T * H * I),
                          ("bwd", lambda: L.liger_fused_linear_swiglu_bwd(X, Wg, Wu, dH, dX, dWg, dWu, ws),
                           12 * T * H * I)):
-        fn()
-        fn()
-        ts = []
-        for _ in range(n):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ms = statistics.median(ts)
+        ms = timed_median(fn)
         res[name] = {"ms": round(ms, 3), "tflops": round(fl / ms / 1e9, 1)}
     # the same work in native PyTorch (two cuBLAS matmuls, silu * mul; backward by autograd),
     # the comparison the pages quote for this fusion
@@ -297,11 +279,11 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
 
     # the saving pair: the forward also keeps g and u, the backward does not recompute them
     gs_, us_ = torch.empty_like(out), torch.empty_like(out)
-    res["fwd_save_ms"] = round(_median_ms(lambda: L.liger_fused_linear_swiglu_fwd_save(X, Wg, Wu, out, gs_, us_), n), 3)
-    res["bwd_saved_ms"] = round(_median_ms(
-        lambda: L.liger_fused_linear_swiglu_bwd_saved(X, Wg, Wu, dH, gs_, us_, dX, dWg, dWu, ws), n), 3)
-    t_fwd = _median_ms(torch_fwd, n)
-    t_fb = _median_ms(torch_fwd_bwd, n)
+    res["fwd_save_ms"] = round(timed_median(lambda: L.liger_fused_linear_swiglu_fwd_save(X, Wg, Wu, out, gs_, us_)), 3)
+    res["bwd_saved_ms"] = round(timed_median(
+        lambda: L.liger_fused_linear_swiglu_bwd_saved(X, Wg, Wu, dH, gs_, us_, dX, dWg, dWu, ws)), 3)
+    t_fwd = timed_median(torch_fwd)
+    t_fb = timed_median(torch_fwd_bwd)
     res["torch_fwd_ms"] = round(t_fwd, 3)
     res["torch_bwd_ms"] = round(max(t_fb - t_fwd, 1e-6), 3)
     res["speedup_fwd_vs_torch"] = round(t_fwd / res["fwd"]["ms"], 3)
@@ -311,12 +293,24 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER, n=5):
     return res
 
 
-def _median_ms(fn, n):
+WARMUP_ITERS, MIN_ITERS, MIN_TIMED_MS, FLOOR_ITERS = 10, 50, 200.0, 5
+
+
+def timed_median(fn, pre=None):
+    """Median ms of one call of fn, timed with CUDA events on the current
+    stream: 10 untimed warm-up calls, then timed calls until 50 have run or
+    200 ms have been timed (and at least 5 have run).  pre() runs before every
+    call, outside the timed region (the L2 flush of the memory-bound ops)."""
     import torch
-    fn()
-    fn()
+    for _ in range(WARMUP_ITERS):
+        if pre is not None:
+            pre()
+        fn()
+    torch.cuda.synchronize()
     ts = []
-    for _ in range(n):
+    while len(ts) < MIN_ITERS and not (sum(ts) >= MIN_TIMED_MS and len(ts) >= FLOOR_ITERS):
+        if pre is not None:
+            pre()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -326,7 +320,7 @@ def _median_ms(fn, n):
     return statistics.median(ts)
 
 
-def rmsnorm_qkv_rope_measure(L, dev, S=32768, H=HIDDEN, Hq=HEADS, Hk=HEADS, D=HEAD_DIM, n=5):
+def rmsnorm_qkv_rope_measure(L, dev, S=32768, H=HIDDEN, Hq=HEADS, Hk=HEADS, D=HEAD_DIM):
     """Fused RMSNorm + QKV projection (+ bias) + RoPE forward at the Qwen-7B layer
     shapes and the chain's sequence length, alone: the whole call (weight fold,
     rstd/angle pre-pass, GEMM with the scale/bias/RoPE epilogue), the call with
@@ -355,8 +349,8 @@ def rmsnorm_qkv_rope_measure(L, dev, S=32768, H=HIDDEN, Hq=HEADS, Hk=HEADS, D=HE
         return lambda: L.liger_rmsnorm_qkv_rope_fwd(x, wn, Wq, Wk, Wv, q, k, v, ws, 1, S, Hq, Hk, D, bq=bq, bk=bk,
                                                     bv=bv, eps=EPS, theta=THETA, folded=folded)
 
-    ms_full = _median_ms(fused(False), n)
-    ms_folded = _median_ms(fused(True), n)
+    ms_full = timed_median(fused(False))
+    ms_folded = timed_median(fused(True))
     del ws
     Wcat = torch.cat([Wq, Wk, Wv]).t()
     bcat = torch.cat([bq, bk, bv])
@@ -368,21 +362,21 @@ def rmsnorm_qkv_rope_measure(L, dev, S=32768, H=HIDDEN, Hq=HEADS, Hk=HEADS, D=HE
         torch.addmm(bcat, xn, Wcat, out=qkv)
         L.liger_rope_fwd_ex(qkv, qkv[:, nq:], N, N, Hq, Hk, D, 1, S, theta=THETA)
 
-    ms_unf = _median_ms(unfused, n)
+    ms_unf = timed_median(unfused)
     return {"ms": round(ms_full, 3), "tflops": round(fl / ms_full / 1e9, 1),
             "ms_folded_weights": round(ms_folded, 3), "tflops_folded_weights": round(fl / ms_folded / 1e9, 1),
             "ms_unfused_cublas": round(ms_unf, 3), "speedup_vs_unfused": round(ms_unf / ms_full, 3)}
 
 
-def linear_ce_two_pass_measure(chain, dev, n=3):
+def linear_ce_two_pass_measure(chain, dev):
     """The two-pass, vocabulary-chunked linear CE on the chain's own head inputs
     (seq x 4096 x 151936), alone: ms, TFLOP/s counting its 8*S*H*V flops and the
     operator's 6*S*H*V, and both variants' workspace bytes."""
     import torch
     L, i, S = chain.L, chain.inp, chain.S
     ws = torch.empty(L.liger_linear_ce_two_pass_workspace(S, HIDDEN, VOCAB), dtype=torch.uint8, device=dev)
-    ms = _median_ms(lambda: L.liger_linear_ce_two_pass_fwd_bwd(i["X"], i["W"], i["labels"], chain.loss, chain.dX,
-                                                               chain.dW, ws), n)
+    ms = timed_median(lambda: L.liger_linear_ce_two_pass_fwd_bwd(i["X"], i["W"], i["labels"], chain.loss, chain.dX,
+                                                               chain.dW, ws))
     fl = float(S) * HIDDEN * VOCAB
     return {"ms": round(ms, 3), "tflops_8shv": round(8 * fl / ms / 1e9, 1), "tflops_6shv": round(6 * fl / ms / 1e9, 1),
             "workspace_bytes": int(ws.numel()), "workspace_bytes_token_chunked": int(chain.ws_c.numel())}
