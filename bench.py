@@ -220,7 +220,8 @@ def isolated_times(chain, dev):
     (timed_median).  Before each launch L2 is flushed by writing a 512 MB buffer
     and then reading it back, so that none of the operator's inputs is resident
     and no other buffer's dirty lines are left for the operator to write back
-    (the state ncu's cache control leaves before a capture)."""
+    (the state ncu's cache control leaves before a capture); the in-place RoPE
+    gets its inputs restored first."""
     import torch
     L, i = chain.L, chain.inp
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -238,8 +239,22 @@ def isolated_times(chain, dev):
         "swiglu_fwd": lambda: L.liger_swiglu_fwd(i["gate"], i["up"], chain.ys),
         "swiglu_bwd": lambda: L.liger_swiglu_bwd(i["dy_s"], i["gate"], i["up"], chain.dg, chain.du),
     }
-    out = {name: timed_median(fn, pre=flush_l2) for name, fn in ops.items()}
-    del flush
+    # RoPE rotates in place: each timed call starts from the same values, restored
+    # (then the flush) before it, outside the timed region
+    saved = {k: i[k].clone() for k in ("q", "k", "dq", "dk")}
+
+    def restore(keys):
+        def pre():
+            for k in keys:
+                i[k].copy_(saved[k])
+            flush_l2()
+        return pre
+
+    pres = {"rope_fwd": restore(("q", "k")), "rope_bwd": restore(("dq", "dk"))}
+    out = {name: timed_median(fn, pre=pres.get(name, flush_l2)) for name, fn in ops.items()}
+    for k, v in saved.items():
+        i[k].copy_(v)
+    del flush, saved
     return out
 
 
