@@ -185,9 +185,12 @@ class Chain:
     def launches_per_step(self):
         chunk = min(self.S, 8192, max(128, (self.S + 1) // 2))
         nchunks = -(-self.S // chunk)
-        # linear CE: label scan, label sort and start tables (once), per chunk the logits GEMM,
-        # dlogits, dX GEMM and dW GEMM, loss reduction
-        return 1 + 1 + 1 + (1 + 2 + 4 * nchunks + 1) + 1 + 1 + 2
+        # the logits GEMM runs over at most 32 MiB of X rows per launch (4096 rows at hidden 4096)
+        sub = max(1, min(chunk, max(256, (32 << 20) // (2 * HIDDEN) // 256 * 256)))
+        logits = sum(-(-min(chunk, self.S - c * chunk) // sub) for c in range(nchunks))
+        # linear CE: label scan, label sort and start tables (once), the logits GEMM launches, per
+        # chunk dlogits, dX GEMM and dW GEMM, loss reduction
+        return 1 + 1 + 1 + (1 + 2 + logits + 3 * nchunks + 1) + 1 + 1 + 2
 
     def step(self, ev=None):
         """One pass of every operator; ev: dict name -> list of (start, end) events."""

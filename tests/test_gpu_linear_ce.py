@@ -313,3 +313,29 @@ def test_linear_ce_labels_at_tile_edges(cuda_lib, V):
     torch.cuda.synchronize()
     lse2 = ws[: 4 * T].view(torch.float32).cpu().numpy().astype(np.float64)
     _check_full(X, W, lab, "bf16", float(l2.item()), dX2, dW2, lse2)
+
+
+def test_linear_ce_logits_in_l2_sized_launches(cuda_lib):
+    """The logits GEMM runs over at most 32 MiB of X rows per launch: at hidden
+    2048 a 16384-row chunk takes two launches of 8192 rows, an 8192-row chunk
+    one.  lse, the loss and dX are bit-identical between the two chunkings,
+    and sampled rows match the oracle."""
+    T, H, V = 16384, 2048, 1000
+    X = datagen.normal(44, "lsX", (T, H), "bf16")
+    W = datagen.normal(44, "lsW", (V, H), "bf16", 0.0, 0.02)
+    lab = datagen.labels(44, "lsl", T, V, 0.1)
+    a = _run(cuda_lib, X, W, lab, "bf16", chunk=16384)
+    b = _run(cuda_lib, X, W, lab, "bf16", chunk=8192)
+    assert a[0] == b[0]
+    assert np.array_equal(a[3], b[3])
+    assert np.array_equal(bits(a[1]), bits(b[1]))
+    assert oracle.rel_err(host(a[2]), host(b[2])) <= 2e-2
+    rows = np.array([0, 4095, 8191, 8192, 12288, 16383])
+    o = oracle.linear_ce_rows(X, W, lab, rows)
+    hdX = host(a[1])
+    for i, r in enumerate(rows):
+        if lab[r] == -100:
+            assert a[3][r] == 0
+            continue
+        assert abs(a[3][r] - o["lse"][i]) <= 1e-5 * abs(o["lse"][i])
+        assert oracle.rel_err(hdX[r], o["dX"][i]) <= 2e-2

@@ -43,6 +43,12 @@ constexpr int kVT = tc::BN;   // vocab tile of the (m, s) partials
 constexpr int kMaxSortKeys = 8192;      // label keys sorted per block (shared memory)
 constexpr int64_t kAutoChunkTC = 8192;   // tensor-core path: most rows per chunk chosen automatically
 constexpr int64_t kMaxChunkTC = 65536;   // tensor-core path: most rows per chunk a caller may ask for
+// A logits GEMM launch sweeps the whole vocabulary over its rows of X, which must stay
+// resident in L2 meanwhile (W and P stream past them): at most this many bytes of X rows
+// per launch, a quarter of the 129 MB L2.  At hidden 4096, 4096 rows: an 8192-row chunk's
+// logits take two launches, which read W twice but each X row once (one launch over all
+// 8192 rows read 12.7x the algorithmic bytes from DRAM).
+constexpr int64_t kLogitsXBytes = int64_t{32} << 20;
 
 struct Hdr {
     unsigned long long n_valid;
@@ -459,6 +465,33 @@ int ensure_sort_attr() {
     return LIGER_OK;
 }
 
+// rows of X per logits GEMM launch (a multiple of 256, at least 256, at most C)
+int64_t logits_rows(int64_t H, int64_t C) {
+    const int64_t r = kLogitsXBytes / (2 * H) / 256 * 256;
+    return std::max<int64_t>(1, std::min(C, std::max<int64_t>(256, r)));
+}
+
+// Z = X_c W^T for the cl rows at Xc with the logits epilogue e (its labels, zlab,
+// part and p_out set for row 0 of the chunk), in launches of logits_rows rows
+int launch_logits(const __nv_bfloat16* Xc, int cl, int H, int V, const CUtensorMap& mW_k, const tc::EpiParams& e,
+                  int64_t ldp, int64_t nvt, cudaStream_t st) {
+    using namespace tc;
+    const int64_t sub = logits_rows(H, cl);
+    for (int64_t s0 = 0; s0 < cl; s0 += sub) {
+        const int sl = static_cast<int>(std::min<int64_t>(sub, cl - s0));
+        CUtensorMap mX;
+        if (int rc = make_map(&mX, Xc + s0 * H, H, sl, H, BK, BM)) return rc;   // A (K-major)
+        EpiParams f = e;
+        f.M = sl;
+        f.labels = e.labels + s0;
+        f.zlab = e.zlab + s0;
+        f.part = e.part + s0 * nvt;
+        if (e.p_out != nullptr) f.p_out = e.p_out + s0 * ldp;
+        if (int rc = launch_gemm<0, 0, EPI_LOGITS, 1>(mX, mW_k, sl, V, H, f, st)) return rc;
+    }
+    return LIGER_OK;
+}
+
 int run_tc(const Args& a, const Layout& L, float scale) {
     using namespace tc;
     if (int rc = ensure_sort_attr()) return rc;
@@ -488,8 +521,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
         const int cl = static_cast<int>(std::min(L.C, a.T - t0));
         const bool first = c == 0, last = c == L.nchunks - 1;
         const __nv_bfloat16* Xc = X + t0 * H;
-        CUtensorMap mX_k, mX_mn, mD_k, mD_mn;
-        if ((rc = make_map(&mX_k, Xc, H, cl, H, BK, BM))) return rc;     // A of Z (K-major)
+        CUtensorMap mX_mn, mD_k, mD_mn;
         if ((rc = make_map(&mX_mn, Xc, H, cl, H, MN_BOX, BK))) return rc;  // B of dW (MN-major)
         if ((rc = make_map(&mD_k, P, V, cl, L.ldp, BK, BM))) return rc;  // A of dX (K-major)
         if ((rc = make_map(&mD_mn, P, V, cl, L.ldp, MN_BOX, BK))) return rc;  // A of dW (MN-major)
@@ -509,7 +541,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
         e.part = part;
         e.nvt = static_cast<int>(L.nvt);
         e.zlab = zlab + t0;
-        if ((rc = launch_gemm<0, 0, EPI_LOGITS, 1>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
+        if ((rc = launch_logits(Xc, cl, H, V, mW_k, e, L.ldp, L.nvt, a.st))) return rc;
         // 2. lse, loss terms, P -> D in place
         dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
                                                           zlab + t0, P, L.ldp, V, scale, lse + t0, lossrow + t0);
@@ -625,8 +657,6 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
     const size_t fac_smem = sizeof(float) * static_cast<size_t>(L.nvt);
     for (int64_t t0 = 0; t0 < a.T; t0 += L.C) {
         const int cl = static_cast<int>(std::min(L.C, a.T - t0));
-        CUtensorMap mX_k;
-        if ((rc = make_map(&mX_k, X + t0 * H, H, cl, H, BK, BM))) return rc;
         EpiParams e{};
         e.err = &hdr->err;
         e.ignore_index = a.ignore;
@@ -640,7 +670,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         e.part = part;
         e.nvt = static_cast<int>(L.nvt);
         e.zlab = zlab + t0;
-        if ((rc = launch_gemm<0, 0, EPI_LOGITS, 1>(mX_k, mW_k, cl, V, H, e, a.st))) return rc;
+        if ((rc = launch_logits(X + t0 * H, cl, H, V, mW_k, e, 0, L.nvt, a.st))) return rc;
         dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
                                                           zlab + t0, nullptr, 0, V, scale, lse + t0, lossrow + t0);
         if ((rc = check_launch("dlogits_bf16"))) return rc;
