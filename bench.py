@@ -188,9 +188,11 @@ class Chain:
         # the logits GEMM runs over at most 32 MiB of X rows per launch (4096 rows at hidden 4096)
         sub = max(1, min(chunk, max(256, (32 << 20) // (2 * HIDDEN) // 256 * 256)))
         logits = sum(-(-min(chunk, self.S - c * chunk) // sub) for c in range(nchunks))
+        # the dX GEMM runs over vocabulary slabs of at most 65536 rows
+        dx = 1 if VOCAB <= 65536 else -(-VOCAB // 65536)
         # linear CE: label scan, label sort and start tables (once), the logits GEMM launches, per
-        # chunk dlogits, dX GEMM and dW GEMM, loss reduction
-        return 1 + 1 + 1 + (1 + 2 + logits + 3 * nchunks + 1) + 1 + 1 + 2
+        # chunk dlogits, the dX GEMM launches and the dW GEMM, loss reduction
+        return 1 + 1 + 1 + (1 + 2 + logits + (2 + dx) * nchunks + 1) + 1 + 1 + 2
 
     def step(self, ev=None):
         """One pass of every operator; ev: dict name -> list of (start, end) events."""

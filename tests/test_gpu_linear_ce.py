@@ -339,3 +339,18 @@ def test_linear_ce_logits_in_l2_sized_launches(cuda_lib):
             continue
         assert abs(a[3][r] - o["lse"][i]) <= 1e-5 * abs(o["lse"][i])
         assert oracle.rel_err(hdX[r], o["dX"][i]) <= 2e-2
+
+
+def test_linear_ce_dx_over_vocabulary_slabs(cuda_lib):
+    """Above 65536 vocabulary rows the dX GEMM runs over equal slabs of the
+    vocabulary (here two of 33280 rows, the second ragged), summed in fp32, the
+    one-hot part subtracted in the last slab: full dX, dW and loss against the
+    oracle, with labels on both sides of the slab boundary and in the last
+    slab, and ignored rows +0."""
+    T, H, V = 256, 64, 66536
+    X = datagen.normal(45, "slX", (T, H), "bf16")
+    W = datagen.normal(45, "slW", (V, H), "bf16", 0.0, 0.05)
+    lab = datagen.labels(45, "sll", T, V, 0.1)
+    lab[:6] = [0, 33279, 33280, 33281, V - 1, 16000]
+    loss, dX, dW, lse = _run(cuda_lib, X, W, lab, "bf16")
+    _check_full(X, W, lab, "bf16", loss, dX, dW, lse)

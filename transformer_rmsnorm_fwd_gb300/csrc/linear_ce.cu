@@ -49,6 +49,19 @@ constexpr int64_t kMaxChunkTC = 65536;   // tensor-core path: most rows per chun
 // logits take two launches, which read W twice but each X row once (one launch over all
 // 8192 rows read 12.7x the algorithmic bytes from DRAM).
 constexpr int64_t kLogitsXBytes = int64_t{32} << 20;
+// The dX GEMM's K is the whole vocabulary: over 150 k vocabulary rows the tiles of a
+// wave drift apart along K and stop sharing their D and W slices through L2 (it read
+// 4-6x its operand bytes from DRAM).  Above this many vocabulary rows it runs in
+// launches over equal slabs of at most this many rows (0: one launch), the partial sums
+// kept in an fp32 [chunk x H] buffer; each launch starts the wave's tiles together.
+constexpr int64_t kDxSlabRows = 65536;
+
+// vocabulary rows per dX launch: V itself, or equal slabs (multiples of 256) of at most kDxSlabRows
+int64_t dx_slab(int64_t V) {
+    if (kDxSlabRows <= 0 || V <= kDxSlabRows) return V;
+    const int64_t n = (V + kDxSlabRows - 1) / kDxSlabRows;
+    return ((V + n - 1) / n + 255) / 256 * 256;
+}
 
 struct Hdr {
     unsigned long long n_valid;
@@ -60,7 +73,7 @@ struct Layout {
     bool tc;
     int64_t C, ldp, nvt, nchunks;
     int seg;   // label-sort segment: the chunk (C <= 8192, indices relative to it) or 8192 tokens (absolute)
-    size_t lse, lossrow, zlab, hdr, keys, lstart, part, scr, acc, total;
+    size_t lse, lossrow, zlab, hdr, keys, lstart, part, scr, acc, dxacc, total;
 };
 
 inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -98,6 +111,8 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     L.scr = o; o = up256(o + static_cast<size_t>(C) * static_cast<size_t>(L.ldp) * (L.tc ? 2 : 4));
     const bool need_acc = L.nchunks > 1 && dtype == LIGER_BF16;
     L.acc = o; o = up256(o + (need_acc ? sizeof(float) * static_cast<size_t>(V * H) : 0));
+    const bool dx_slabs = L.tc && dx_slab(V) < V;
+    L.dxacc = o; o = up256(o + (dx_slabs ? sizeof(float) * static_cast<size_t>(C * H) : 0));
     L.total = o;
     return L;
 }
@@ -547,7 +562,38 @@ int run_tc(const Args& a, const Layout& L, float scale) {
                                                           zlab + t0, P, L.ldp, V, scale, lse + t0, lossrow + t0);
         if ((rc = check_launch("dlogits_bf16"))) return rc;
         // 3. dX_c = D W, minus scale * W[label] in fp32
-        if (a.dX) {
+        if (a.dX && dx_slab(V) < V) {
+            // over vocabulary slabs, summed in fp32; the last slab subtracts scale * W[label]
+            // and writes dX in bf16
+            float* dxacc = reinterpret_cast<float*>(a.ws + L.dxacc);
+            const int64_t slab = dx_slab(V);
+            for (int64_t v0 = 0; v0 < V; v0 += slab) {
+                const int vl = static_cast<int>(std::min<int64_t>(slab, V - v0));
+                const bool s_first = v0 == 0, s_last = v0 + vl >= V;
+                CUtensorMap mDs_k, mWs_mn;
+                if ((rc = make_map(&mDs_k, P + v0, vl, cl, L.ldp, BK, BM))) return rc;     // A: D[:, slab] (K-major)
+                if ((rc = make_map(&mWs_mn, W + v0 * H, H, vl, H, MN_BOX, BK))) return rc;  // B: W[slab, :] (MN-major)
+                EpiParams d = e;
+                d.p_out = nullptr;
+                d.M = cl;
+                d.N = H;
+                d.raster = RASTER_N_GROUPS;
+                d.hint_a = HINT_NORMAL;
+                d.hint_b = HINT_NORMAL;
+                d.acc = dxacc;
+                d.lda = H;
+                d.acc_read = s_first ? 0 : 1;
+                d.acc_write = s_last ? 0 : 1;
+                d.out_write = s_last ? 1 : 0;
+                d.out = static_cast<__nv_bfloat16*>(a.dX) + t0 * H;
+                d.ldo = H;
+                d.keys = nullptr;
+                d.corr_src = s_last ? W : nullptr;
+                d.ld_corr = H;
+                d.corr_scale = scale;
+                if ((rc = launch_gemm<0, 1, EPI_ACCUM, 1>(mDs_k, mWs_mn, cl, H, vl, d, a.st))) return rc;
+            }
+        } else if (a.dX) {
             EpiParams d = e;
             d.M = cl;
             d.N = H;
