@@ -314,6 +314,10 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER):
 
 
 WARMUP_ITERS, MIN_ITERS, MIN_TIMED_MS, FLOOR_ITERS = 10, 50, 200.0, 5
+# DRAM bytes (read + written) of one linear-CE call at seq 32768, from one ncu capture of
+# every launch of the call with the kernels as they are now (profiles/dram_linear_ce_s32768.md);
+# to be retaken whenever a kernel of the call changes
+LINEAR_CE_TRAFFIC = 144_341_915_648
 
 
 def timed_median(fn, pre=None):
@@ -658,7 +662,10 @@ def native_arm(args):
     ce_tf = alg["linear_ce_flops"] / (per_op["linear_ce"] / 1000.0) / 1e12
     roofline = {"kernel": "liger_linear_ce_fwd_bwd (tcgen05 GEMMs + fused epilogues; 6*S*H*V flops per call)",
                 "bound": "tensor", "achieved": round(ce_tf, 1), "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                "frac": round(ce_tf / pk["bf16_sustained"], 4), "traffic": None,
+                "frac": round(ce_tf / pk["bf16_sustained"], 4),
+                "traffic": LINEAR_CE_TRAFFIC if S == 32768 else None, "traffic_unit": "bytes per call",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over every launch of one "
+                                  "call at seq 32768 (one pass, full size): profiles/dram_linear_ce_s32768.md",
                 "peak_source": f"{pk['src']} bf16 sustained (cuBLAS loop under the power cap)",
                 "ms_per_call": round(per_op["linear_ce"], 3)}
     cpu = None
