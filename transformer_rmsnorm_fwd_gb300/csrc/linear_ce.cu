@@ -626,7 +626,9 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             }
             d.M = V;
             d.N = H;
-            d.raster = RASTER_N_FASTEST;
+            // groups of 8 column blocks of X_c (33.5 MB at hidden 4096) stay in L2 through the
+            // vocabulary sweep; n fastest would touch all of X_c in every wave
+            d.raster = RASTER_N_GROUPS;
             d.hint_a = HINT_NORMAL;        // D^T (evict-first measured ~1 % slower with CTA-pair tiles)
             d.hint_b = HINT_EVICT_LAST;    // X_c: reused by every vocab row block, keep in L2
             d.labels = nullptr;
