@@ -43,12 +43,6 @@ constexpr int kVT = tc::BN;   // vocab tile of the (m, s) partials
 constexpr int kMaxSortKeys = 8192;      // label keys sorted per block (shared memory)
 constexpr int64_t kAutoChunkTC = 8192;   // tensor-core path: most rows per chunk chosen automatically
 constexpr int64_t kMaxChunkTC = 65536;   // tensor-core path: most rows per chunk a caller may ask for
-// A logits GEMM launch sweeps the whole vocabulary over its rows of X, which must stay
-// resident in L2 meanwhile (W and P stream past them): at most this many bytes of X rows
-// per launch, a quarter of the 129 MB L2.  At hidden 4096, 4096 rows: an 8192-row chunk's
-// logits take two launches, which read W twice but each X row once (one launch over all
-// 8192 rows read 12.7x the algorithmic bytes from DRAM).
-constexpr int64_t kLogitsXBytes = int64_t{32} << 20;
 // The dX GEMM's K is the whole vocabulary: over 150 k vocabulary rows the tiles of a
 // wave drift apart along K and stop sharing their D and W slices through L2 (it read
 // 4-6x its operand bytes from DRAM).  Above this many vocabulary rows it runs in
@@ -480,18 +474,14 @@ int ensure_sort_attr() {
     return LIGER_OK;
 }
 
-// rows of X per logits GEMM launch (a multiple of 256, at least 256, at most C)
-int64_t logits_rows(int64_t H, int64_t C) {
-    const int64_t r = kLogitsXBytes / (2 * H) / 256 * 256;
-    return std::max<int64_t>(1, std::min(C, std::max<int64_t>(256, r)));
-}
-
 // Z = X_c W^T for the cl rows at Xc with the logits epilogue e (its labels, zlab,
-// part and p_out set for row 0 of the chunk), in launches of logits_rows rows
+// part and p_out set for row 0 of the chunk), in launches over rows_in_l2 rows: each
+// launch sweeps the whole vocabulary over its rows of X (an 8192-row chunk at hidden
+// 4096 takes two launches, reading W twice but each X row once)
 int launch_logits(const __nv_bfloat16* Xc, int cl, int H, int V, const CUtensorMap& mW_k, const tc::EpiParams& e,
                   int64_t ldp, int64_t nvt, cudaStream_t st) {
     using namespace tc;
-    const int64_t sub = logits_rows(H, cl);
+    const int64_t sub = rows_in_l2(H, cl);
     for (int64_t s0 = 0; s0 < cl; s0 += sub) {
         const int sl = static_cast<int>(std::min<int64_t>(sub, cl - s0));
         CUtensorMap mX;

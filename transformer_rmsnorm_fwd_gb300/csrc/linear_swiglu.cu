@@ -71,9 +71,8 @@ int fwd_impl(const void* X, const void* Wg, const void* Wu, void* out, void* g_s
     if (!aligned16(X) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(out) || (g_save && !aligned16(g_save)) ||
         (u_save && !aligned16(u_save)))
         return fail(LIGER_ERR_ALIGN, "%s: tensors must be 16-byte aligned", who);
-    CUtensorMap mX, mG, mU;
+    CUtensorMap mG, mU;
     int rc;
-    if ((rc = make_map(&mX, X, H, T, H, BK, BM))) return rc;
     if ((rc = make_map(&mG, Wg, H, I, H, BK, BN / 2))) return rc;
     if ((rc = make_map(&mU, Wu, H, I, H, BK, BN / 2))) return rc;
     int* d_err = nullptr;
@@ -89,10 +88,24 @@ int fwd_impl(const void* X, const void* Wg, const void* Wu, void* out, void* g_s
     e.bsplit = 1;
     e.raster = RASTER_M_FASTEST;
     e.hint_a = HINT_EVICT_LAST;    // X: reused by every column tile
-    e.hint_b = HINT_EVICT_FIRST;   // weights: streamed once
+    e.hint_b = HINT_EVICT_FIRST;   // weights: streamed once per launch
     const int ntile_n = static_cast<int>(ceil_div(I, BN / 2));
-    return launch_gemm<0, 0, EPI_SWIGLU, 1>(mX, mG, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
-                                            as_stream(stream), 0, &mX, &mU);
+    // launches over rows_in_l2 rows of X, each sweeping all of W_g, W_u over rows that stay in L2
+    const int64_t sub = rows_in_l2(H, T);
+    for (int64_t m0 = 0; m0 < T; m0 += sub) {
+        const int ml = static_cast<int>(std::min<int64_t>(sub, T - m0));
+        CUtensorMap mX;
+        if ((rc = make_map(&mX, static_cast<const __nv_bfloat16*>(X) + m0 * H, H, ml, H, BK, BM))) return rc;
+        EpiParams f = e;
+        f.M = ml;
+        f.out = e.out + m0 * I;
+        if (e.out2 != nullptr) f.out2 = e.out2 + m0 * I;
+        if (e.out3 != nullptr) f.out3 = e.out3 + m0 * I;
+        if ((rc = launch_gemm<0, 0, EPI_SWIGLU, 1>(mX, mG, ml, ntile_n * BN, static_cast<int>(H), f, as_stream(stream),
+                                                   0, &mX, &mU)))
+            return rc;
+    }
+    return LIGER_OK;
 }
 
 // dX = dG W_g + dU W_u (one GEMM over K = 2I) and dW_g = dG^T X, dW_u = dU^T X,
@@ -129,7 +142,8 @@ int grads_from_dgdu(const void* X, const void* Wg, const void* Wu, const __nv_bf
     w.N = static_cast<int>(H);
     w.ldo = H;
     w.out_write = 1;
-    w.raster = RASTER_N_FASTEST;
+    // groups of 8 column blocks of X (33.5 MB at T = 8192) stay in L2 through the sweep over I
+    w.raster = RASTER_N_GROUPS;
     w.hint_a = HINT_EVICT_FIRST;
     w.hint_b = HINT_EVICT_LAST;   // X: reused by every row block
     w.out = static_cast<__nv_bfloat16*>(dWg);
@@ -189,9 +203,8 @@ extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, cons
     __nv_bfloat16* dG = static_cast<__nv_bfloat16*>(ws);
     __nv_bfloat16* dU = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + need / 2);
     int rc;
-    // 1. recompute g, u; dG, dU from dh
-    CUtensorMap mX_k, mG_k, mU_k;
-    if ((rc = make_map(&mX_k, X, H, T, H, BK, BM))) return rc;
+    // 1. recompute g, u; dG, dU from dh (in launches over rows_in_l2 rows of X, as the forward)
+    CUtensorMap mG_k, mU_k;
     if ((rc = make_map(&mG_k, Wg, H, I, H, BK, BN / 2))) return rc;
     if ((rc = make_map(&mU_k, Wu, H, I, H, BK, BN / 2))) return rc;
     EpiParams e{};
@@ -208,9 +221,20 @@ extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, cons
     e.hint_a = HINT_EVICT_LAST;
     e.hint_b = HINT_EVICT_FIRST;
     const int ntile_n = static_cast<int>(ceil_div(I, BN / 2));
-    if ((rc = launch_gemm<0, 0, EPI_SWIGLU_BWD, 1>(mX_k, mG_k, static_cast<int>(T), ntile_n * BN, static_cast<int>(H), e,
-                                               st, 0, &mX_k, &mU_k)))
-        return rc;
+    const int64_t sub = rows_in_l2(H, T);
+    for (int64_t m0 = 0; m0 < T; m0 += sub) {
+        const int ml = static_cast<int>(std::min<int64_t>(sub, T - m0));
+        CUtensorMap mX_k;
+        if ((rc = make_map(&mX_k, static_cast<const __nv_bfloat16*>(X) + m0 * H, H, ml, H, BK, BM))) return rc;
+        EpiParams f = e;
+        f.M = ml;
+        f.out = dG + m0 * I;
+        f.out2 = dU + m0 * I;
+        f.src = static_cast<const __nv_bfloat16*>(dH) + m0 * I;
+        if ((rc = launch_gemm<0, 0, EPI_SWIGLU_BWD, 1>(mX_k, mG_k, ml, ntile_n * BN, static_cast<int>(H), f, st, 0,
+                                                       &mX_k, &mU_k)))
+            return rc;
+    }
     // 2. dX = dG W_g + dU W_u (K = 2I: k-blocks of the second product follow those of the first);
     // 3. dW_g = dG^T X, dW_u = dU^T X (both operands MN-major, K = T)
     return grads_from_dgdu(X, Wg, Wu, dG, dU, dX, dWg, dWu, T, H, I, d_err, st);

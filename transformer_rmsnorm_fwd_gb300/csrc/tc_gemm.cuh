@@ -1152,6 +1152,17 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_fn();
 
+// Rows of a K-major A operand [M, K] bf16 per launch, for a GEMM whose tiles
+// sweep all of B over the same A rows: those rows must stay in L2 meanwhile.
+// At most 32 MiB of them (a multiple of 256 rows, at least 256, at most M):
+// measured on the 129 MB L2, 33.5 MB of reused rows stayed resident beside
+// streamed operands and 67 MB did not (one launch over 67 MB of X rows read
+// 12.7x its operand bytes from DRAM).  At K = 4096: 4096 rows.
+inline int64_t rows_in_l2(int64_t K, int64_t M) {
+    const int64_t r = (int64_t{32} << 20) / (2 * K) / 256 * 256;
+    return std::max<int64_t>(1, std::min(M, std::max<int64_t>(256, r)));
+}
+
 // 2-D bf16 map over a row-major matrix [outer, inner] with row stride
 // `ld` elements, box (box_inner x box_outer), 128-byte swizzle, zero fill.
 int make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_inner,
