@@ -137,3 +137,25 @@ def test_rmsnorm_qkv_rope_empty_and_errors(cuda_lib):
     with pytest.raises(cuda_lib.LigerError) as err:
         cuda_lib.liger_rmsnorm_qkv_rope_fwd(xf, wn, W, W, W, e, e, e, ws, 1, 4, 1, 1, 64)
     assert err.value.status == -3
+
+
+def test_rmsnorm_qkv_rope_caller_tables_without_positions_over_batches(cuda_lib):
+    """Caller cos/sin tables and no positions, two sequences of 4500 tokens at
+    hidden 2048: every token indexes the tables by its position in its own
+    sequence (token % seq), across the batch boundary and beyond 8192 rows;
+    sampled tokens against the oracle."""
+    B, S, H, Hq, Hk, D, n_tab = 2, 4500, 2048, 1, 1, 64, 4500
+    x, w, Wq, Wk, Wv, b = _inputs(66, B, S, H, Hq, Hk, D)
+    p = np.arange(n_tab, dtype=np.float64)[:, None] / 2.0
+    ang = p * 1e4 ** (-2.0 * np.arange(D // 2)[None, :] / D)
+    ct, st = np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+    q, k, v, rstd, _ = _run(cuda_lib, x, w, Wq, Wk, Wv, b, B, S, Hq, Hk, D, 1e-6, 1e4, cos_tab=ct, sin_tab=st)
+    rows = np.array([0, 4499, 4500, 8191, 8192, 8999])
+    pos = (rows % S).astype(np.int32).reshape(1, -1)
+    want = oracle.rmsnorm_qkv_rope(x[rows], w, Wq, Wk, Wv, 1, len(rows), Hq, Hk, 1e-6, 1e4, *b, pos=pos,
+                                   cos_tab=ct, sin_tab=st)
+    flat = lambda t: t.reshape(B * S, *t.shape[2:])[rows]
+    assert oracle.rel_err(host(flat(q)), want[0][0]) <= TOL["bf16"]
+    assert oracle.rel_err(host(flat(k)), want[1][0]) <= TOL["bf16"]
+    assert oracle.rel_err(host(flat(v)), want[2][0]) <= TOL["bf16"]
+    assert oracle.rel_err(host(rstd[rows]), want[3]) <= TOL["f32"]
