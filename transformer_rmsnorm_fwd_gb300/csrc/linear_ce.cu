@@ -616,9 +616,10 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             }
             d.M = V;
             d.N = H;
-            // groups of 8 column blocks of X_c (33.5 MB at hidden 4096) stay in L2 through the
-            // vocabulary sweep; n fastest would touch all of X_c in every wave
-            d.raster = RASTER_N_GROUPS;
+            // n fastest touches all of X_c in every wave: fine while X_c stays in L2 (up to
+            // 32 MiB), above that groups of 8 column blocks of it do (at the price of reading
+            // each D block once per group)
+            d.raster = static_cast<int64_t>(cl) * H * 2 > (int64_t{32} << 20) ? RASTER_N_GROUPS : RASTER_N_FASTEST;
             d.hint_a = HINT_NORMAL;        // D^T (evict-first measured ~1 % slower with CTA-pair tiles)
             d.hint_b = HINT_EVICT_LAST;    // X_c: reused by every vocab row block, keep in L2
             d.labels = nullptr;

@@ -142,8 +142,9 @@ int grads_from_dgdu(const void* X, const void* Wg, const void* Wu, const __nv_bf
     w.N = static_cast<int>(H);
     w.ldo = H;
     w.out_write = 1;
-    // groups of 8 column blocks of X (33.5 MB at T = 8192) stay in L2 through the sweep over I
-    w.raster = RASTER_N_GROUPS;
+    // n fastest touches all of X in every wave: fine while X stays in L2 (up to 32 MiB), above
+    // that groups of 8 column blocks of it do (each dG / dU block is then read once per group)
+    w.raster = T * H * 2 > (int64_t{32} << 20) ? RASTER_N_GROUPS : RASTER_N_FASTEST;
     w.hint_a = HINT_EVICT_FIRST;
     w.hint_b = HINT_EVICT_LAST;   // X: reused by every row block
     w.out = static_cast<__nv_bfloat16*>(dWg);
