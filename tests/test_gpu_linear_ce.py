@@ -315,22 +315,24 @@ def test_linear_ce_labels_at_tile_edges(cuda_lib, V):
     _check_full(X, W, lab, "bf16", float(l2.item()), dX2, dW2, lse2)
 
 
-def test_linear_ce_logits_in_l2_sized_launches(cuda_lib):
+@pytest.mark.parametrize("T,big,small", [(16384, 16384, 8192), (12000, 16384, 4000)])
+def test_linear_ce_logits_in_l2_sized_launches(cuda_lib, T, big, small):
     """The logits GEMM runs over at most 32 MiB of X rows per launch: at hidden
-    2048 a 16384-row chunk takes two launches of 8192 rows, an 8192-row chunk
-    one.  lse, the loss and dX are bit-identical between the two chunkings,
-    and sampled rows match the oracle."""
-    T, H, V = 16384, 2048, 1000
+    2048 a 16384-row chunk takes two launches of 8192 rows, a 12000-row chunk a
+    full and a ragged one (8192 + 3808), chunks of 8192 or 4000 rows one each.
+    lse, the loss and dX are bit-identical between the two chunkings, and
+    sampled rows match the oracle."""
+    H, V = 2048, 1000
     X = datagen.normal(44, "lsX", (T, H), "bf16")
     W = datagen.normal(44, "lsW", (V, H), "bf16", 0.0, 0.02)
     lab = datagen.labels(44, "lsl", T, V, 0.1)
-    a = _run(cuda_lib, X, W, lab, "bf16", chunk=16384)
-    b = _run(cuda_lib, X, W, lab, "bf16", chunk=8192)
+    a = _run(cuda_lib, X, W, lab, "bf16", chunk=big)
+    b = _run(cuda_lib, X, W, lab, "bf16", chunk=small)
     assert a[0] == b[0]
     assert np.array_equal(a[3], b[3])
     assert np.array_equal(bits(a[1]), bits(b[1]))
     assert oracle.rel_err(host(a[2]), host(b[2])) <= 2e-2
-    rows = np.array([0, 4095, 8191, 8192, 12288, 16383])
+    rows = np.array([0, 4095, 8191, 8192, 11999, T - 1])
     o = oracle.linear_ce_rows(X, W, lab, rows)
     hdX = host(a[1])
     for i, r in enumerate(rows):

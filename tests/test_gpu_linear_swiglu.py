@@ -140,3 +140,31 @@ def test_fused_linear_swiglu_saved_llama_mlp_sampled(cuda_lib):
     _, odWg, odWu = oracle.linear_swiglu_bwd(X, Wg[cols], Wu[cols], dH[:, cols])
     assert oracle.rel_err(host(dWg)[cols], odWg) <= 2e-2
     assert oracle.rel_err(host(dWu)[cols], odWu) <= 2e-2
+
+
+def test_fused_linear_swiglu_l2_sized_launches(cuda_lib):
+    """The forward and the backward's recompute GEMM run over at most 32 MiB of
+    X rows per launch (8192 rows at hidden 2048): T = 9000 takes a full and a
+    ragged launch; the dW GEMMs take the grouped tile order (X above 32 MiB).
+    Forward, backward and the saving pair against the oracle."""
+    T, H, I = 9000, 2048, 64
+    X = datagen.normal(54, "lx", (T, H), "bf16")
+    Wg = datagen.normal(54, "lg", (I, H), "bf16", 0.0, 0.02)
+    Wu = datagen.normal(54, "lu", (I, H), "bf16", 0.0, 0.02)
+    dH = datagen.normal(54, "ld", (T, I), "bf16")
+    out, dX, dWg, dWu = _run(cuda_lib, X, Wg, Wu, dH)
+    assert oracle.rel_err(host(out), oracle.linear_swiglu_fwd(X, Wg, Wu)) <= 2e-2
+    odX, odWg, odWu = oracle.linear_swiglu_bwd(X, Wg, Wu, dH)
+    assert oracle.rel_err(host(dX), odX) <= 2e-2
+    assert oracle.rel_err(host(dWg), odWg) <= 2e-2
+    assert oracle.rel_err(host(dWu), odWu) <= 2e-2
+    # the saving pair: h as above; its backward is the exact backward from the g, u it
+    # stored (bf16: one rounding more than the recompute path, which over 18 M elements
+    # reaches 2.5 % of rms against the oracle's unrounded g, u)
+    out2, g, u, dX2, dWg2, dWu2 = _run_saved(cuda_lib, X, Wg, Wu, dH)
+    assert np.array_equal(host(out2), host(out))
+    dGr, dUr = oracle.swiglu_bwd(datagen.to_f64(dH, "bf16"), host(g), host(u))
+    xf, gf, uf = (datagen.to_f64(a, "bf16") for a in (X, Wg, Wu))
+    assert oracle.rel_err(host(dX2), dGr @ gf + dUr @ uf) <= 2e-2
+    assert oracle.rel_err(host(dWg2), dGr.T @ xf) <= 2e-2
+    assert oracle.rel_err(host(dWu2), dUr.T @ xf) <= 2e-2
