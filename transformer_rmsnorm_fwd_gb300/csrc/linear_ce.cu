@@ -737,8 +737,10 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         // a. D_c = scale * softmax part, from the recomputed logits and lse
         e.M = T;
         e.N = vl;
-        e.raster = RASTER_N_FASTEST;
-        e.hint_a = HINT_EVICT_FIRST;   // X: streamed once per chunk
+        // groups of 8 column blocks of W_c (16 MB) stay in L2 while X streams past once per
+        // group (n fastest needs all 67 MB of W_c in every wave); X reused within a wave
+        e.raster = RASTER_N_GROUPS;
+        e.hint_a = HINT_NORMAL;
         e.hint_b = HINT_EVICT_LAST;    // W_c: reused by every token block
         e.lse = lse;
         e.corr_scale = scale;
