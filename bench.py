@@ -415,7 +415,10 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.proc = None
         self.idx = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # the raw samples go to $BENCH_CLOCKS_DIR (default: the system temporary directory)
+        import tempfile
+        self.path = os.path.join(os.environ.get("BENCH_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
