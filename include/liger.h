@@ -41,6 +41,9 @@
  *     (liger_rmsnorm_bwd_noalloc shares its scratch array: see there).  The
  *     library's own per-device state (kernel attributes, occupancy, the
  *     tensor-map encoder) is set up on first use and safe to race.
+ *   - After a first call on a device, every entry point except the two
+ *     linear cross-entropies (which wait for their label scan) can be
+ *     captured in a CUDA graph.
  */
 #ifndef LIGER_H
 #define LIGER_H
