@@ -41,9 +41,10 @@
  *     (liger_rmsnorm_bwd_noalloc shares its scratch array: see there).  The
  *     library's own per-device state (kernel attributes, occupancy, the
  *     tensor-map encoder) is set up on first use and safe to race.
- *   - After a first call on a device, every entry point except the two
- *     linear cross-entropies (which wait for their label scan) can be
- *     captured in a CUDA graph.
+ *   - After a first call on a device, every entry point except
+ *     liger_linear_ce_fwd_bwd and liger_linear_ce_two_pass_fwd_bwd (which
+ *     wait for their label scan) can be captured in a CUDA graph; their
+ *     _async forms do not wait.
  */
 #ifndef LIGER_H
 #define LIGER_H
@@ -357,6 +358,29 @@ int liger_linear_ce_two_pass_fwd_bwd(const void* X, const void* W, const int64_t
                                      int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
                                      void* dX, void* dW, void* ws, size_t ws_bytes, int64_t vchunk, int dtype,
                                      void* stream);
+
+/* The two linear cross-entropies without their host wait, for callers that
+ * capture a training step in a CUDA graph.  Same arguments, workspace and
+ * results as liger_linear_ce_fwd_bwd and liger_linear_ce_two_pass_fwd_bwd,
+ * except:
+ *   - the call queues work only (no stream synchronisation), so it can be
+ *     captured once the device has seen one call of either kind;
+ *   - labels are checked on the device: a label outside [0, V) that is not
+ *     ignore_index does not make the call fail; it is treated as ignored (not
+ *     counted in n_valid, its lse, loss term and gradient rows 0) and the
+ *     loss is NaN, so the error shows in the result.  Argument errors are
+ *     still returned before anything is queued;
+ *   - the count n_valid and the gradient scale are formed on the device.
+ * Results are bit-identical to the waiting variant whenever every label is
+ * valid. */
+int liger_linear_ce_fwd_bwd_async(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H,
+                                  int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
+                                  void* dX, void* dW, void* ws, size_t ws_bytes, int64_t chunk, int dtype,
+                                  void* stream);
+int liger_linear_ce_two_pass_fwd_bwd_async(const void* X, const void* W, const int64_t* labels, int64_t T,
+                                           int64_t H, int64_t V, int64_t ignore_index, int reduction,
+                                           float grad_scale, float* loss, void* dX, void* dW, void* ws,
+                                           size_t ws_bytes, int64_t vchunk, int dtype, void* stream);
 
 #ifdef __cplusplus
 }

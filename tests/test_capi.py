@@ -20,7 +20,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = _native.header_functions()
-    assert len(names) == 22
+    assert len(names) == 24
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_native.SIGNATURES)
@@ -69,6 +69,12 @@ def test_alignment_and_workspace_errors(lib):
                                        None) == -6
     assert lib.liger_linear_ce_fwd_bwd(ok, ok, ok, 100, 64, 1000, -100, 0, 1.0, ok, None, None, ctypes.c_void_p(0x1010),
                                        n, 0, 1, None) == -6   # not 256-byte aligned
+    # the forms without the host wait check their arguments the same way, before queueing anything
+    for fn in (lib.liger_linear_ce_fwd_bwd_async, lib.liger_linear_ce_two_pass_fwd_bwd_async):
+        assert fn(None, None, None, 4, 64, 256, -100, 0, 1.0, None, None, None, None, 0, 0, 1, None) == -1
+        assert fn(ok, ok, ok, 4, 64, 256, -100, 2, 1.0, ok, None, None, ok, 1 << 30, 0, 1, None) == -2
+        assert fn(ok, ok, ok, 100, 64, 1000, -100, 0, 1.0, ok, None, None, ok, 256, 0, 1, None) == -6
+        assert fn(ok, ok, ok, 100, 64, 1000, -100, 0, 1.0, ok, None, None, ok, 1 << 30, 0, 7, None) == -3
 
 
 def test_workspace_sizes(lib):

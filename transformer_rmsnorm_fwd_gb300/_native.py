@@ -56,6 +56,10 @@ SIGNATURES = {
     "liger_linear_ce_workspace": ([_I64, _I64, _I64, _I64, _INT], _SZ),
     "liger_linear_ce_fwd_bwd": ([_P, _P, _P, _I64, _I64, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _I64, _INT, _P],
                                 _INT),
+    "liger_linear_ce_fwd_bwd_async": ([_P, _P, _P, _I64, _I64, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ, _I64, _INT,
+                                       _P], _INT),
+    "liger_linear_ce_two_pass_fwd_bwd_async": ([_P, _P, _P, _I64, _I64, _I64, _I64, _INT, _F, _P, _P, _P, _P, _SZ,
+                                                _I64, _INT, _P], _INT),
 }
 
 
@@ -293,14 +297,17 @@ def liger_linear_ce_workspace(T: int, H: int, V: int, chunk: int = 0, dtype: int
 
 
 def liger_linear_ce_fwd_bwd(X, W, labels, loss, dX, dW, ws, ignore_index: int = -100, reduction: str = "mean",
-                            grad_scale: float = 1.0, chunk: int = 0):
+                            grad_scale: float = 1.0, chunk: int = 0, wait: bool = True):
+    """Fused linear cross-entropy (see liger.h); wait=False calls the _async form
+    (no host wait: capturable in a CUDA graph; a bad label makes the loss NaN)."""
     _dense(X, W, labels, loss, dX, dW, ws)
     T, H = X.shape
     V = W.shape[0]
     nbytes = ws.numel() * ws.element_size() if ws is not None else 0
-    _check(load().liger_linear_ce_fwd_bwd(_ptr(X), _ptr(W), _ptr(labels), T, H, V, int(ignore_index),
-                                          0 if reduction == "mean" else 1, float(grad_scale), _ptr(loss), _ptr(dX),
-                                          _ptr(dW), _ptr(ws), nbytes, int(chunk), _dtype_code(X), _stream()))
+    fn = load().liger_linear_ce_fwd_bwd if wait else load().liger_linear_ce_fwd_bwd_async
+    _check(fn(_ptr(X), _ptr(W), _ptr(labels), T, H, V, int(ignore_index), 0 if reduction == "mean" else 1,
+              float(grad_scale), _ptr(loss), _ptr(dX), _ptr(dW), _ptr(ws), nbytes, int(chunk), _dtype_code(X),
+              _stream()))
     return loss, dX, dW
 
 
@@ -309,14 +316,16 @@ def liger_linear_ce_two_pass_workspace(T: int, H: int, V: int, vchunk: int = 0) 
 
 
 def liger_linear_ce_two_pass_fwd_bwd(X, W, labels, loss, dX, dW, ws, ignore_index: int = -100,
-                                     reduction: str = "mean", grad_scale: float = 1.0, vchunk: int = 0):
-    """Two-pass, vocabulary-chunked fused linear cross-entropy (see liger.h)."""
+                                     reduction: str = "mean", grad_scale: float = 1.0, vchunk: int = 0,
+                                     wait: bool = True):
+    """Two-pass, vocabulary-chunked fused linear cross-entropy (see liger.h);
+    wait=False calls the _async form."""
     _dense(X, W, labels, loss, dX, dW, ws)
     T, H = X.shape
     V = W.shape[0]
     nbytes = ws.numel() * ws.element_size() if ws is not None else 0
-    _check(load().liger_linear_ce_two_pass_fwd_bwd(_ptr(X), _ptr(W), _ptr(labels), T, H, V, int(ignore_index),
-                                                   0 if reduction == "mean" else 1, float(grad_scale), _ptr(loss),
-                                                   _ptr(dX), _ptr(dW), _ptr(ws), nbytes, int(vchunk), _dtype_code(X),
-                                                   _stream()))
+    fn = load().liger_linear_ce_two_pass_fwd_bwd if wait else load().liger_linear_ce_two_pass_fwd_bwd_async
+    _check(fn(_ptr(X), _ptr(W), _ptr(labels), T, H, V, int(ignore_index), 0 if reduction == "mean" else 1,
+              float(grad_scale), _ptr(loss), _ptr(dX), _ptr(dW), _ptr(ws), nbytes, int(vchunk), _dtype_code(X),
+              _stream()))
     return loss, dX, dW

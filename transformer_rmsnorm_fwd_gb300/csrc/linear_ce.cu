@@ -61,13 +61,14 @@ struct Hdr {
     unsigned long long n_valid;
     int bad;
     int err;
+    float scale;   // the gradient scale, when it is formed on the device (no host wait)
 };
 
 struct Layout {
     bool tc;
     int64_t C, ldp, nvt, nchunks;
     int seg;   // label-sort segment: the chunk (C <= 8192, indices relative to it) or 8192 tokens (absolute)
-    size_t lse, lossrow, zlab, hdr, keys, lstart, part, scr, acc, dxacc, total;
+    size_t lse, lossrow, zlab, hdr, labs, keys, lstart, part, scr, acc, dxacc, total;
 };
 
 inline size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -98,6 +99,8 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     L.lossrow = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
     L.zlab = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
     L.hdr = o; o = up256(o + sizeof(Hdr));
+    // the labels with bad ones replaced by ignore_index (the entry points that do not wait)
+    L.labs = o; o = up256(o + sizeof(int64_t) * static_cast<size_t>(T));
     // every chunk's sorted label keys and start table, made in one pass before the chunks
     L.keys = o; o = up256(o + (L.tc ? sizeof(unsigned long long) * static_cast<size_t>(std::max<int64_t>(T, 1)) : 0));
     L.lstart = o; o = up256(o + (L.tc ? sizeof(int) * static_cast<size_t>(ceil_div(std::max<int64_t>(T, 1), L.seg) * (V + 1)) : 0));
@@ -112,15 +115,22 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
 }
 
 // ---------------------------------------------------------------- kernels
-__global__ void label_scan(const int64_t* __restrict__ labels, int64_t T, int64_t V, int64_t ignore, Hdr* hdr) {
+// Counts the labels that are not ignore_index and flags any outside [0, V).  With
+// lab_out set, also writes the labels with every bad one replaced by ignore_index
+// (and not counted), so that no later kernel indexes with it.
+__global__ void label_scan(const int64_t* __restrict__ labels, int64_t T, int64_t V, int64_t ignore, Hdr* hdr,
+                           int64_t* __restrict__ lab_out) {
     unsigned long long cnt = 0;
     int bad = 0;
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t y = labels[t];
-        if (y == ignore) continue;
-        ++cnt;
-        if (y < 0 || y >= V) bad = 1;
+        int64_t y = labels[t];
+        if (y != ignore && (y < 0 || y >= V)) {
+            bad = 1;
+            if (lab_out != nullptr) y = ignore;
+        }
+        if (lab_out != nullptr) lab_out[t] = y;
+        if (y != ignore) ++cnt;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -131,6 +141,15 @@ __global__ void label_scan(const int64_t* __restrict__ labels, int64_t T, int64_
         if (cnt) atomicAdd(&hdr->n_valid, cnt);
         if (bad) atomicOr(&hdr->bad, 1);
     }
+}
+
+// The gradient scale from the device-side count: grad_scale / n_valid (mean; 0 when
+// nothing is valid) or grad_scale (sum)
+__global__ void ce_scale(Hdr* hdr, int reduction, float grad_scale) {
+    const unsigned long long n = hdr->n_valid;
+    hdr->scale = reduction == 0 ? (n > 0 ? static_cast<float>(static_cast<double>(grad_scale) / static_cast<double>(n))
+                                         : 0.0f)
+                                : grad_scale;
 }
 
 template <int NT>
@@ -234,8 +253,9 @@ constexpr int kRowThreads = 256;
 __global__ void __launch_bounds__(kRowThreads) dlogits_bf16(const int64_t* __restrict__ labels, int64_t ignore,
                                                             const float2* __restrict__ part, int nvt,
                                                             const float* __restrict__ zlab, __nv_bfloat16* P,
-                                                            int64_t ldp, int V, float scale, float* __restrict__ lse,
-                                                            float* __restrict__ lossrow) {
+                                                            int64_t ldp, int V, float scale,
+                                                            const float* __restrict__ scale_dev,
+                                                            float* __restrict__ lse, float* __restrict__ lossrow) {
     extern __shared__ float fac[];   // [nvt]
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
@@ -263,7 +283,8 @@ __global__ void __launch_bounds__(kRowThreads) dlogits_bf16(const int64_t* __res
     }
     s = block_reduce<kRowThreads>(s, false, red);
     const float l = m + logf(s);
-    for (int j = threadIdx.x; j < nvt; j += kRowThreads) fac[j] = scale * expf(pr[j].x - l);
+    const float sc = scale_dev != nullptr ? *scale_dev : scale;   // scale_dev: formed on the device
+    for (int j = threadIdx.x; j < nvt; j += kRowThreads) fac[j] = sc * expf(pr[j].x - l);
     if (threadIdx.x == 0) {
         lse[row] = l;
         lossrow[row] = l - zlab[row];
@@ -284,6 +305,7 @@ __global__ void __launch_bounds__(kRowThreads) dlogits_bf16(const int64_t* __res
 // fp32 path: z row -> lse, loss term, D (fp32, in place).
 __global__ void __launch_bounds__(kRowThreads) dlogits_f32(const int64_t* __restrict__ labels, int64_t ignore,
                                                            float* Z, int64_t ldz, int V, float scale,
+                                                           const float* __restrict__ scale_dev,
                                                            float* __restrict__ lse, float* __restrict__ lossrow) {
     __shared__ float red[32];
     const int64_t row = blockIdx.x;
@@ -310,13 +332,16 @@ __global__ void __launch_bounds__(kRowThreads) dlogits_f32(const int64_t* __rest
         lse[row] = l;
         lossrow[row] = l - zy;
     }
-    for (int v = threadIdx.x; v < V; v += kRowThreads) z[v] = scale * (expf(z[v] - l) - (v == y ? 1.0f : 0.0f));
+    const float sc = scale_dev != nullptr ? *scale_dev : scale;   // scale_dev: formed on the device
+    for (int v = threadIdx.x; v < V; v += kRowThreads) z[v] = sc * (expf(z[v] - l) - (v == y ? 1.0f : 0.0f));
 }
 
 // loss = sum of the row terms (fixed order, fp64) / n_valid; NaN if a
 // tensor-core kernel recorded an error.
+// dev_denom 0: divide by denom; 1 (mean) / 2 (sum): the denominator from the device-side
+// count, and NaN when a label was bad
 __global__ void __launch_bounds__(1024) loss_final(const float* __restrict__ lossrow, int64_t T, double denom,
-                                                   const Hdr* hdr, float* loss) {
+                                                   const Hdr* hdr, float* loss, int dev_denom) {
     __shared__ double red[32];
     double s = 0.0;
     for (int64_t t = threadIdx.x; t < T; t += 1024) s += static_cast<double>(lossrow[t]);
@@ -327,8 +352,9 @@ __global__ void __launch_bounds__(1024) loss_final(const float* __restrict__ los
     if (threadIdx.x == 0) {
         double tot = 0.0;
         for (int i = 0; i < 32; ++i) tot += red[i];
+        if (dev_denom != 0) denom = dev_denom == 1 ? static_cast<double>(hdr->n_valid) : 1.0;
         float r = denom > 0.0 ? static_cast<float>(tot / denom) : 0.0f;
-        if (hdr->err != 0) r = __int_as_float(0x7fc00000);
+        if (hdr->err != 0 || (dev_denom != 0 && hdr->bad != 0)) r = __int_as_float(0x7fc00000);
         *loss = r;
     }
 }
@@ -413,6 +439,7 @@ struct Args {
     uint8_t* ws;
     int dtype;
     cudaStream_t st;
+    const float* scale_dev;   // non-null: the gradient scale is read from the device (no host wait)
 };
 
 template <typename TI>
@@ -434,7 +461,8 @@ int run_simt(const Args& a, const Layout& L, float scale) {
         const bool first = c == 0, last = c == L.nchunks - 1;
         if ((rc = simt<TI, TI, TI, 0>(cl, V, H, X + t0 * H, H, 1, W, 1, H, Z, (TI*)nullptr, V, nullptr, 0, a.st)))
             return rc;
-        dlogits_f32<<<cl, kRowThreads, 0, a.st>>>(a.labels + t0, a.ignore, Z, V, V, scale, lse + t0, lossrow + t0);
+        dlogits_f32<<<cl, kRowThreads, 0, a.st>>>(a.labels + t0, a.ignore, Z, V, V, scale, a.scale_dev, lse + t0,
+                                                  lossrow + t0);
         if ((rc = check_launch("dlogits_f32"))) return rc;
         if (dX && (rc = simt<float, TI, TI, 1>(cl, H, V, Z, V, 1, W, H, 1, nullptr, dX + t0 * H, H, a.labels + t0,
                                                a.ignore, a.st)))
@@ -549,7 +577,8 @@ int run_tc(const Args& a, const Layout& L, float scale) {
         if ((rc = launch_logits(Xc, cl, H, V, mW_k, e, L.ldp, L.nvt, a.st))) return rc;
         // 2. lse, loss terms, P -> D in place
         dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
-                                                          zlab + t0, P, L.ldp, V, scale, lse + t0, lossrow + t0);
+                                                          zlab + t0, P, L.ldp, V, scale, a.scale_dev, lse + t0,
+                                                          lossrow + t0);
         if ((rc = check_launch("dlogits_bf16"))) return rc;
         // 3. dX_c = D W, minus scale * W[label] in fp32
         if (a.dX && dx_slab(V) < V) {
@@ -581,6 +610,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
                 d.corr_src = s_last ? W : nullptr;
                 d.ld_corr = H;
                 d.corr_scale = scale;
+                d.scale_ptr = a.scale_dev;
                 if ((rc = launch_gemm<0, 1, EPI_ACCUM, 1>(mDs_k, mWs_mn, cl, H, vl, d, a.st))) return rc;
             }
         } else if (a.dX) {
@@ -595,6 +625,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             d.corr_src = W;
             d.ld_corr = H;
             d.corr_scale = scale;
+            d.scale_ptr = a.scale_dev;
             if ((rc = launch_gemm<0, 1, EPI_STORE, 1>(mD_k, mW_mn, cl, H, V, d, a.st))) return rc;
         }
         // 4. dW (+)= D^T X_c, minus scale * X_t in fp32 for each token t labelled with the row
@@ -602,6 +633,7 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             EpiParams d = e;
             d.ld_corr = H;
             d.corr_scale = scale;
+            d.scale_ptr = a.scale_dev;
             d.nkeys = cl;
             if (rel) {
                 d.corr_src = Xc;
@@ -649,7 +681,7 @@ constexpr int64_t kAutoVChunk = 8192;
 
 struct Layout2 {
     int64_t C, nvt, Vc, ldc, nvchunks, nseg;
-    size_t lse, lossrow, zlab, hdr, keys, lstart, part, dscr, acc, total;
+    size_t lse, lossrow, zlab, hdr, labs, keys, lstart, part, dscr, acc, total;
 };
 
 Layout2 layout2(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
@@ -665,6 +697,8 @@ Layout2 layout2(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
     L.lossrow = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
     L.zlab = o; o = up256(o + sizeof(float) * static_cast<size_t>(T));
     L.hdr = o; o = up256(o + sizeof(Hdr));
+    // the labels with bad ones replaced by ignore_index (the entry points that do not wait)
+    L.labs = o; o = up256(o + sizeof(int64_t) * static_cast<size_t>(T));
     L.keys = o; o = up256(o + sizeof(unsigned long long) * static_cast<size_t>(T));
     L.lstart = o; o = up256(o + sizeof(int) * static_cast<size_t>(L.nseg * (V + 1)));
     L.part = o; o = up256(o + sizeof(float2) * static_cast<size_t>(L.C * L.nvt));
@@ -711,7 +745,8 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         e.zlab = zlab + t0;
         if ((rc = launch_logits(X + t0 * H, cl, H, V, mW_k, e, 0, L.nvt, a.st))) return rc;
         dlogits_bf16<<<cl, kRowThreads, fac_smem, a.st>>>(a.labels + t0, a.ignore, part, static_cast<int>(L.nvt),
-                                                          zlab + t0, nullptr, 0, V, scale, lse + t0, lossrow + t0);
+                                                          zlab + t0, nullptr, 0, V, scale, a.scale_dev, lse + t0,
+                                                          lossrow + t0);
         if ((rc = check_launch("dlogits_bf16"))) return rc;
     }
     // label keys of all tokens, sorted in segments of kMaxSortKeys, one start table per segment
@@ -744,6 +779,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
         e.hint_b = HINT_EVICT_LAST;    // W_c: reused by every token block
         e.lse = lse;
         e.corr_scale = scale;
+        e.scale_ptr = a.scale_dev;
         e.out = D;
         e.ldo = L.ldc;
         if ((rc = launch_gemm<0, 0, EPI_SOFTMAX, 1>(mX_all, mWc_k, T, vl, H, e, a.st))) return rc;
@@ -756,6 +792,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
             d.corr_src = c == 0 ? W : nullptr;
             d.ld_corr = H;
             d.corr_scale = scale;
+            d.scale_ptr = a.scale_dev;
             d.M = T;
             d.N = H;
             d.raster = RASTER_N_GROUPS;
@@ -776,6 +813,7 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
             d.corr_src = X;
             d.ld_corr = H;
             d.corr_scale = scale;
+            d.scale_ptr = a.scale_dev;
             d.keys = keys;
             d.nkeys = T;
             d.lstart = lstart + c0;
@@ -807,16 +845,19 @@ namespace liger {
 namespace {
 
 struct CommonLayout {
-    size_t lse, lossrow, hdr, total;
+    size_t lse, lossrow, hdr, labs, total;
 };
 
 // Shared tail of both entry points: pointer and workspace checks, the label
 // scan (bad labels -> LIGER_ERR_LABEL before any other work), the all-ignored
 // case, the gradient scale, the variant's GEMMs, the final loss.
+// sync = false: no host wait (capturable in a CUDA graph); bad labels are replaced by
+// ignore_index in a workspace copy, the scale and the mean's count stay on the device,
+// and the loss is NaN if a label was bad.
 template <typename Run>
 int ce_entry(const char* who, const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H, int64_t V,
              int64_t ignore_index, int reduction, float grad_scale, float* loss, void* dX, void* dW, void* ws,
-             size_t ws_bytes, int dtype, void* stream, const CommonLayout& CL, Run run) {
+             size_t ws_bytes, int dtype, void* stream, const CommonLayout& CL, Run run, bool sync = true) {
     if (!X || !W || !loss || (T > 0 && !labels)) return fail(LIGER_ERR_NULL, "%s: X, W, labels, loss required", who);
     if (!aligned16(X) || !aligned16(W) || (dX && !aligned16(dX)) || (dW && !aligned16(dW)) ||
         (reinterpret_cast<uintptr_t>(loss) & 3) || (reinterpret_cast<uintptr_t>(labels) & 7))
@@ -828,10 +869,23 @@ int ce_entry(const char* who, const void* X, const void* W, const int64_t* label
     uint8_t* w8 = static_cast<uint8_t*>(ws);
     Hdr* hdr = reinterpret_cast<Hdr*>(w8 + CL.hdr);
     if (cudaMemsetAsync(hdr, 0, sizeof(Hdr), st) != cudaSuccess) return check_launch("linear_ce memset");
+    if (!sync && T > 0) {
+        int64_t* labs = reinterpret_cast<int64_t*>(w8 + CL.labs);
+        const int grid = static_cast<int>(std::min<int64_t>(ceil_div(T, 256), 4 * sm_count()));
+        label_scan<<<grid, 256, 0, st>>>(labels, T, V, ignore_index, hdr, labs);
+        if (int rc = check_launch("label_scan")) return rc;
+        ce_scale<<<1, 1, 0, st>>>(hdr, reduction, grad_scale);
+        if (int rc = check_launch("ce_scale")) return rc;
+        Args a{X, W, labs, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st, &hdr->scale};
+        if (int rc = run(a, 0.0f)) return rc;
+        loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + CL.lossrow), T, 0.0, hdr, loss,
+                                       reduction == 0 ? 1 : 2);
+        return check_launch("loss_final");
+    }
     Hdr h{};
     if (T > 0) {
         const int grid = static_cast<int>(std::min<int64_t>(ceil_div(T, 256), 4 * sm_count()));
-        label_scan<<<grid, 256, 0, st>>>(labels, T, V, ignore_index, hdr);
+        label_scan<<<grid, 256, 0, st>>>(labels, T, V, ignore_index, hdr, nullptr);
         if (int rc = check_launch("label_scan")) return rc;
         if (cudaMemcpyAsync(&h, hdr, sizeof(Hdr), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
             cudaStreamSynchronize(st) != cudaSuccess)
@@ -853,20 +907,20 @@ int ce_entry(const char* who, const void* X, const void* W, const int64_t* label
     }
     const float scale = reduction == 0 ? static_cast<float>(static_cast<double>(grad_scale) / static_cast<double>(n_valid))
                                        : grad_scale;
-    Args a{X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st};
+    Args a{X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st, nullptr};
     if (int rc = run(a, scale)) return rc;
     const double denom = reduction == 0 ? static_cast<double>(n_valid) : 1.0;
-    loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + CL.lossrow), T, denom, hdr, loss);
+    loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + CL.lossrow), T, denom, hdr, loss, 0);
     return check_launch("loss_final");
 }
 
 }  // namespace
 }  // namespace liger
 
-extern "C" int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H,
-                                       int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
-                                       void* dX, void* dW, void* ws, size_t ws_bytes, int64_t chunk, int dtype,
-                                       void* stream) {
+namespace {
+int linear_ce_impl(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H, int64_t V,
+                   int64_t ignore_index, int reduction, float grad_scale, float* loss, void* dX, void* dW, void* ws,
+                   size_t ws_bytes, int64_t chunk, int dtype, void* stream, bool sync) {
     clear_error();
     if (dtype != LIGER_F32 && dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "linear_ce: dtype %d", dtype);
     if (T < 0 || H <= 0 || V <= 0 || chunk < 0 || H > (1 << 30) || V > (1 << 30) || T > (int64_t{1} << 31) ||
@@ -874,13 +928,33 @@ extern "C" int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64
         return fail(LIGER_ERR_SHAPE, "linear_ce: T=%lld H=%lld V=%lld chunk=%lld reduction=%d", (long long)T,
                     (long long)H, (long long)V, (long long)chunk, reduction);
     const Layout L = layout(T, H, V, chunk, dtype);
-    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.total};
-    return ce_entry("linear_ce", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws,
-                    ws_bytes, dtype, stream, CL, [&](const Args& a, float scale) {
-                        if (L.tc) return run_tc(a, L, scale);
-                        if (dtype == LIGER_F32) return run_simt<float>(a, L, scale);
-                        return run_simt<__nv_bfloat16>(a, L, scale);
-                    });
+    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.labs, L.total};
+    return ce_entry(
+        "linear_ce", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws, ws_bytes, dtype,
+        stream, CL,
+        [&](const Args& a, float scale) {
+            if (L.tc) return run_tc(a, L, scale);
+            if (dtype == LIGER_F32) return run_simt<float>(a, L, scale);
+            return run_simt<__nv_bfloat16>(a, L, scale);
+        },
+        sync);
+}
+}  // namespace
+
+extern "C" int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H,
+                                       int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
+                                       void* dX, void* dW, void* ws, size_t ws_bytes, int64_t chunk, int dtype,
+                                       void* stream) {
+    return linear_ce_impl(X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws, ws_bytes,
+                          chunk, dtype, stream, true);
+}
+
+extern "C" int liger_linear_ce_fwd_bwd_async(const void* X, const void* W, const int64_t* labels, int64_t T,
+                                             int64_t H, int64_t V, int64_t ignore_index, int reduction,
+                                             float grad_scale, float* loss, void* dX, void* dW, void* ws,
+                                             size_t ws_bytes, int64_t chunk, int dtype, void* stream) {
+    return linear_ce_impl(X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws, ws_bytes,
+                          chunk, dtype, stream, false);
 }
 
 extern "C" size_t liger_linear_ce_two_pass_workspace(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
@@ -888,10 +962,10 @@ extern "C" size_t liger_linear_ce_two_pass_workspace(int64_t T, int64_t H, int64
     return layout2(T, H, V, vchunk).total;
 }
 
-extern "C" int liger_linear_ce_two_pass_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T,
-                                                int64_t H, int64_t V, int64_t ignore_index, int reduction,
-                                                float grad_scale, float* loss, void* dX, void* dW, void* ws,
-                                                size_t ws_bytes, int64_t vchunk, int dtype, void* stream) {
+namespace {
+int linear_ce_two_pass_impl(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H, int64_t V,
+                            int64_t ignore_index, int reduction, float grad_scale, float* loss, void* dX, void* dW,
+                            void* ws, size_t ws_bytes, int64_t vchunk, int dtype, void* stream, bool sync) {
     clear_error();
     if (dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "linear_ce_two_pass: bf16 only (tensor-core path)");
     if (T < 0 || H < 64 || H % 8 || V < 256 || vchunk < 0 || (vchunk % 8) || H > (1 << 30) || V > (1 << 30) ||
@@ -900,8 +974,25 @@ extern "C" int liger_linear_ce_two_pass_fwd_bwd(const void* X, const void* W, co
                     "(H >= 64 and a multiple of 8, V >= 256, vchunk a multiple of 8)", (long long)T, (long long)H,
                     (long long)V, (long long)vchunk, reduction);
     const Layout2 L = layout2(T, H, V, vchunk);
-    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.total};
-    return ce_entry("linear_ce_two_pass", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW,
-                    ws, ws_bytes, dtype, stream, CL,
-                    [&](const Args& a, float scale) { return run_two_pass(a, L, scale); });
+    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.labs, L.total};
+    return ce_entry(
+        "linear_ce_two_pass", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws, ws_bytes,
+        dtype, stream, CL, [&](const Args& a, float scale) { return run_two_pass(a, L, scale); }, sync);
+}
+}  // namespace
+
+extern "C" int liger_linear_ce_two_pass_fwd_bwd(const void* X, const void* W, const int64_t* labels, int64_t T,
+                                                int64_t H, int64_t V, int64_t ignore_index, int reduction,
+                                                float grad_scale, float* loss, void* dX, void* dW, void* ws,
+                                                size_t ws_bytes, int64_t vchunk, int dtype, void* stream) {
+    return linear_ce_two_pass_impl(X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws,
+                                   ws_bytes, vchunk, dtype, stream, true);
+}
+
+extern "C" int liger_linear_ce_two_pass_fwd_bwd_async(const void* X, const void* W, const int64_t* labels, int64_t T,
+                                                      int64_t H, int64_t V, int64_t ignore_index, int reduction,
+                                                      float grad_scale, float* loss, void* dX, void* dW, void* ws,
+                                                      size_t ws_bytes, int64_t vchunk, int dtype, void* stream) {
+    return linear_ce_two_pass_impl(X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws,
+                                   ws_bytes, vchunk, dtype, stream, false);
 }

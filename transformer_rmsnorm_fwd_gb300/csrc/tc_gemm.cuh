@@ -122,6 +122,7 @@ struct EpiParams {
     const __nv_bfloat16* corr_src;
     int64_t ld_corr;
     float corr_scale;
+    const float* scale_ptr;             // non-null: corr_scale is read from here (set on the device)
     // The keys may come in nseg sorted segments with one start table each,
     // lstride ints apart (nseg 0 counts as 1).
     const unsigned long long* keys;
@@ -697,6 +698,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row = mi * Cfg::TM + static_cast<int>(crank) * BM + rl;
             const int n0 = ni * BN;
             const bool row_ok = row < ep.M;
+            const float cscale = ep.scale_ptr != nullptr ? *ep.scale_ptr : ep.corr_scale;
             // EPI_ACCUM: everything that does not depend on the accumulator is fetched
             // before waiting for it (label range, first 32 columns of the fp32 sum)
             int k_lo = 0, k_hi = 0;
@@ -809,7 +811,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int c = 0; c < BN / 32; ++c) {
                     float v[32];
                     tmem_ld32(taddr + c * 32, v);
-                    if (crow != nullptr) sub_scaled32(v, crow + c * 32, ep.corr_scale, ep.N - (n0 + c * 32));
+                    if (crow != nullptr) sub_scaled32(v, crow + c * 32, cscale, ep.N - (n0 + c * 32));
                     uint4 u[4] = {pack_bf8(v), pack_bf8(v + 8), pack_bf8(v + 16), pack_bf8(v + 24)};
                     if (zero) {
 #pragma unroll
@@ -903,7 +905,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         float a[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            a[e] = live ? ep.corr_scale *
+                            a[e] = live ? cscale *
                                               ex2_approx(fmaf(__uint_as_float(cur[g * 8 + e]), 1.4426950408889634f, -l2))
                                         : 0.f;
                         sts16(sbuf + stage_slot<4>(lane, g), pack(a));
@@ -1079,11 +1081,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         for (int kk = lo; kk < hi; ++kk) {
                             const int64_t t = static_cast<int64_t>(ep.keys[kk] & 0xFFFFFFFFull);
-                            sub_scaled32(v, ep.corr_src + t * ep.ld_corr + n0 + c * 32, ep.corr_scale,
+                            sub_scaled32(v, ep.corr_src + t * ep.ld_corr + n0 + c * 32, cscale,
                                          ep.N - (n0 + c * 32));
                         }
                     }
-                    if (lrow != nullptr) sub_scaled32(v, lrow + c * 32, ep.corr_scale, ep.N - (n0 + c * 32));
+                    if (lrow != nullptr) sub_scaled32(v, lrow + c * 32, cscale, ep.N - (n0 + c * 32));
                     if (zero_row) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] = 0.f;
