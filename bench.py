@@ -317,7 +317,7 @@ WARMUP_ITERS, MIN_ITERS, MIN_TIMED_MS, FLOOR_ITERS = 10, 50, 200.0, 5
 # DRAM bytes (read + written) of one linear-CE call at seq 32768, from one ncu capture of
 # every launch of the call with the kernels as they are now (profiles/dram_linear_ce_s32768.md);
 # to be retaken whenever a kernel of the call changes
-LINEAR_CE_TRAFFIC = 136_387_927_808
+LINEAR_CE_TRAFFIC = 154_224_649_216
 
 
 def timed_median(fn, pre=None):
