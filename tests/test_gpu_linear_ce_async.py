@@ -53,6 +53,7 @@ def _same(a, b):
     (130, 64, 300, "f32", False, "mean", 0),          # fp32 SIMT path
     (300, 320, 2037, "bf16", True, "mean", 512),
     (129, 64, 256, "bf16", True, "sum", 0),
+    (256, 64, 66536, "bf16", False, "mean", 0),       # dX over two vocabulary slabs
 ])
 def test_async_matches_waiting_form(cuda_lib, T, H, V, dtype, two_pass, reduction, chunk):
     X, W, lab = _inputs(71, T, H, V, dtype)
