@@ -45,6 +45,11 @@
  *     liger_linear_ce_fwd_bwd and liger_linear_ce_two_pass_fwd_bwd (which
  *     wait for their label scan) can be captured in a CUDA graph; their
  *     _async forms do not wait.
+ *   - Every wait inside the tensor-core kernels is bounded (about 4 s); one
+ *     that expires (never seen in normal operation) ends the kernel early,
+ *     its outputs incomplete.  The linear cross-entropies then return a NaN
+ *     loss; FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE record it
+ *     in a library-owned device word that no entry point reads back yet.
  */
 #ifndef LIGER_H
 #define LIGER_H
