@@ -70,3 +70,19 @@ def test_reference_arm_json_contract():
     d = json.loads(p.stdout.strip().splitlines()[-1])
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_launch_count_per_step():
+    """The benchmark's gpu_launches claim: 39 launches of this library per chain step
+    at seq 32768 (the ncu launch list of the step, profiles/launches_qwen_chain_s32768.md,
+    counts 117 over 3 steps): RMSNorm, RoPE and SwiGLU forwards, the linear CE (label
+    scan, sort and starts, 4 chunks x (2 logits launches, dlogits, 3 dX slab launches,
+    dW), loss reduction), SwiGLU and RoPE backwards, RMSNorm backward (2)."""
+    class _C:
+        S = 32768
+    assert bench.Chain.launches_per_step(_C()) == 39
+    with open(os.path.join(ROOT, "profiles", "launches_qwen_chain_s32768.md")) as f:
+        text = f.read()
+    assert "-c 117" in text and "TOTAL" in text
+    total = [l for l in text.splitlines() if l.startswith("TOTAL")][0].split()
+    assert int(total[1]) == 3 * 39
