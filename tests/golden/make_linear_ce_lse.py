@@ -1,8 +1,9 @@
 """Writes the fp64 oracle's full forward of a linear cross-entropy configuration
 to tests/golden: the mean loss over every valid token and the lse of every
-token (llama3: 8192 tokens x hidden 4096 x vocabulary 128256, seed 3), or of
-every 64th token (qwen32768: the Qwen-7B head of the benchmark's chain, 32768
-tokens x 4096 x 151936, seed 4); 10 % of the labels are ignored in both.
+token, for llama3 (8192 tokens x hidden 4096 x vocabulary 128256, seed 3) and
+qwen32768 (the Qwen-7B head of the benchmark's chain, 32768 tokens x 4096 x
+151936, seed 4); 10 % of the labels are ignored in both.  With every token's
+lse stored, the tests can also form rows of dW exactly at these shapes.
 
 The oracle computes the unchunked definition one row at a time (about 0.4 s a
 row on one core), so the rows are split over worker processes (spawned, each
@@ -24,7 +25,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CONFIGS = {
     # name: (workload call, H, V, seed, stride of the stored lse rows, output file)
     "llama3": ("linear_ce_llama3()", 4096, 128256, 3, 1, "linear_ce_llama3_lse.json"),
-    "qwen32768": ("qwen_chain(32768)['linear_ce']", 4096, 151936, 4, 64, "linear_ce_qwen32768_lse.json"),
+    "qwen32768": ("qwen_chain(32768)['linear_ce']", 4096, 151936, 4, 1, "linear_ce_qwen32768_lse.json"),
 }
 
 

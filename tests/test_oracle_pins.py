@@ -277,6 +277,60 @@ def test_linear_swiglu_identity_weights_golden():
     assert np.all(oracle.linear_swiglu_fwd(X, E, np.zeros((3, 3))) == 0.0)   # up = 0
 
 
+def test_linear_swiglu_asymmetric_weights_golden():
+    """Wg = I, Wu = 2I: out = silu(x) * 2x.  Swapping the gate and up roles would give
+    silu(2x) * x instead (silu(2) = 1.7616 at x = 1, against 2 silu(1) = 1.4621)."""
+    g = golden("silu_values.json")
+    X = np.array([[1.0, -1.0, 0.0]]); E = np.eye(3)
+    out = oracle.linear_swiglu_fwd(X, E, 2.0 * E)
+    assert abs(out[0, 0] - 2.0 * g["silu_1"]) < 1e-15
+    assert abs(out[0, 1] - (-2.0 * g["silu_m1"])) < 1e-15
+    assert out[0, 2] == 0.0
+    # the gate enters only through silu: gate weights 0 give silu(0) * up = 0 whatever up is,
+    # while up weights 0 with a nonzero gate also give 0; a gate of 0 and up = x must give 0,
+    # and a gate of x with up = 1 (a constant column) must give silu(x)
+    Xc = np.array([[1.0, 1.0]])                          # column 1 is the constant 1
+    Wg = np.array([[1.0, 0.0]]); Wu = np.array([[0.0, 1.0]])
+    assert abs(oracle.linear_swiglu_fwd(Xc, Wg, Wu)[0, 0] - g["silu_1"]) < 1e-15
+    assert abs(oracle.linear_swiglu_fwd(Xc, Wu, Wg)[0, 0] - g["silu_1"]) < 1e-15   # silu(1) * 1 both ways here
+    Xd = np.array([[-1.0, 1.0]])
+    assert abs(oracle.linear_swiglu_fwd(Xd, Wg, Wu)[0, 0] - g["silu_m1"]) < 1e-15   # silu(-1) * 1
+    assert abs(oracle.linear_swiglu_fwd(Xd, Wu, Wg)[0, 0] - (-g["silu_1"])) < 1e-15  # silu(1) * (-1)
+
+
+def _mlp_case(T=4, H=6, I=5):
+    X = RNG.standard_normal((T, H)); Wg = RNG.standard_normal((I, H)); Wu = RNG.standard_normal((I, H))
+    dH = RNG.standard_normal((T, I))
+    return X, Wg, Wu, dH
+
+
+def test_linear_swiglu_is_the_composition_of_the_pinned_steps():
+    """Forward = the pinned SwiGLU applied to two library matmuls (gate X Wg^T, up X Wu^T);
+    backward = the pinned SwiGLU backward pushed through the same matmuls by the chain rule."""
+    X, Wg, Wu, dH = _mlp_case()
+    G, U = np.matmul(X, Wg.T), np.matmul(X, Wu.T)
+    assert np.max(np.abs(oracle.linear_swiglu_fwd(X, Wg, Wu) - oracle.swiglu_fwd(G, U))) < 1e-12
+    dG, dU = oracle.swiglu_bwd(dH, G, U)
+    dX, dWg, dWu = oracle.linear_swiglu_bwd(X, Wg, Wu, dH)
+    assert np.max(np.abs(dX - (np.matmul(dG, Wg) + np.matmul(dU, Wu)))) < 1e-12
+    assert np.max(np.abs(dWg - np.matmul(dG.T, X))) < 1e-12
+    assert np.max(np.abs(dWu - np.matmul(dU.T, X))) < 1e-12
+
+
+def test_linear_swiglu_bwd_finite_differences_of_the_composition():
+    """Gradients against central differences of silu(X Wg^T) * (X Wu^T) written with numpy
+    alone (sigmoid by np.exp), not the oracle's own forward."""
+    X, Wg, Wu, dH = _mlp_case(3, 4, 5)
+    dX, dWg, dWu = oracle.linear_swiglu_bwd(X, Wg, Wu, dH)
+
+    def L(xx, gg, uu):
+        z = np.matmul(xx, gg.T)
+        return float(np.sum(dH * (z / (1.0 + np.exp(-z))) * np.matmul(xx, uu.T)))
+    assert np.max(np.abs(dX - _fd(lambda v: L(v, Wg, Wu), X))) < 1e-7
+    assert np.max(np.abs(dWg - _fd(lambda v: L(X, v, Wu), Wg))) < 1e-7
+    assert np.max(np.abs(dWu - _fd(lambda v: L(X, Wg, v), Wu))) < 1e-7
+
+
 def test_linear_swiglu_bwd_finite_differences():
     T, H, I = 3, 4, 5
     X = RNG.standard_normal((T, H)); Wg = RNG.standard_normal((I, H)); Wu = RNG.standard_normal((I, H))
