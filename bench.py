@@ -15,6 +15,12 @@ bounded sample, and SM clocks sampled during the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--seq S] [--impl reference]
 
+Beside the headline chain, the line carries one entry per named workload
+("configs"): per-operator latency of the tiny set (fp32 and bf16), HBM GB/s of
+SwiGLU at [4, 2048, 11008] and of RMSNorm / RoPE at the Llama-3-8B shapes,
+tokens/s and tensor-core fraction of the fused linear-CE at the Llama-3 head
+(8192 x 4096 x 128256), and the chain's tokens/s at seq 512 / 2048 / 8192.
+
 Under torchrun (N > 1) every rank runs its own chain on its own data (weak
 scaling, no collective on the data path); the timed region is bracketed by
 barriers and the slowest rank's time is reported.
@@ -51,6 +57,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", default="native", choices=["native", "reference"])
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-configs", action="store_true", help="skip the per-workload entries (configs)")
     p.add_argument("--op", default="chain",
                    choices=["chain", "linear_ce", "linear_ce_two_pass", "rmsnorm_qkv_rope", "fused_linear_swiglu",
                             "rmsnorm", "rope", "swiglu"],
@@ -106,6 +113,36 @@ def sum_over_ranks(value: float, dist, device=None) -> float:
     return float(t.item())
 
 
+class DataParallel:
+    """The exchanges of a token-sharded (data-parallel) step, over one process
+    per GPU: every rank holds its own tokens, the operators run on them with no
+    exchange, and only what the mean and the weight gradients imply crosses
+    ranks -- the count of non-ignored labels (all ranks' sum) before the fused
+    linear-CE, which then runs in sum mode with grad_scale = 1 / that count,
+    and after the backward the sums of the loss, of dW [V, H] and of the
+    RMSNorm dw [H].  dX, dx and the other operators' gradients stay local.
+    n_local is this rank's count of non-ignored labels (known on the host,
+    where the labels come from)."""
+
+    def __init__(self, dist, n_local, device):
+        self.dist, self.n_local, self.device = dist, int(n_local), device
+        self.n_global = None
+
+    def valid_count(self) -> int:
+        import torch
+        t = torch.tensor([self.n_local], dtype=torch.int64, device=self.device)
+        self.dist.all_reduce(t)
+        self.n_global = int(t.item())
+        return self.n_global
+
+    def reduce_grads(self, loss, dW, dw):
+        for t in (loss, dW, dw):
+            self.dist.all_reduce(t)
+
+    def mean_loss(self, loss_sum: float) -> float:
+        return loss_sum / self.n_global if self.n_global else 0.0
+
+
 # ---------------------------------------------------------------- workload
 def workload_config(S):
     return {"workload": f"Qwen-7B-like layer op chain, batch 1, seq {S}: RMSNorm [{S}x{HIDDEN}] -> RoPE Q/K "
@@ -114,7 +151,9 @@ def workload_config(S):
             "batch": 1, "seq_len": S, "hidden": HIDDEN, "heads": HEADS, "head_dim": HEAD_DIM,
             "intermediate": INTER, "vocab": VOCAB, "ignore_frac": 0.10, "eps": EPS, "rope_theta": THETA,
             "l2": "inputs larger than L2 (every tensor >= 2*S*4096 bytes; lm_head 1.24 GB)",
-            "parallelism": "one chain per GPU (weak scaling, no collective)"}
+            "parallelism": "one GPU; under torchrun, data parallel over tokens (each rank its own S tokens; "
+                           "all-reduce of the valid-label count before the linear-CE, of the loss, dW and RMSNorm "
+                           "dw after the backward)"}
 
 
 def algorithmic(S):
@@ -161,9 +200,10 @@ def to_torch(a, device=None, pin=False):
 class Chain:
     """Device buffers of one chain and the calls of one step."""
 
-    def __init__(self, L, inputs, device):
+    def __init__(self, L, inputs, device, dp: DataParallel | None = None):
         import torch
         self.L = L
+        self.dp = dp
         bf = torch.bfloat16
         S = inputs["x"].shape[0]
         self.S = S
@@ -212,12 +252,21 @@ class Chain:
         rec("rmsnorm_fwd", lambda: L.liger_rmsnorm_fwd(i["x"], i["w"], self.y, self.rstd, EPS))
         rec("rope_fwd", lambda: L.liger_rope_fwd(i["q"], i["k"], None, THETA))
         rec("swiglu_fwd", lambda: L.liger_swiglu_fwd(i["gate"], i["up"], self.ys))
-        rec("linear_ce", lambda: L.liger_linear_ce_fwd_bwd(i["X"], i["W"], i["labels"], self.loss, self.dX, self.dW,
-                                                           self.ws_c))
+        if self.dp is None:
+            rec("linear_ce", lambda: L.liger_linear_ce_fwd_bwd(i["X"], i["W"], i["labels"], self.loss, self.dX,
+                                                               self.dW, self.ws_c))
+        else:
+            # data parallel: the mean over every rank's valid tokens
+            n = self.dp.valid_count()
+            rec("linear_ce", lambda: L.liger_linear_ce_fwd_bwd(i["X"], i["W"], i["labels"], self.loss, self.dX,
+                                                               self.dW, self.ws_c, reduction="sum",
+                                                               grad_scale=1.0 / max(n, 1)))
         rec("swiglu_bwd", lambda: L.liger_swiglu_bwd(i["dy_s"], i["gate"], i["up"], self.dg, self.du))
         rec("rope_bwd", lambda: L.liger_rope_bwd(i["dq"], i["dk"], None, THETA))
         rec("rmsnorm_bwd", lambda: L.liger_rmsnorm_bwd(i["dy_r"], i["x"], i["w"], self.rstd, self.dx, self.dw,
                                                        self.ws_r))
+        if self.dp is not None:
+            self.dp.reduce_grads(self.loss, self.dW, self.dw)
 
 
 def isolated_times(chain, dev):
@@ -227,13 +276,8 @@ def isolated_times(chain, dev):
     and no other buffer's dirty lines are left for the operator to write back
     (the state ncu's cache control leaves before a capture); the in-place RoPE
     gets its inputs restored first."""
-    import torch
     L, i = chain.L, chain.inp
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-
-    def flush_l2():
-        flush.zero_()
-        flush.view(torch.int32).amax()   # read back: L2 left holding clean lines of the flush buffer
+    flush_l2 = L2Flush(dev)
 
     ops = {
         "rmsnorm_fwd": lambda: L.liger_rmsnorm_fwd(i["x"], i["w"], chain.y, chain.rstd, EPS),
@@ -259,14 +303,15 @@ def isolated_times(chain, dev):
     out = {name: timed_median(fn, pre=pres.get(name, flush_l2)) for name, fn in ops.items()}
     for k, v in saved.items():
         i[k].copy_(v)
-    del flush, saved
+    del flush_l2, saved
     return out
 
 
 def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER):
     """FusedLinearSwiGLU at the pages' MLP shape (8192 tokens, hidden 4096,
-    intermediate 11008), forward and backward alone: ms and TFLOP/s
-    (forward 4*T*H*I flops; backward 12*T*H*I: recompute, dX, dW)."""
+    intermediate 11008), forward and backward alone: ms and TFLOP/s of the
+    operator's useful flops (forward 4*T*H*I; backward 8*T*H*I: dX, dW_g, dW_u;
+    the recomputing backward also executes the forward's 4*T*H*I again)."""
     import torch
     from datagen import normal
     X = to_torch(normal(5, "mlp.X", (T, H), "bf16"), dev)
@@ -279,9 +324,10 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER):
     res = {}
     for name, fn, fl in (("fwd", lambda: L.liger_fused_linear_swiglu_fwd(X, Wg, Wu, out), 4 * T * H * I),
                          ("bwd", lambda: L.liger_fused_linear_swiglu_bwd(X, Wg, Wu, dH, dX, dWg, dWu, ws),
-                          12 * T * H * I)):
+                          8 * T * H * I)):
         ms = timed_median(fn)
         res[name] = {"ms": round(ms, 3), "tflops": round(fl / ms / 1e9, 1)}
+    res["bwd"]["tflops_executed_12thi"] = round(12 * T * H * I / res["bwd"]["ms"] / 1e9, 1)
     # the same work in native PyTorch (two cuBLAS matmuls, silu * mul; backward by autograd),
     # the comparison the pages quote for this fusion
     import torch.nn.functional as F
@@ -310,13 +356,18 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER):
     res["speedup_bwd_vs_torch"] = round(res["torch_bwd_ms"] / res["bwd"]["ms"], 3)
     res["speedup_fwd_bwd_vs_torch"] = round(t_fb / (res["fwd"]["ms"] + res["bwd"]["ms"]), 3)
     res["speedup_fwd_bwd_saved_vs_torch"] = round(t_fb / (res["fwd_save_ms"] + res["bwd_saved_ms"]), 3)
+    # the training pair (the forward keeps g and u for the backward, as autograd keeps its activations)
+    fb = res["fwd_save_ms"] + res["bwd_saved_ms"]
+    res["fwd_bwd"] = {"pair": "liger_fused_linear_swiglu_fwd_save + liger_fused_linear_swiglu_bwd_saved",
+                      "ms": round(fb, 3), "tflops": round(12 * T * H * I / fb / 1e9, 1),
+                      "torch_ms": round(t_fb, 3), "speedup_vs_torch": round(t_fb / fb, 3)}
     return res
 
 
 WARMUP_ITERS, MIN_ITERS, MIN_TIMED_MS, FLOOR_ITERS = 10, 50, 200.0, 5
-# DRAM bytes (read + written) of one linear-CE call at seq 32768, from one ncu capture of
-# every launch of the call with the kernels as they are now (profiles/dram_linear_ce_s32768.md);
-# to be retaken whenever a kernel of the call changes
+# DRAM bytes (read + written) of one linear-CE call at seq 32768 (one ncu capture of the DRAM
+# byte counters over every launch of one call, kernels as of that capture); not re-measured
+# since, and reported as that capture's figure
 LINEAR_CE_TRAFFIC = 154_224_649_216
 
 
@@ -394,8 +445,9 @@ def rmsnorm_qkv_rope_measure(L, dev, S=32768, H=HIDDEN, Hq=HEADS, Hk=HEADS, D=HE
 
 def linear_ce_two_pass_measure(chain, dev):
     """The two-pass, vocabulary-chunked linear CE on the chain's own head inputs
-    (seq x 4096 x 151936), alone: ms, TFLOP/s counting its 8*S*H*V flops and the
-    operator's 6*S*H*V, and both variants' workspace bytes."""
+    (seq x 4096 x 151936), alone: ms, TFLOP/s of the operator's useful 6*S*H*V
+    flops and of the 8*S*H*V it executes (the logits twice), and both
+    variants' workspace bytes."""
     import torch
     L, i, S = chain.L, chain.inp, chain.S
     ws = torch.empty(L.liger_linear_ce_two_pass_workspace(S, HIDDEN, VOCAB), dtype=torch.uint8, device=dev)
@@ -404,6 +456,195 @@ def linear_ce_two_pass_measure(chain, dev):
     fl = float(S) * HIDDEN * VOCAB
     return {"ms": round(ms, 3), "tflops_8shv": round(8 * fl / ms / 1e9, 1), "tflops_6shv": round(6 * fl / ms / 1e9, 1),
             "workspace_bytes": int(ws.numel()), "workspace_bytes_token_chunked": int(chain.ws_c.numel())}
+
+
+# ------------------------------------------------------- named workloads
+class L2Flush:
+    """Writes a 512 MB buffer and reads it back: afterwards no input of the next
+    call is resident in the 129 MB L2 and no other buffer's dirty lines are
+    left for the call to write back."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        self.buf.view(torch.int32).amax()
+
+
+def _hbm_entry(nbytes, ms, pk):
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    return {"ms": round(ms, 4), "bytes": int(nbytes), "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4)}
+
+
+def tiny_latency(L, dev, flush):
+    """The tiny decoder-op set (batch 2, seq 128, hidden 256, 4 heads x 64,
+    intermediate 688, vocab 1024) in fp32 and bf16: median latency of each
+    operator call in microseconds, L2 flushed before every call (the set fits
+    in L2).  fp32 linear-CE runs on the fp32 SIMT path, bf16 on the tensor cores."""
+    import torch
+    from datagen import workloads
+    out = {}
+    for dt in ("f32", "bf16"):
+        w = workloads.tiny(dt)
+        r, p, sw, c = w["rmsnorm"], w["rope"], w["swiglu"], w["linear_ce"]
+        x, wn, dy = (to_torch(r.make(k), dev) for k in ("x", "w", "dy"))
+        q, k = to_torch(p.make("q"), dev), to_torch(p.make("k"), dev)
+        g, u, dys = (to_torch(sw.make(k_), dev) for k_ in ("gate", "up", "dy"))
+        X, W = to_torch(c.make("X"), dev), to_torch(c.make("W"), dev)
+        lab = torch.from_numpy(c.make("labels")).to(dev)
+        T, H = x.shape
+        y, dx, dw = torch.empty_like(x), torch.empty_like(x), torch.empty_like(wn)
+        rstd = torch.empty(T, dtype=torch.float32, device=dev)
+        wsr = torch.empty(L.liger_rmsnorm_bwd_workspace(T, H), dtype=torch.uint8, device=dev)
+        ys, dg, du = torch.empty_like(g), torch.empty_like(g), torch.empty_like(g)
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+        dX, dW = torch.empty_like(X), torch.empty_like(W)
+        code = L.LIGER_F32 if dt == "f32" else L.LIGER_BF16
+        wsc = torch.empty(L.liger_linear_ce_workspace(T, H, W.shape[0], 0, code), dtype=torch.uint8, device=dev)
+        eps, theta = r.params["eps"], p.params["theta"]
+        L.liger_rmsnorm_fwd(x, wn, y, rstd, eps)
+        ops = {
+            "rmsnorm_fwd": lambda: L.liger_rmsnorm_fwd(x, wn, y, rstd, eps),
+            "rmsnorm_bwd": lambda: L.liger_rmsnorm_bwd(dy, x, wn, rstd, dx, dw, wsr),
+            "rope_fwd": lambda: L.liger_rope_fwd(q, k, None, theta),
+            "rope_bwd": lambda: L.liger_rope_bwd(q, k, None, theta),
+            "swiglu_fwd": lambda: L.liger_swiglu_fwd(g, u, ys),
+            "swiglu_bwd": lambda: L.liger_swiglu_bwd(dys, g, u, dg, du),
+            "linear_ce_fwd_bwd": lambda: L.liger_linear_ce_fwd_bwd(X, W, lab, loss, dX, dW, wsc),
+        }
+        out[dt] = {name: round(1000.0 * timed_median(fn, pre=flush), 2) for name, fn in ops.items()}
+    out["unit"] = "us per call (median, L2 flushed before each call)"
+    out["shape"] = "T=256 H=256 heads 4x64 I=688 V=1024"
+    return out
+
+
+def swiglu_config(L, dev, flush, pk):
+    """SwiGLU fwd and bwd on gate/up [4, 2048, 11008] bf16 (seed 1), alone, L2
+    flushed before each call: 3 and 5 bytes x 2 per element."""
+    import torch
+    from datagen import workloads
+    w = workloads.swiglu_llama()
+    g, u, dy = (to_torch(w.make(k), dev) for k in ("gate", "up", "dy"))
+    y, dg, du = torch.empty_like(g), torch.empty_like(g), torch.empty_like(g)
+    n = g.numel()
+    f = timed_median(lambda: L.liger_swiglu_fwd(g, u, y), pre=flush)
+    b = timed_median(lambda: L.liger_swiglu_bwd(dy, g, u, dg, du), pre=flush)
+    return {"shape": "gate/up [4,2048,11008] bf16", "fwd": _hbm_entry(3 * n * 2, f, pk),
+            "bwd": _hbm_entry(5 * n * 2, b, pk)}
+
+
+def llama3_norm_rope_config(L, dev, flush, pk):
+    """RMSNorm fwd/bwd on x [32768, 4096] (eps 1e-5) and RoPE fwd/bwd on
+    Q [4, 8192, 32, 128] + K [4, 8192, 8, 128] (theta 5e5), bf16, seed 2,
+    alone, L2 flushed before each call (RoPE's inputs restored first)."""
+    import torch
+    from datagen import workloads
+    w = workloads.rmsnorm_rope_llama3()
+    r, p = w["rmsnorm"], w["rope"]
+    x, wn, dy = (to_torch(r.make(k), dev) for k in ("x", "w", "dy"))
+    T, H = x.shape
+    y, dx, dw = torch.empty_like(x), torch.empty_like(x), torch.empty_like(wn)
+    rstd = torch.empty(T, dtype=torch.float32, device=dev)
+    wsr = torch.empty(L.liger_rmsnorm_bwd_workspace(T, H), dtype=torch.uint8, device=dev)
+    eps, theta = r.params["eps"], p.params["theta"]
+    L.liger_rmsnorm_fwd(x, wn, y, rstd, eps)
+    rf = timed_median(lambda: L.liger_rmsnorm_fwd(x, wn, y, rstd, eps), pre=flush)
+    rb = timed_median(lambda: L.liger_rmsnorm_bwd(dy, x, wn, rstd, dx, dw, wsr), pre=flush)
+    del y, dx
+    q, k, dq, dk = (to_torch(p.make(n), dev) for n in ("q", "k", "dq", "dk"))
+    saved = {n: t.clone() for n, t in (("q", q), ("k", k), ("dq", dq), ("dk", dk))}
+
+    def restore(*pairs):
+        def pre():
+            for t, n in pairs:
+                t.copy_(saved[n])
+            flush()
+        return pre
+    pf = timed_median(lambda: L.liger_rope_fwd(q, k, None, theta), pre=restore((q, "q"), (k, "k")))
+    pb = timed_median(lambda: L.liger_rope_bwd(dq, dk, None, theta), pre=restore((dq, "dq"), (dk, "dk")))
+    e = 2
+    qk = q.numel() + k.numel()
+    return {"shape": "x [32768,4096]; Q [4,8192,32,128] + K [4,8192,8,128] theta 5e5, bf16",
+            "rmsnorm_fwd": _hbm_entry(2 * T * H * e + 4 * T + H * e, rf, pk),
+            "rmsnorm_bwd": _hbm_entry(3 * T * H * e + 4 * T + 2 * H * e, rb, pk),
+            "rope_fwd": _hbm_entry(2 * qk * e, pf, pk), "rope_bwd": _hbm_entry(2 * qk * e, pb, pk)}
+
+
+def llama3_head_config(L, dev, pk):
+    """Fused linear-CE fwd+bwd at the Llama-3 head: 8192 tokens x hidden 4096 x
+    vocab 128256 bf16, 10 % ignored labels, mean (seed 3), back-to-back calls
+    (lm_head 1.05 GB: larger than L2).  6*T*H*V useful flops per call."""
+    import torch
+    from datagen import workloads
+    c = workloads.linear_ce_llama3()
+    X, W = to_torch(c.make("X"), dev), to_torch(c.make("W"), dev)
+    lab = torch.from_numpy(c.make("labels")).to(dev)
+    T, H = X.shape
+    V = W.shape[0]
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    dX, dW = torch.empty_like(X), torch.empty_like(W)
+    ws = torch.empty(L.liger_linear_ce_workspace(T, H, V, 0, L.LIGER_BF16), dtype=torch.uint8, device=dev)
+    ms = timed_median(lambda: L.liger_linear_ce_fwd_bwd(X, W, lab, loss, dX, dW, ws))
+    tf = 6.0 * T * H * V / (ms / 1000.0) / 1e12
+    return {"shape": "T=8192 H=4096 V=128256 bf16, mean, 10% ignored", "ms": round(ms, 3),
+            "tokens_per_s": round(T / (ms / 1000.0), 1), "tflops_6thv": round(tf, 1),
+            "frac_sustained": round(tf / pk["bf16_sustained"], 4), "frac_burst": round(tf / pk["bf16"], 4),
+            "loss": float(loss.item()),
+            "timing": "median of >= 50 back-to-back calls after 10 warm-ups (power-capped clock: compare with "
+                      "the sustained peak)"}
+
+
+def chain_sweep(L, dev, flush, base_inputs, seqs=(512, 2048, 8192), steps=10):
+    """The layer chain at shorter sequences (the same named tensors of seed 4,
+    i.e. the first S rows of the seq-32768 draws, and labels drawn for S
+    tokens): median ms of one step (every operator fwd+bwd) with L2 flushed
+    before each step, and tokens/s = S / that time."""
+    import torch
+    from datagen import workloads
+    out = {}
+    for S in seqs:
+        inp = {}
+        for k_, v in base_inputs.items():
+            if k_ in ("q", "k", "dq", "dk"):
+                inp[k_] = np.ascontiguousarray(v[:, :S])
+            elif k_ in ("w", "W"):
+                inp[k_] = v
+            elif k_ == "labels":
+                inp[k_] = workloads.qwen_chain(S)["linear_ce"].make("labels")
+            else:
+                inp[k_] = np.ascontiguousarray(v[:S])
+        ch = Chain(L, inp, dev)
+        for _ in range(3):
+            ch.step()
+        ts = []
+        for _ in range(steps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            ch.step()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = statistics.median(ts)
+        out[str(S)] = {"ms_per_step": round(ms, 3), "tokens_per_s": round(S / (ms / 1000.0), 1)}
+        del ch
+        torch.cuda.empty_cache()
+    out["timing"] = f"median of {steps} steps, L2 flushed before each"
+    return out
+
+
+def named_configs(L, dev, pk, chain_inputs):
+    flush = L2Flush(dev)
+    res = {"tiny_set": tiny_latency(L, dev, flush),
+           "swiglu_4x2048x11008": swiglu_config(L, dev, flush, pk),
+           "llama3_rmsnorm_rope": llama3_norm_rope_config(L, dev, flush, pk),
+           "llama3_linear_ce": llama3_head_config(L, dev, pk),
+           "qwen_chain_seq_sweep": chain_sweep(L, dev, flush, chain_inputs)}
+    del flush
+    return res
 
 
 # ------------------------------------------------------------------ clocks
@@ -497,21 +738,52 @@ def cpu_oracle_sample(S, inputs, n_rows=32, n_tokens=1):
     return 1.0 / per_token, desc, per_token
 
 
+# Arm CPU parts by (implementer, part) of the main ID register, as /proc/cpuinfo prints them
+ARM_PARTS = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+             ("0x41", "0xd0c"): "Arm Neoverse N1", ("0x41", "0xd49"): "Arm Neoverse N2",
+             ("0x41", "0xd84"): "Arm Neoverse V3", ("0x41", "0xd8e"): "Arm Neoverse N3"}
+
+
+def cpu_model(cpuinfo_text: str, lscpu_text: str = "") -> str | None:
+    """The CPU model: /proc/cpuinfo's model name (x86), else lscpu's "Model
+    name", else the Arm implementer/part pair of /proc/cpuinfo, named where known."""
+    for line in cpuinfo_text.splitlines():
+        k, _, v = line.partition(":")
+        if k.strip().lower() in ("model name", "cpu model", "processor name") and v.strip():
+            return v.strip()
+    for line in lscpu_text.splitlines():
+        k, _, v = line.partition(":")
+        if k.strip().lower() == "model name" and v.strip() and v.strip() != "-":
+            return v.strip()
+    impl = part = None
+    for line in cpuinfo_text.splitlines():
+        k, _, v = line.partition(":")
+        k, v = k.strip().lower(), v.strip().lower()
+        if k == "cpu implementer" and impl is None:
+            impl = v
+        elif k == "cpu part" and part is None:
+            part = v
+    if impl and part:
+        name = ARM_PARTS.get((impl, part))
+        return f"{name} (implementer {impl}, part {part})" if name else f"Arm implementer {impl}, part {part}"
+    return None
+
+
 def host_cpu():
-    """The host the oracle ran on: logical CPUs and the CPU model (from
-    /proc/cpuinfo where it names one, else the machine type)."""
+    """The host the oracle ran on: logical CPUs and the CPU model."""
     import platform
-    model = None
+    info = ls = ""
     try:
         with open("/proc/cpuinfo") as f:
-            for line in f:
-                k, _, v = line.partition(":")
-                if k.strip().lower() in ("model name", "cpu model", "processor name") and v.strip():
-                    model = v.strip()
-                    break
+            info = f.read()
     except OSError:
         pass
-    return {"host_nproc": os.cpu_count(), "host_cpu": model or platform.machine()}
+    try:
+        ls = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+    except Exception:
+        pass
+    return {"host_nproc": os.cpu_count(), "host_cpu": cpu_model(info, ls) or platform.machine(),
+            "host_arch": platform.machine()}
 
 
 def emit(d):
@@ -532,7 +804,9 @@ def reference_arm(args):
             vals.append(v)
     value = statistics.mean(vals)
     d = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * S / value, "higher_is_better": True,
+         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * S / value,
+         "ms_per_step_kind": f"extrapolated: seq {S} tokens / the tokens/s of a 16-row / 1-token sample per step",
+         "higher_is_better": True,
          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_config(S),
          "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc, **host_cpu()},
          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -551,7 +825,8 @@ def native_arm(args):
     S, K, W = args.seq, args.steps, args.warmup
     assert W >= 0 and K >= 1
     inputs = gen_inputs(S, seed_offset=rank)
-    chain = Chain(L, inputs, dev)
+    dp = DataParallel(dist, int((inputs["labels"] != -100).sum()), dev) if dist else None
+    chain = Chain(L, inputs, dev, dp)
     torch.cuda.synchronize()
 
     # ---- device-resident timing
@@ -581,6 +856,8 @@ def native_arm(args):
     qkv = rmsnorm_qkv_rope_measure(L, dev, S)
     two_pass = linear_ce_two_pass_measure(chain, dev)
     loss = float(chain.loss.item())
+    if dp is not None:
+        loss = dp.mean_loss(loss)
 
     # ---- end to end through host buffers: every step copies its inputs (activations,
     # labels, upstream gradients) host -> device from pinned memory and reads its loss back;
@@ -654,6 +931,9 @@ def native_arm(args):
         return 0
 
     pk = peaks()
+    configs = None
+    if not args.no_configs:
+        configs = named_configs(L, dev, pk, inputs)
     alg = algorithmic(S)
     hbm = {}
     for k in ("rmsnorm_fwd", "rmsnorm_bwd", "rope_fwd", "rope_bwd", "swiglu_fwd", "swiglu_bwd"):
@@ -668,7 +948,7 @@ def native_arm(args):
                 "frac": round(ce_tf / pk["bf16_sustained"], 4),
                 "traffic": LINEAR_CE_TRAFFIC if S == 32768 else None, "traffic_unit": "bytes per call",
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over every launch of one "
-                                  "call at seq 32768 (one pass, full size): profiles/dram_linear_ce_s32768.md",
+                                  "call at seq 32768, from an earlier capture (not re-measured)",
                 "peak_source": f"{pk['src']} bf16 sustained (cuBLAS loop under the power cap)",
                 "ms_per_call": round(per_op["linear_ce"], 3)}
     cpu = None
@@ -679,14 +959,17 @@ def native_arm(args):
          "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
          "data": "synthetic (seeded SplitMix64/Box-Muller, shapes and distributions of the Qwen-7B layer chain)",
          "config": workload_config(S), "roofline": roofline, "hbm_kernels": hbm,
-         "hbm_peak_gbs": pk["hbm_gbs"], "cpu_baseline": cpu, "e2e": e2e,
+         "hbm_peak_gbs": pk["hbm_gbs"], "cpu_baseline": cpu, "e2e": e2e, "configs": configs,
          "gpu_launches": chain.launches_per_step() * K, "clocks": clocks, "loss": loss,
          "fused_linear_swiglu": dict(mlp, shape="T=8192 H=4096 I=11008 bf16 (alone, not part of the step)",
                                      peak_tflops_burst=pk["bf16"], peak_tflops_sustained=pk["bf16_sustained"],
+                                     flops="useful: fwd 4*T*H*I, bwd 8*T*H*I, fwd_bwd 12*T*H*I",
                                      frac_fwd=round(mlp["fwd"]["tflops"] / pk["bf16"], 4),
                                      frac_bwd=round(mlp["bwd"]["tflops"] / pk["bf16"], 4),
                                      frac_fwd_sustained=round(mlp["fwd"]["tflops"] / pk["bf16_sustained"], 4),
                                      frac_bwd_sustained=round(mlp["bwd"]["tflops"] / pk["bf16_sustained"], 4),
+                                     frac_fwd_bwd_sustained=round(mlp["fwd_bwd"]["tflops"] / pk["bf16_sustained"],
+                                                                  4),
                                      timing="median of >= 50 back-to-back calls after 10 warm-ups (power-capped "
                                             "clock: compare with the sustained peak)"),
          "rmsnorm_qkv_rope": dict(qkv, shape=f"T={S} H={HIDDEN} Hq=Hk={HEADS} D={HEAD_DIM} QKV bias, bf16 "
@@ -701,7 +984,8 @@ def native_arm(args):
                                          "clock: compare with the sustained peak)"),
          "linear_ce_two_pass": dict(two_pass, shape=f"S={S} H={HIDDEN} V={VOCAB} bf16, auto vocabulary chunk "
                                                     "(alone, not part of the step)",
-                                    frac=round(two_pass["tflops_8shv"] / pk["bf16_sustained"], 4))}
+                                    frac_useful_6shv=round(two_pass["tflops_6shv"] / pk["bf16_sustained"], 4),
+                                    frac_executed_8shv=round(two_pass["tflops_8shv"] / pk["bf16_sustained"], 4))}
     emit(d)
     if dist:
         dist.destroy_process_group()

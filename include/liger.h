@@ -45,11 +45,14 @@
  *     liger_linear_ce_fwd_bwd and liger_linear_ce_two_pass_fwd_bwd (which
  *     wait for their label scan) can be captured in a CUDA graph; their
  *     _async forms do not wait.
- *   - Every wait inside the tensor-core kernels is bounded (about 4 s); one
- *     that expires (never seen in normal operation) ends the kernel early,
- *     its outputs incomplete.  The linear cross-entropies then return a NaN
- *     loss; FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE record it
- *     in a library-owned device word that no entry point reads back yet.
+ *   - Every wait inside the tensor-core kernels and the staged RMSNorm
+ *     kernels is bounded (about 4 s); one that expires (never seen in normal
+ *     operation) ends the kernel early, its outputs incomplete.  The linear
+ *     cross-entropies then return a NaN loss; the RMSNorm kernels write NaN
+ *     into the rows they did not finish (and into dw); RMSNorm,
+ *     FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE also record the
+ *     expiry in library-owned device words that liger_device_status reads
+ *     back and clears.
  */
 #ifndef LIGER_H
 #define LIGER_H
@@ -77,6 +80,33 @@ extern "C" {
 
 /* Message for the last failing call on this thread ("" if none). */
 const char* liger_last_error(void);
+
+/* Status of the work already queued on the current device.
+ *
+ * The calls return their status when they queue work, before it runs; an
+ * expired bounded wait inside a kernel happens later.  The linear
+ * cross-entropies report one through their NaN loss.  The staged RMSNorm
+ * kernels, FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE record it in
+ * three library-owned device words (one per family, per device).  This call
+ * queues a one-thread kernel on `stream` that reads and clears the three
+ * words, waits for `stream` (cudaStreamSynchronize), and returns LIGER_OK if
+ * none was set, else LIGER_ERR_CUDA with liger_last_error() naming the
+ * families whose wait expired.  It covers the work queued on `stream` before
+ * it and any other work of the library on the device that has finished by
+ * then; an expiry in a kernel still running on another stream shows at a
+ * later call.  Each word is cleared when read, so a second call returns
+ * LIGER_OK until a new expiry.  A failing CUDA call (no device, an earlier
+ * kernel fault) also returns LIGER_ERR_CUDA.  Not for use inside a stream
+ * capture (it waits for the stream).
+ */
+int liger_device_status(void* stream);
+
+/* Marks family `which` (0 = RMSNorm, 1 = FusedLinearSwiGLU, 2 = fused
+ * RMSNorm + QKV + RoPE) as an expired wait would, by a one-thread kernel on
+ * `stream`, without any wait expiring: for tests of liger_device_status and
+ * of the caller's own handling of it.  LIGER_ERR_SHAPE for another `which`.
+ */
+int liger_device_status_mark(int which, void* stream);
 
 /* ------------------------------------------------------------- RMSNorm
  * Source: the RMSNorm step of the fused RMSNorm + QKV + RoPE kernel on the

@@ -74,15 +74,116 @@ def test_reference_arm_json_contract():
 
 def test_launch_count_per_step():
     """The benchmark's gpu_launches claim: 39 launches of this library per chain step
-    at seq 32768 (the ncu launch list of the step, profiles/launches_qwen_chain_s32768.md,
-    counts 117 over 3 steps): RMSNorm, RoPE and SwiGLU forwards, the linear CE (label
-    scan, sort and starts, 4 chunks x (2 logits launches, dlogits, 3 dX slab launches,
-    dW), loss reduction), SwiGLU and RoPE backwards, RMSNorm backward (2)."""
+    at seq 32768 (an ncu launch list of 3 steps counted 117): RMSNorm, RoPE and SwiGLU
+    forwards, the linear CE (label scan, sort and starts, 4 chunks x (2 logits launches,
+    dlogits, 3 dX slab launches, dW), loss reduction), SwiGLU and RoPE backwards,
+    RMSNorm backward (2)."""
     class _C:
         S = 32768
     assert bench.Chain.launches_per_step(_C()) == 39
-    with open(os.path.join(ROOT, "profiles", "launches_qwen_chain_s32768.md")) as f:
-        text = f.read()
-    assert "-c 117" in text and "TOTAL" in text
-    total = [l for l in text.splitlines() if l.startswith("TOTAL")][0].split()
-    assert int(total[1]) == 3 * 39
+    assert 3 * bench.Chain.launches_per_step(_C()) == 117
+
+
+def test_cpu_model_names_x86_and_arm_hosts():
+    assert bench.cpu_model("processor\t: 0\nmodel name\t: Intel(R) Xeon(R) Platinum 8480C\n") == \
+        "Intel(R) Xeon(R) Platinum 8480C"
+    arm = "processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\nCPU part\t: 0xd4f\n"
+    assert bench.cpu_model(arm) == "Arm Neoverse V2 (implementer 0x41, part 0xd4f)"
+    assert bench.cpu_model(arm, "Architecture: aarch64\nModel name: Neoverse-V2\n") == "Neoverse-V2"
+    assert bench.cpu_model("processor\t: 0\nCPU implementer\t: 0x61\nCPU part\t: 0x001\n") == \
+        "Arm implementer 0x61, part 0x001"
+
+
+class _RecordingLib:
+    """Stands in for the CUDA library: records the order of the operator calls."""
+    LIGER_BF16 = 1
+
+    def __init__(self, log):
+        self.log = log
+
+    def liger_rmsnorm_bwd_workspace(self, rows, cols):
+        return 16
+
+    def liger_linear_ce_workspace(self, T, H, V, chunk, dtype):
+        return 16
+
+    def __getattr__(self, name):
+        if not name.startswith("liger_"):
+            raise AttributeError(name)
+
+        def call(*args, **kw):
+            self.log.append((name, kw.get("reduction", None), kw.get("grad_scale", None)))
+        return call
+
+
+class _RecordingDist:
+    """Stands in for torch.distributed on one rank whose peer holds 30 valid labels."""
+
+    def __init__(self, log):
+        self.log = log
+
+    def all_reduce(self, t, op=None):
+        self.log.append(("all_reduce", tuple(t.shape), None))
+        if t.dtype.is_floating_point is False:
+            t += 30
+
+
+def test_data_parallel_step_issues_the_exchanges_in_order(monkeypatch):
+    """The chain step under data parallelism: the valid-label count is summed over
+    ranks before the linear-CE, which runs in sum mode scaled by 1 / that count;
+    after the backward the loss, dW [V, H] and the RMSNorm dw [H] are summed."""
+    import numpy as np
+    import torch
+    monkeypatch.setattr(bench, "HIDDEN", 8)
+    monkeypatch.setattr(bench, "INTER", 12)
+    monkeypatch.setattr(bench, "VOCAB", 10)
+    S = 4
+    inputs = {k: np.zeros(sh, np.float32) for k, sh in
+              {"x": (S, 8), "w": (8,), "dy_r": (S, 8), "q": (1, S, 2, 4), "k": (1, S, 2, 4), "dq": (1, S, 2, 4),
+               "dk": (1, S, 2, 4), "gate": (S, 12), "up": (S, 12), "dy_s": (S, 12), "X": (S, 8),
+               "W": (10, 8)}.items()}
+    inputs["labels"] = np.array([1, -100, 3, 4], np.int64)
+    log = []
+    dp = bench.DataParallel(_RecordingDist(log), int((inputs["labels"] != -100).sum()), "cpu")
+    ch = bench.Chain(_RecordingLib(log), inputs, torch.device("cpu"), dp)
+    ch.step()
+    names = [e[0] for e in log]
+    assert names == ["liger_rmsnorm_fwd", "liger_rope_fwd", "liger_swiglu_fwd", "all_reduce",
+                     "liger_linear_ce_fwd_bwd", "liger_swiglu_bwd", "liger_rope_bwd", "liger_rmsnorm_bwd",
+                     "all_reduce", "all_reduce", "all_reduce"]
+    assert log[3][1] == (1,)                                  # the count
+    assert log[4][1:] == ("sum", 1.0 / 33)                    # 3 local + 30 on the peer
+    assert [e[1] for e in log[8:]] == [(1,), (10, 8), (8,)]   # loss, dW, dw
+    assert dp.mean_loss(66.0) == 2.0
+
+
+def _dp_worker(rank, port, q):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": "2"})
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    dp = bench.DataParallel(dist, 5 + 2 * rank, "cpu")
+    n = dp.valid_count()
+    loss = torch.tensor([1.5 * (rank + 1)])
+    dW = torch.full((3, 2), float(rank + 1))
+    dw = torch.tensor([rank, 1.0])
+    dp.reduce_grads(loss, dW, dw)
+    q.put((rank, n, float(loss.item()), dW.tolist(), dw.tolist(), dp.mean_loss(float(loss.item()))))
+    dist.destroy_process_group()
+
+
+def test_data_parallel_exchanges_over_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    ps = [ctx.Process(target=_dp_worker, args=(r, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    out = sorted(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, n, loss, dW, dw, mean in out:
+        assert n == 12 and loss == 4.5 and dW == [[3.0, 3.0]] * 3 and dw == [1.0, 2.0] and mean == 4.5 / 12

@@ -20,7 +20,7 @@ def lib():
 
 def test_exports_every_declared_function(lib):
     names = _native.header_functions()
-    assert len(names) == 24
+    assert len(names) == 26
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(_native.SIGNATURES)
@@ -108,3 +108,10 @@ def test_rmsnorm_qkv_rope_host_checks(lib):
     assert lib.liger_rmsnorm_qkv_rope_fwd(*args(ws=ctypes.c_void_p(0x1010))) == -6
     assert lib.liger_rmsnorm_qkv_rope_fwd(*args(x=None)) == -1
     assert lib.liger_rmsnorm_qkv_rope_fwd(*args(x=ctypes.c_void_p(0x1008))) == -4
+
+
+def test_device_status_marker_checks_its_family(lib):
+    # an unknown family is rejected before any CUDA call
+    assert lib.liger_device_status_mark(3, None) == -2
+    assert lib.liger_device_status_mark(-1, None) == -2
+    assert "which" in _err(lib)

@@ -237,6 +237,16 @@ def test_linear_ce_qwen_chain_seq32768(cuda_lib):
     assert g["n_valid"] == int((lab != -100).sum())
     assert np.max(np.abs(lse[::st][keep] - olse[keep]) / np.abs(olse[keep])) <= 1e-5
     assert abs(float(loss.item()) - g["loss_mean"]) <= LOSS_TOL_BF16 * abs(g["loss_mean"])
+    if st == 1:
+        # rows of dW (each a sum over all 32768 tokens of four chunks, accumulated in fp32
+        # across chunks, grouped tile order) from the oracle's lse of every token: rows that
+        # are labels of tokens in each chunk, and random rows
+        lab_rows = [int(lab[t]) for t in (3, 8200, 16390, 32760) if lab[t] >= 0]
+        vrows = np.unique(np.concatenate([lab_rows, np.random.default_rng(6).choice(V, 14, replace=False),
+                                          [0, V - 1]]))
+        assert len(vrows) >= 16
+        odW = oracle.linear_ce_dw_rows(X, W, lab, olse, vrows)
+        assert oracle.rel_err(host(dW[torch.as_tensor(vrows, device="cuda")]), odW) <= 2e-2
     rows = np.array([1, 8191, 8192, 32766])
     o = oracle.linear_ce_rows(X, W, lab, rows)
     hdX = host(dX[torch.as_tensor(rows, device="cuda")])
@@ -356,3 +366,39 @@ def test_linear_ce_dx_over_vocabulary_slabs(cuda_lib):
     lab[:6] = [0, 33279, 33280, 33281, V - 1, 16000]
     loss, dX, dW, lse = _run(cuda_lib, X, W, lab, "bf16")
     _check_full(X, W, lab, "bf16", loss, dX, dW, lse)
+
+
+def test_linear_ce_dw_grouped_tile_order_against_the_oracle(cuda_lib):
+    """The dW GEMM switches to groups of 8 column tiles when a chunk's X exceeds
+    32 MiB: at hidden 2560 (10 column tiles: a group of 8 and a ragged group of
+    2) a chunk of 8192 tokens is 40 MiB (grouped), the second chunk of 4096
+    tokens 20 MiB (n fastest), the fp32 dW sum carried across them.  lse of
+    every token, the loss, sampled dX rows and rows of dW (labelled rows, rows
+    in the ragged vocabulary tile, random rows) against the oracle."""
+    import torch
+    T, H, V, chunk = 12288, 2560, 300, 8192
+    X = datagen.normal(46, "grX", (T, H), "bf16")
+    W = datagen.normal(46, "grW", (V, H), "bf16", 0.0, 0.05)
+    lab = datagen.labels(46, "grl", T, V, 0.1)
+    loss, dX, dW, lse = _run(cuda_lib, X, W, lab, "bf16", chunk=chunk)
+    o = oracle.linear_ce_rows_fwd(X, W, lab, np.arange(T))
+    valid = lab != -100
+    n = int(valid.sum())
+    assert np.max(np.abs(lse[valid] - o["lse"][valid]) / np.abs(o["lse"][valid])) <= 1e-5
+    assert np.all(lse[~valid] == 0)
+    oloss = float(np.sum(o["loss_term"][valid]) / n)
+    assert abs(loss - oloss) <= LOSS_TOL_BF16 * abs(oloss)
+    olse = np.where(valid, o["lse"], 0.0)
+    vrows = np.unique(np.concatenate([lab[:8][lab[:8] >= 0], lab[8200:8204][lab[8200:8204] >= 0],
+                                      [0, 255, 256, 280, V - 1],
+                                      np.random.default_rng(7).choice(V, 16, replace=False)]))
+    odW = oracle.linear_ce_dw_rows(X, W, lab, olse, vrows)
+    assert oracle.rel_err(host(dW[torch.as_tensor(vrows, device="cuda")]), odW) <= 2e-2
+    rows = np.array([0, 8191, 8192, T - 1])
+    od = oracle.linear_ce_rows(X, W, lab, rows)
+    hdX = host(dX)
+    for i, r in enumerate(rows):
+        if lab[r] == -100:
+            assert np.all(bits(dX)[r] == 0)
+            continue
+        assert oracle.rel_err(hdX[r], od["dX"][i]) <= 2e-2

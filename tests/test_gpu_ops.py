@@ -158,6 +158,25 @@ def test_rope_llama3_full_size(cuda_lib):
         assert oracle.rel_err(hk[b:b + 1, ss], ok) <= 2e-2
 
 
+def test_rope_bwd_llama3_full_size(cuda_lib):
+    """The backward at the same shape: dQ [4, 8192, 32, 128], dK [4, 8192, 8, 128]
+    bf16 rotated by -phi in place, theta 5e5: sampled positions of every batch
+    row against the oracle's rotation with sign -1."""
+    p = workloads.rmsnorm_rope_llama3()["rope"]
+    theta = p.params["theta"]
+    dq, dk = p.make("dq"), p.make("dk")
+    tq, tk = dev(dq), dev(dk)
+    cuda_lib.liger_rope_bwd(tq, tk, None, theta)
+    hq, hk = host(tq), host(tk)
+    ss = np.concatenate([[0, 1, 4095, 8191], np.random.default_rng(1).choice(8192, 60, replace=False)])
+    pos = ss.astype(np.int32)[None, :]
+    for b in range(4):
+        oq = oracle.rope(np.ascontiguousarray(dq[b:b + 1, ss]), theta, sign=-1, pos=pos)
+        ok = oracle.rope(np.ascontiguousarray(dk[b:b + 1, ss]), theta, sign=-1, pos=pos)
+        assert oracle.rel_err(hq[b:b + 1, ss], oq) <= 2e-2
+        assert oracle.rel_err(hk[b:b + 1, ss], ok) <= 2e-2
+
+
 # ------------------------------------------------------------------ SwiGLU
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_swiglu_tiny(cuda_lib, dtype):

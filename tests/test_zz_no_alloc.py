@@ -36,6 +36,7 @@ def _case(lib, dtype, rows, cols):
     raw = lib.load()
     code = lib.LIGER_F32 if dtype == "f32" else lib.LIGER_BF16
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    odx, odw = oracle.rmsnorm_bwd(dy, x, w, 1e-6)
     for _ in range(2):                      # two calls in a row share the built-in scratch
         dx, dw = torch.full_like(tx, 7.0), torch.full_like(tw, 7.0)
         rc = raw.liger_rmsnorm_bwd_noalloc(tdy.data_ptr(), tx.data_ptr(), tw.data_ptr(), rstd.data_ptr(),
@@ -44,11 +45,18 @@ def _case(lib, dtype, rows, cols):
         torch.cuda.synchronize()
         assert oracle.rel_err(host(dx), host(dx_ref)) <= TOL[dtype]
         assert oracle.rel_err(host(dw), host(dw_ref)) <= TOL[dtype]
+        # and against the fp64 oracle directly (the backward from the same stored inputs and
+        # the forward's eps; the kernel reads the rstd the GPU forward wrote)
+        assert oracle.rel_err(host(dx), odx) <= TOL[dtype]
+        assert oracle.rel_err(host(dw), odw) <= TOL[dtype]
     return host(dw), host(dw_ref)
 
 
+# the last two cases are wide enough that the scratch array bounds the number of
+# partial rows: 16 MiB / (4 * 65536) = 64 partial rows for 2048 rows (bf16), and
+# 16 MiB / (4 * 1048576) = 4 partial rows for 64 rows (fp32)
 @pytest.mark.parametrize("dtype,rows,cols", [("bf16", 3000, 4096), ("f32", 257, 1000), ("bf16", 2048, 8192),
-                                             ("bf16", 7, 33)])
+                                             ("bf16", 7, 33), ("bf16", 2048, 65536), ("f32", 64, 1048576)])
 def test_noalloc_matches_workspace_entry_point(cuda_lib, dtype, rows, cols):
     _case(cuda_lib, dtype, rows, cols)
 

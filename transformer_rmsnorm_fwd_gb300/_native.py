@@ -29,6 +29,8 @@ _P, _I64, _F, _D, _INT, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, 
                                ctypes.c_size_t)
 SIGNATURES = {
     "liger_last_error": ([], ctypes.c_char_p),
+    "liger_device_status": ([_P], _INT),
+    "liger_device_status_mark": ([_INT, _P], _INT),
     "liger_rmsnorm_fwd": ([_P, _P, _P, _P, _I64, _I64, _F, _INT, _P], _INT),
     "liger_rmsnorm_bwd_workspace": ([_I64, _I64], _SZ),
     "liger_rmsnorm_bwd": ([_P, _P, _P, _P, _P, _P, _P, _SZ, _I64, _I64, _INT, _P], _INT),
@@ -125,6 +127,20 @@ def _dense(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ------------------------------------------------------------- device status
+def liger_device_status():
+    """Waits for the current stream and raises LigerError (LIGER_ERR_CUDA) if a
+    bounded wait expired in a kernel of the RMSNorm, FusedLinearSwiGLU or fused
+    RMSNorm + QKV + RoPE entry points since the last check (the words are cleared)."""
+    _check(load().liger_device_status(_stream()))
+
+
+def liger_device_status_mark(which: int):
+    """Marks family `which` (0 RMSNorm, 1 FusedLinearSwiGLU, 2 fused QKV) as an
+    expired wait would, on the current stream (a test hook; nothing expires)."""
+    _check(load().liger_device_status_mark(int(which), _stream()))
 
 
 # ------------------------------------------------------------------ RMSNorm

@@ -21,6 +21,13 @@ int check_launch(const char* what);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device addresses (current device) of the library-owned words in which kernels
+// without a per-call workspace header record an expired bounded wait: the staged
+// RMSNorm kernels, FusedLinearSwiGLU's GEMMs and the fused QKV GEMM.
+int rmsnorm_err_word(int** out);
+int lsw_err_word(int** out);
+int qkv_err_word(int** out);
+
 // SM count of the current device (cached per device).
 int sm_count();
 // Maximum dynamic shared memory per block (opt-in) of the current device.
@@ -87,6 +94,10 @@ __device__ __forceinline__ uint4 ldg16_nc(const void* p) {
     return r;
 }
 __device__ __forceinline__ void stg16(void* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
+// 16 bytes of quiet NaNs in the storage type (written where a kernel gave up)
+template <typename T> __device__ __forceinline__ uint4 nan16();
+template <> __device__ __forceinline__ uint4 nan16<float>() { return make_uint4(0x7FC00000u, 0x7FC00000u, 0x7FC00000u, 0x7FC00000u); }
+template <> __device__ __forceinline__ uint4 nan16<__nv_bfloat16>() { return make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u); }
 // streaming load (evict-first): data read once by this kernel
 __device__ __forceinline__ uint4 ldg16_cs(const void* p) {
     uint4 r;

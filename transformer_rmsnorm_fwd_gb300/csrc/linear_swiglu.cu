@@ -25,13 +25,13 @@
 #include "tc_gemm.cuh"
 
 namespace liger {
-namespace {
 
 // Error word of the GEMMs launched here (bounded-wait expiry codes); these
-// entry points take no workspace header, so it is a module variable.
+// entry points take no workspace header, so it is a module variable, read
+// back and cleared by liger_device_status.
 static __device__ int g_lsw_err;
 
-int err_word(int** out) {
+int lsw_err_word(int** out) {
     static std::atomic<int*> addr[64];   // per device; racing threads store the same address
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(LIGER_ERR_CUDA, "no CUDA device");
@@ -44,6 +44,8 @@ int err_word(int** out) {
     *out = a;
     return LIGER_OK;
 }
+
+namespace {
 
 int check_shapes(int64_t T, int64_t H, int64_t I, int dtype, const char* who) {
     if (dtype != LIGER_BF16) return fail(LIGER_ERR_DTYPE, "%s: bf16 only (tensor-core path)", who);
@@ -76,7 +78,7 @@ int fwd_impl(const void* X, const void* Wg, const void* Wu, void* out, void* g_s
     if ((rc = make_map(&mG, Wg, H, I, H, BK, BN / 2))) return rc;
     if ((rc = make_map(&mU, Wu, H, I, H, BK, BN / 2))) return rc;
     int* d_err = nullptr;
-    if ((rc = err_word(&d_err))) return rc;
+    if ((rc = lsw_err_word(&d_err))) return rc;
     EpiParams e{};
     e.err = d_err;
     e.M = static_cast<int>(T);
@@ -200,7 +202,7 @@ extern "C" int liger_fused_linear_swiglu_bwd(const void* X, const void* Wg, cons
         return LIGER_OK;
     }
     int* d_err = nullptr;
-    if (int rc0 = err_word(&d_err)) return rc0;
+    if (int rc0 = lsw_err_word(&d_err)) return rc0;
     __nv_bfloat16* dG = static_cast<__nv_bfloat16*>(ws);
     __nv_bfloat16* dU = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + need / 2);
     int rc;
@@ -265,7 +267,7 @@ extern "C" int liger_fused_linear_swiglu_bwd_saved(const void* X, const void* Wg
         return LIGER_OK;
     }
     int* d_err = nullptr;
-    if (int rc0 = err_word(&d_err)) return rc0;
+    if (int rc0 = lsw_err_word(&d_err)) return rc0;
     __nv_bfloat16* dG = static_cast<__nv_bfloat16*>(ws);
     __nv_bfloat16* dU = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) + need / 2);
     // 1. dG, dU from dh and the saved g, u (the elementwise SwiGLU backward)

@@ -17,6 +17,8 @@
 //    barrier (double-buffered shared slots); the next row is prefetched while
 //    the current one is reduced.  Per-block dw partials go to the workspace
 //    and a second kernel sums them in a fixed order, so dw is deterministic.
+#include <atomic>
+
 #include "common.cuh"
 #include "mbarrier.cuh"
 
@@ -249,8 +251,11 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_reduce(const float* __restrict
 // Rows travel HBM -> shared memory by 1-D bulk copies (cp.async.bulk) into a
 // ring of `nst` buffers per warp (forward) or per block (backward), so that
 // several rows per warp are in flight without holding them in registers.
-// Every wait is bounded; on expiry the kernel records it in g_stage_err,
-// waits (bounded) for the copies it issued and stops.
+// Every wait is bounded; on expiry the kernel records it in g_stage_err
+// (read back and cleared by liger_device_status), waits (bounded) for the
+// copies it issued, writes NaN into the outputs it did not finish (the
+// forward's remaining rows of y and rstd; the backward's remaining rows of dx
+// and its partial row of dw, so that dw is NaN) and stops.
 static __device__ int g_stage_err;
 
 struct Stage {
@@ -293,7 +298,8 @@ __global__ void rmsnorm_fwd_staged(const T* x, const T* __restrict__ w, T* y, fl
     bool ok = __all_sync(0xffffffffu, mbar_wait(wbar, 0));
     const float inv_cols = 1.0f / static_cast<float>(cols);
     int it = 0;
-    for (int64_t r = gw; ok && r < rows; r += stride, ++it) {
+    int64_t r = gw;
+    for (; ok && r < rows; r += stride, ++it) {
         const int s = it % nst;
         const uint32_t ph = static_cast<uint32_t>(it / nst) & 1u;
         if (!__all_sync(0xffffffffu, mbar_wait(mybar + 8u * s, ph))) {
@@ -330,12 +336,19 @@ __global__ void rmsnorm_fwd_staged(const T* x, const T* __restrict__ w, T* y, fl
             }
         }
     }
-    if (!ok && lane == 0) {
-        atomicExch(&g_stage_err, 1);
-        // copies already issued into this warp's ring: the next phase of each buffer
-        for (int s = 0; s < nst; ++s) {
-            const int64_t first = static_cast<int64_t>(it) + ((s - it % nst) + nst) % nst;  // next use of buffer s
-            if (gw + first * stride < rows) mbar_wait(mybar + 8u * s, static_cast<uint32_t>(first / nst) & 1u);
+    if (!ok) {
+        if (lane == 0) {
+            atomicExch(&g_stage_err, 1);
+            // copies already issued into this warp's ring: the next phase of each buffer
+            for (int s = 0; s < nst; ++s) {
+                const int64_t first = static_cast<int64_t>(it) + ((s - it % nst) + nst) % nst;  // next use of buffer s
+                if (gw + first * stride < rows) mbar_wait(mybar + 8u * s, static_cast<uint32_t>(first / nst) & 1u);
+            }
+        }
+        // the rows this warp did not finish: NaN
+        for (; r < rows; r += stride) {
+            for (int v = lane; v < nvec; v += 32) stg16(y + r * cols + static_cast<int64_t>(v) * EPV, nan16<T>());
+            if (rstd != nullptr && lane == 0) rstd[r] = __int_as_float(0x7FC00000);
         }
     }
 }
@@ -497,6 +510,7 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads) rmsnorm_bwd_staged(const
             }
         }
     }
+    float* pr = part + static_cast<int64_t>(blockIdx.x) * cols;
     if (!ok) {
         if (tid == 0) {
             atomicExch(&g_stage_err, 1);
@@ -504,9 +518,13 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads) rmsnorm_bwd_staged(const
             for (int64_t ii = i; ii < i + nst; ++ii)
                 if (r0 + ii < r1) mbar_wait(bars + 8u * static_cast<uint32_t>(ii % nst), static_cast<uint32_t>(ii / nst) & 1u);
         }
+        // the unfinished rows of dx and this block's partial row of dw: NaN
+        for (int64_t r = r0 + i; r < r1; ++r)
+            for (int v = tid; v < nvec; v += NT) stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, nan16<T>());
+        for (int64_t c = static_cast<int64_t>(tid) * 4; c < cols; c += static_cast<int64_t>(NT) * 4)
+            stg16(pr + c, nan16<float>());
         return;
     }
-    float* pr = part + static_cast<int64_t>(blockIdx.x) * cols;
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = j * NT + tid;
@@ -599,6 +617,21 @@ int check_common(int64_t rows, int64_t cols, int dtype) {
 }
 
 }  // namespace
+
+int rmsnorm_err_word(int** out) {
+    static std::atomic<int*> addr[64];   // per device; racing threads store the same address
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(LIGER_ERR_CUDA, "no CUDA device");
+    int* a = addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&a), g_stage_err) != cudaSuccess)
+            return check_launch("rmsnorm error word");
+        addr[dev].store(a, std::memory_order_release);
+    }
+    *out = a;
+    return LIGER_OK;
+}
+
 }  // namespace liger
 
 using namespace liger;

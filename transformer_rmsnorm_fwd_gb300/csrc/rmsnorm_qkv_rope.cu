@@ -39,7 +39,7 @@ struct InvFreqQkv {
 
 static __device__ int g_qkv_err;
 
-int qkv_err_word(int** out) {
+int qkv_err_addr(int** out) {
     static std::atomic<int*> addr[64];   // per device; racing threads store the same address
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(LIGER_ERR_CUDA, "no CUDA device");
@@ -136,6 +136,10 @@ __global__ void __launch_bounds__(256) qkv_prep(const __nv_bfloat16* __restrict_
 }
 
 }  // namespace
+
+// exported to liger_device_status, which reads and clears the word
+int qkv_err_word(int** out) { return qkv_err_addr(out); }
+
 }  // namespace liger
 
 using namespace liger;
@@ -222,7 +226,7 @@ extern "C" int liger_rmsnorm_qkv_rope_fwd(const void* x, const void* w_norm, con
     if ((rc = make_map(&mX, x, H, T, H, BK, BM))) return rc;
     if ((rc = make_map(&mW, wf, H, N, H, BK, B_BOX_ROWS))) return rc;
     int* d_err = nullptr;
-    if ((rc = qkv_err_word(&d_err))) return rc;
+    if ((rc = qkv_err_addr(&d_err))) return rc;
     EpiParams e{};
     e.err = d_err;
     e.M = static_cast<int>(T);
