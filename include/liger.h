@@ -45,14 +45,14 @@
  *     liger_linear_ce_fwd_bwd and liger_linear_ce_two_pass_fwd_bwd (which
  *     wait for their label scan) can be captured in a CUDA graph; their
  *     _async forms do not wait.
- *   - Every wait inside the tensor-core kernels and the staged RMSNorm
- *     kernels is bounded (about 4 s); one that expires (never seen in normal
- *     operation) ends the kernel early, its outputs incomplete.  The linear
- *     cross-entropies then return a NaN loss; the RMSNorm kernels write NaN
- *     into the rows they did not finish (and into dw); RMSNorm,
- *     FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE also record the
- *     expiry in library-owned device words that liger_device_status reads
- *     back and clears.
+ *   - Every wait inside the tensor-core kernels and the staged RMSNorm and
+ *     RoPE kernels is bounded (about 4 s); one that expires (never seen in
+ *     normal operation) ends the kernel early, its outputs incomplete.  The
+ *     linear cross-entropies then return a NaN loss; the RMSNorm and RoPE
+ *     kernels write NaN into the rows they did not finish (and into dw);
+ *     RMSNorm, RoPE, FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE
+ *     also record the expiry in library-owned device words that
+ *     liger_device_status reads back and clears.
  */
 #ifndef LIGER_H
 #define LIGER_H
@@ -86,10 +86,10 @@ const char* liger_last_error(void);
  * The calls return their status when they queue work, before it runs; an
  * expired bounded wait inside a kernel happens later.  The linear
  * cross-entropies report one through their NaN loss.  The staged RMSNorm
- * kernels, FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE record it in
- * three library-owned device words (one per family, per device).  This call
- * queues a one-thread kernel on `stream` that reads and clears the three
- * words, waits for `stream` (cudaStreamSynchronize), and returns LIGER_OK if
+ * kernels, FusedLinearSwiGLU, the fused RMSNorm + QKV + RoPE and the staged
+ * RoPE kernel record it in four library-owned device words (one per family,
+ * per device).  This call queues a one-thread kernel on `stream` that reads
+ * and clears the four words, waits for `stream` (cudaStreamSynchronize), and returns LIGER_OK if
  * none was set, else LIGER_ERR_CUDA with liger_last_error() naming the
  * families whose wait expired.  It covers the work queued on `stream` before
  * it and any other work of the library on the device that has finished by
@@ -102,9 +102,10 @@ const char* liger_last_error(void);
 int liger_device_status(void* stream);
 
 /* Marks family `which` (0 = RMSNorm, 1 = FusedLinearSwiGLU, 2 = fused
- * RMSNorm + QKV + RoPE) as an expired wait would, by a one-thread kernel on
- * `stream`, without any wait expiring: for tests of liger_device_status and
- * of the caller's own handling of it.  LIGER_ERR_SHAPE for another `which`.
+ * RMSNorm + QKV + RoPE, 3 = RoPE) as an expired wait would, by a one-thread
+ * kernel on `stream`, without any wait expiring: for tests of
+ * liger_device_status and of the caller's own handling of it.
+ * LIGER_ERR_SHAPE for another `which`.
  */
 int liger_device_status_mark(int which, void* stream);
 

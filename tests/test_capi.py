@@ -112,6 +112,6 @@ def test_rmsnorm_qkv_rope_host_checks(lib):
 
 def test_device_status_marker_checks_its_family(lib):
     # an unknown family is rejected before any CUDA call
-    assert lib.liger_device_status_mark(3, None) == -2
+    assert lib.liger_device_status_mark(4, None) == -2
     assert lib.liger_device_status_mark(-1, None) == -2
     assert "which" in _err(lib)

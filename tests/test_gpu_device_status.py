@@ -1,6 +1,6 @@
 """liger_device_status: the read-back of the library-owned words in which the
-staged RMSNorm kernels, FusedLinearSwiGLU and the fused RMSNorm + QKV + RoPE
-record an expired bounded wait.  Normal calls leave every word clear; a word
+staged RMSNorm and RoPE kernels, FusedLinearSwiGLU and the fused RMSNorm +
+QKV + RoPE record an expired bounded wait.  Normal calls leave every word clear; a word
 marked by the test hook (nothing expires, no GPU fault) is reported as
 LIGER_ERR_CUDA naming its family, and is clear again after the read."""
 import pytest
@@ -23,10 +23,12 @@ def test_clear_after_normal_calls(cuda_lib):
     Wg = dev(datagen.normal(51, "dsg", (512, 4096), "bf16", 0.0, 0.02))
     out = torch.empty(300, 512, dtype=torch.bfloat16, device="cuda")
     cuda_lib.liger_fused_linear_swiglu_fwd(x, Wg, Wg, out)
+    qk = dev(datagen.normal(51, "dsq", (1, 300, 4, 128), "bf16"))
+    cuda_lib.liger_rope_fwd(qk, None, None, 1e4)
     cuda_lib.liger_device_status()          # raises if any word is set
 
 
-@pytest.mark.parametrize("which,name", [(0, "RMSNorm"), (1, "FusedLinearSwiGLU"), (2, "QKV")])
+@pytest.mark.parametrize("which,name", [(0, "RMSNorm"), (1, "FusedLinearSwiGLU"), (2, "QKV"), (3, "RoPE")])
 def test_marked_word_is_reported_once(cuda_lib, which, name):
     cuda_lib.liger_device_status()
     cuda_lib.liger_device_status_mark(which)

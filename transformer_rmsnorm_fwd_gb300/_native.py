@@ -132,14 +132,15 @@ def _dense(*ts):
 # ------------------------------------------------------------- device status
 def liger_device_status():
     """Waits for the current stream and raises LigerError (LIGER_ERR_CUDA) if a
-    bounded wait expired in a kernel of the RMSNorm, FusedLinearSwiGLU or fused
-    RMSNorm + QKV + RoPE entry points since the last check (the words are cleared)."""
+    bounded wait expired in a kernel of the RMSNorm, RoPE, FusedLinearSwiGLU or
+    fused RMSNorm + QKV + RoPE entry points since the last check (the words are
+    cleared)."""
     _check(load().liger_device_status(_stream()))
 
 
 def liger_device_status_mark(which: int):
-    """Marks family `which` (0 RMSNorm, 1 FusedLinearSwiGLU, 2 fused QKV) as an
-    expired wait would, on the current stream (a test hook; nothing expires)."""
+    """Marks family `which` (0 RMSNorm, 1 FusedLinearSwiGLU, 2 fused QKV, 3 RoPE)
+    as an expired wait would, on the current stream (a test hook; nothing expires)."""
     _check(load().liger_device_status_mark(int(which), _stream()))
 
 

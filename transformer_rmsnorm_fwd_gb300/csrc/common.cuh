@@ -23,10 +23,12 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Device addresses (current device) of the library-owned words in which kernels
 // without a per-call workspace header record an expired bounded wait: the staged
-// RMSNorm kernels, FusedLinearSwiGLU's GEMMs and the fused QKV GEMM.
+// RMSNorm kernels, FusedLinearSwiGLU's GEMMs, the fused QKV GEMM and the staged
+// RoPE kernel.
 int rmsnorm_err_word(int** out);
 int lsw_err_word(int** out);
 int qkv_err_word(int** out);
+int rope_err_word(int** out);
 
 // SM count of the current device (cached per device).
 int sm_count();
@@ -58,10 +60,29 @@ __device__ __forceinline__ void unpack(const uint4& u, float (&f)[8]) {
     f[0] = bf_lo(u.x); f[1] = bf_hi(u.x); f[2] = bf_lo(u.y); f[3] = bf_hi(u.y);
     f[4] = bf_lo(u.z); f[5] = bf_hi(u.z); f[6] = bf_lo(u.w); f[7] = bf_hi(u.w);
 }
+// The same as pairs, for the packed fp32x2 arithmetic (__ffma2_rn, __fmul2_rn)
+__device__ __forceinline__ void unpack2(const uint4& u, float2 (&f)[2]) {
+    f[0] = make_float2(__uint_as_float(u.x), __uint_as_float(u.y));
+    f[1] = make_float2(__uint_as_float(u.z), __uint_as_float(u.w));
+}
+__device__ __forceinline__ void unpack2(const uint4& u, float2 (&f)[4]) {
+    f[0] = make_float2(bf_lo(u.x), bf_hi(u.x));
+    f[1] = make_float2(bf_lo(u.y), bf_hi(u.y));
+    f[2] = make_float2(bf_lo(u.z), bf_hi(u.z));
+    f[3] = make_float2(bf_lo(u.w), bf_hi(u.w));
+}
 // round-to-nearest-even pair -> packed bf16x2 (low half = first element)
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint4 pack2(const float2 (&f)[2]) {
+    return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                      __float_as_uint(f[1].y));
+}
+__device__ __forceinline__ uint4 pack2(const float2 (&f)[4]) {
+    return make_uint4(pack_bf2(f[0].x, f[0].y), pack_bf2(f[1].x, f[1].y), pack_bf2(f[2].x, f[2].y),
+                      pack_bf2(f[3].x, f[3].y));
 }
 __device__ __forceinline__ uint4 pack(const float (&f)[8]) {
     return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));

@@ -6,17 +6,22 @@
 // y = x * rstd * w.  The backward is the derivative of that forward.
 //
 // GB300 design (HBM-bound, ~2 bytes/element each way in bf16):
-//  * forward: one warp per row, the row held packed in registers as 16-byte
-//    vectors (VPL vectors per lane; 64 registers for a 4096-wide bf16 row),
-//    w re-read per row through L1, one warp-shuffle reduction, no shared
-//    memory and no block barrier; a persistent grid of (SMs x resident
-//    blocks) warps strides over rows.
-//  * backward: one block per contiguous group of rows; each thread owns
-//    fixed columns and keeps its share of dw in fp32 registers across the
-//    group's rows (no atomics); the row dot product is a shuffle + one
-//    barrier (double-buffered shared slots); the next row is prefetched while
-//    the current one is reduced.  Per-block dw partials go to the workspace
-//    and a second kernel sums them in a fixed order, so dw is deterministic.
+//  * forward (rows of whole 16-byte vectors that fit the ring): one warp per
+//    row, each warp a ring of row buffers in shared memory filled by 1-D bulk
+//    copies (cp.async.bulk, completion on an mbarrier), so several rows per
+//    warp are in flight without registers; one warp-shuffle reduction, no
+//    block barrier.  Other widths: the row held in registers (warp per row)
+//    or a block per row.
+//  * backward (the same rows): a persistent block per contiguous group of
+//    rows, its (dy, x) rows brought into a ring of 4 buffers by bulk copies;
+//    each thread owns fixed 16-byte column vectors and keeps its share of dw
+//    in fp32 registers across the group's rows (no atomics); the dot products
+//    of two rows are reduced together (shuffles, one block barrier), then the
+//    two rows are read again from shared memory for dx and dw; the float
+//    arithmetic runs on column pairs with the packed fp32x2 instructions.
+//    Other widths: the row in registers, or a generic loop.
+//  * dw: per-block partial rows (workspace) summed by a second kernel in a
+//    fixed order, so dw is deterministic.
 #include <atomic>
 
 #include "common.cuh"
@@ -247,6 +252,58 @@ __global__ void __launch_bounds__(256) rmsnorm_dw_reduce(const float* __restrict
     }
 }
 
+// The same sum for rows of a multiple of 4 columns, 4 columns per thread:
+// block of 32 warps over 128 columns, warp w summing the partial rows w, w +
+// 32, ... in ascending order, the 32 slice sums then combined in slice order
+// (deterministic for a given number of partial rows).  Many independent
+// 16-byte loads per SM instead of one 4-byte chain per thread.
+template <typename T>
+__global__ void __launch_bounds__(1024) rmsnorm_dw_reduce4(const float* __restrict__ part, T* __restrict__ dw,
+                                                           int nparts, int cols) {
+    __shared__ float4 red[32][32];
+    const int lane = threadIdx.x & 31, sl = threadIdx.x >> 5;
+    const int n4 = cols >> 2;
+    const int c4 = blockIdx.x * 32 + lane;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c4 < n4) {
+        const float4* p = reinterpret_cast<const float4*>(part) + c4;
+#pragma unroll 4
+        for (int b = sl; b < nparts; b += 32) {
+            const float4 v = p[static_cast<int64_t>(b) * n4];
+            s.x += v.x;
+            s.y += v.y;
+            s.z += v.z;
+            s.w += v.w;
+        }
+    }
+    red[sl][lane] = s;
+    __syncthreads();
+    if (sl == 0 && c4 < n4) {
+        float4 t = red[0][lane];
+        for (int i = 1; i < 32; ++i) {
+            const float4 v = red[i][lane];
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        T* o = dw + static_cast<int64_t>(c4) * 4;
+        stf(o, t.x);
+        stf(o + 1, t.y);
+        stf(o + 2, t.z);
+        stf(o + 3, t.w);
+    }
+}
+
+// dw from nparts partial rows, with the 4-column form where the rows allow it.
+template <typename T>
+void launch_dw_reduce(const float* part, T* dw, int nparts, int cols, cudaStream_t st) {
+    if (cols % 4 == 0)
+        rmsnorm_dw_reduce4<T><<<static_cast<unsigned>(ceil_div(cols / 4, 32)), 1024, 0, st>>>(part, dw, nparts, cols);
+    else
+        rmsnorm_dw_reduce<T><<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, st>>>(part, dw, nparts, cols);
+}
+
 // ------------------------------------------------- rows staged by bulk copy
 // Rows travel HBM -> shared memory by 1-D bulk copies (cp.async.bulk) into a
 // ring of `nst` buffers per warp (forward) or per block (backward), so that
@@ -412,101 +469,140 @@ int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
 
 constexpr int kBwdStagedMaxThreads = 256;
 
-// Staged backward: the same arithmetic as rmsnorm_bwd_block, with the rows
-// of dy and x brought into a ring of nst shared-memory buffers by 1-D bulk
-// copies (nst rows in flight per block whatever the SM clock).  Each thread
-// copies its column vectors of the row into registers before the row's
-// reduction barrier, so after that barrier thread 0 refills the buffer at once.
+// Row r of dy and x into ring buffer s (one mbarrier per buffer).
+template <typename T>
+__device__ __forceinline__ void bwd_issue_row(uint8_t* sm, uint32_t bars, const T* dy, const T* x, int64_t r, int s,
+                                              uint32_t rb, int cols) {
+    const uint32_t bar = bars + 8u * static_cast<uint32_t>(s);
+    uint8_t* dst = sm + static_cast<size_t>(s) * 2 * rb;
+    mbar_expect_tx(bar, 2 * rb);
+    bulk_g2s(smem_u32(dst), dy + r * cols, rb, bar);
+    bulk_g2s(smem_u32(dst + rb), x + r * cols, rb, bar);
+}
+
+// Staged backward, two rows per block barrier: the block reduces the dot
+// products of its rows i and i + 1 together (two independent shuffle trees,
+// one barrier), then reads both rows again from shared memory for dx and dw,
+// so no row is held in registers across the barrier.  After the barrier of
+// rows (i, i + 1) every thread is past rows (i - 2, i - 1), whose buffers
+// thread 0 refills with rows i - 2 + nst and i - 1 + nst (nst >= 4).  Each
+// block takes a contiguous group of rows (rows interleaved across blocks
+// measured no faster).
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kBwdStagedMaxThreads) rmsnorm_bwd_staged(const T* dy, const T* __restrict__ x,
-                                                          const T* __restrict__ w, const float* __restrict__ rstd,
-                                                          T* dx, float* __restrict__ part, int64_t rows, int cols,
-                                                          int64_t rows_per_block, int nst) {
+__global__ void __launch_bounds__(kBwdStagedMaxThreads, 3) rmsnorm_bwd_staged2(const T* dy, const T* __restrict__ x,
+                                                           const T* __restrict__ w, const float* __restrict__ rstd,
+                                                           T* dx, float* __restrict__ part, int64_t rows, int cols,
+                                                           int64_t rows_per_block, int nst) {
     constexpr int EPV = Vec<T>::N;
     extern __shared__ __align__(128) uint8_t sm[];
-    __shared__ float red[2][32];
+    __shared__ float red[2][2][32];
     const int tid = threadIdx.x, NT = blockDim.x, lane = tid & 31, wid = tid >> 5, NW = NT >> 5;
     const int nvec = cols / EPV;
     const uint32_t rb = static_cast<uint32_t>(cols) * sizeof(T);   // row bytes (multiple of 16)
     const uint32_t bars = smem_u32(sm + static_cast<size_t>(nst) * 2 * rb);
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows_per_block;
-    const int64_t r1 = min(rows, r0 + rows_per_block);
+    const int64_t nr = min(rows, r0 + rows_per_block) - r0;   // this block's rows: r0 + i, i < nr
+    auto row_of = [&](int64_t i) { return r0 + i; };
     if (tid == 0)
         for (int s = 0; s < nst; ++s) mbar_init(bars + 8u * s, 1);
     mbar_init_fence();
     __syncthreads();
-    auto issue = [&](int64_t i) {   // row r0 + i into buffer i % nst: dy, then x
-        const int64_t r = r0 + i;
-        if (r >= r1) return;
-        const uint32_t bar = bars + 8u * static_cast<uint32_t>(i % nst);
-        uint8_t* dst = sm + static_cast<size_t>(i % nst) * 2 * rb;
-        mbar_expect_tx(bar, 2 * rb);
-        bulk_g2s(smem_u32(dst), dy + r * cols, rb, bar);
-        bulk_g2s(smem_u32(dst + rb), x + r * cols, rb, bar);
-    };
     if (tid == 0)
-        for (int s = 0; s < nst; ++s) issue(s);
-    uint4 wv[VPT];
-    float dwa[VPT][EPV];
+        for (int s = 0; s < nst && s < nr; ++s) bwd_issue_row(sm, bars, dy, x, row_of(s), s, rb, cols);
+    int64_t issued = nst;   // rows 0 .. issued-1 have been asked for (thread 0's view; same on all threads)
+    // arithmetic on pairs of columns with the packed fp32x2 instructions (half the
+    // floating-point instruction count of scalar code)
+    constexpr int NP = EPV / 2;
+    float2 wf[VPT][NP], dwa[VPT][NP];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = j * NT + tid;
-        wv[j] = v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0);
+        unpack2(v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0), wf[j]);
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) dwa[j][e] = 0.f;
+        for (int e = 0; e < NP; ++e) dwa[j][e] = make_float2(0.f, 0.f);
     }
     const float inv_cols = 1.0f / static_cast<float>(cols);
     bool ok = true;
     int64_t i = 0;
-    for (; r0 + i < r1; ++i) {
-        const int64_t r = r0 + i;
-        const int s = static_cast<int>(i % nst);
-        const bool got = mbar_wait(bars + 8u * s, static_cast<uint32_t>(i / nst) & 1u);
-        const float rs = rstd[r];
-        const uint8_t* bdy = sm + static_cast<size_t>(s) * 2 * rb;
-        const uint8_t* bx = bdy + rb;
-        uint4 cx[VPT], cdy[VPT];
-        float gx = 0.f;
+    int it = 0;
+    for (; i < nr; i += 2, ++it) {
+        const bool two = i + 1 < nr;
+        const int s0 = static_cast<int>(i % nst), s1 = static_cast<int>((i + 1) % nst);
+        bool got = mbar_wait(bars + 8u * s0, static_cast<uint32_t>(i / nst) & 1u);
+        if (two) got = got && mbar_wait(bars + 8u * s1, static_cast<uint32_t>((i + 1) / nst) & 1u);
+        const uint8_t* b0 = sm + static_cast<size_t>(s0) * 2 * rb;
+        const uint8_t* b1 = sm + static_cast<size_t>(s1) * 2 * rb;
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+        if (got) {
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = j * NT + tid;
-            cx[j] = v < nvec && got ? *reinterpret_cast<const uint4*>(bx + static_cast<size_t>(v) * 16) : make_uint4(0, 0, 0, 0);
-            cdy[j] = v < nvec && got ? *reinterpret_cast<const uint4*>(bdy + static_cast<size_t>(v) * 16) : make_uint4(0, 0, 0, 0);
-            float fx[EPV], fd[EPV], fw[EPV];
-            unpack(cx[j], fx);
-            unpack(cdy[j], fd);
-            unpack(wv[j], fw);
+            for (int j = 0; j < VPT; ++j) {
+                const int v = j * NT + tid;
+                if (v < nvec) {
+                    float2 fx[NP], fd[NP];
+                    unpack2(*reinterpret_cast<const uint4*>(b0 + static_cast<size_t>(v) * 16), fd);
+                    unpack2(*reinterpret_cast<const uint4*>(b0 + rb + static_cast<size_t>(v) * 16), fx);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) gx = fmaf(fd[e] * fw[e], fx[e], gx);
+                    for (int e = 0; e < NP; ++e) a0 = __ffma2_rn(__fmul2_rn(fd[e], wf[j][e]), fx[e], a0);
+                    if (two) {
+                        unpack2(*reinterpret_cast<const uint4*>(b1 + static_cast<size_t>(v) * 16), fd);
+                        unpack2(*reinterpret_cast<const uint4*>(b1 + rb + static_cast<size_t>(v) * 16), fx);
+#pragma unroll
+                        for (int e = 0; e < NP; ++e) a1 = __ffma2_rn(__fmul2_rn(fd[e], wf[j][e]), fx[e], a1);
+                    }
+                }
+            }
         }
-        gx = warp_sum(gx);
-        if (lane == 0) red[i & 1][wid] = gx;
-        // the row's partial sums are published; every thread has its vectors of buffer s in registers
+        float g0 = a0.x + a0.y, g1 = a1.x + a1.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g0 += __shfl_xor_sync(0xffffffffu, g0, o);
+            g1 += __shfl_xor_sync(0xffffffffu, g1, o);
+        }
+        if (lane == 0) {
+            red[it & 1][0][wid] = g0;
+            red[it & 1][1][wid] = g1;
+        }
+        // both rows' partial sums are published, and every thread is past rows i-2, i-1
         if (!__syncthreads_and(got ? 1 : 0)) {
             ok = false;
             break;
         }
-        if (tid == 0) {
-            fence_proxy_async_smem();   // the reads of buffer s happen before the copy overwrites it
-            issue(i + nst);
+        if (tid == 0 && i >= 2) {
+            fence_proxy_async_smem();   // the reads of those buffers happen before the copies overwrite them
+            if (i - 2 + nst < nr)
+                bwd_issue_row(sm, bars, dy, x, row_of(i - 2 + nst), static_cast<int>((i - 2) % nst), rb, cols);
+            if (i - 1 + nst < nr)
+                bwd_issue_row(sm, bars, dy, x, row_of(i - 1 + nst), static_cast<int>((i - 1) % nst), rb, cols);
         }
-        float tot = 0.f;
-        for (int q = 0; q < NW; ++q) tot += red[i & 1][q];
-        const float c = rs * rs * rs * inv_cols * tot;
+        if (i >= 2) issued = i + nst;
+        float t0 = 0.f, t1 = 0.f;
+        for (int q = 0; q < NW; ++q) {
+            t0 += red[it & 1][0][q];
+            t1 += red[it & 1][1][q];
+        }
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = j * NT + tid;
-            if (v < nvec) {
-                float fx[EPV], fd[EPV], fw[EPV], o[EPV];
-                unpack(cx[j], fx);
-                unpack(cdy[j], fd);
-                unpack(wv[j], fw);
+        for (int rr = 0; rr < 2; ++rr) {
+            if (rr == 1 && !two) break;
+            const int64_t r = row_of(i + rr);
+            const float rs = rstd[r];
+            const float c = rs * rs * rs * inv_cols * (rr ? t1 : t0);
+            const float2 rs2 = make_float2(rs, rs), nc2 = make_float2(-c, -c);
+            const uint8_t* bb = rr ? b1 : b0;
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    o[e] = rs * (fd[e] * fw[e]) - c * fx[e];
-                    dwa[j][e] = fmaf(fd[e] * fx[e], rs, dwa[j][e]);
+            for (int j = 0; j < VPT; ++j) {
+                const int v = j * NT + tid;
+                if (v < nvec) {
+                    float2 fx[NP], fd[NP], o[NP];
+                    unpack2(*reinterpret_cast<const uint4*>(bb + static_cast<size_t>(v) * 16), fd);
+                    unpack2(*reinterpret_cast<const uint4*>(bb + rb + static_cast<size_t>(v) * 16), fx);
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) {
+                        // dx = rs (dy w) - c x;  dw += (dy x) rs
+                        o[e] = __ffma2_rn(nc2, fx[e], __fmul2_rn(rs2, __fmul2_rn(fd[e], wf[j][e])));
+                        dwa[j][e] = __ffma2_rn(__fmul2_rn(fd[e], fx[e]), rs2, dwa[j][e]);
+                    }
+                    stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, pack2(o));
                 }
-                stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, pack(o));
             }
         }
     }
@@ -514,13 +610,14 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads) rmsnorm_bwd_staged(const
     if (!ok) {
         if (tid == 0) {
             atomicExch(&g_stage_err, 1);
-            // copies in flight: rows i .. i+nst-1 (the refill after the failed barrier never happened)
-            for (int64_t ii = i; ii < i + nst; ++ii)
-                if (r0 + ii < r1) mbar_wait(bars + 8u * static_cast<uint32_t>(ii % nst), static_cast<uint32_t>(ii / nst) & 1u);
+            // copies in flight: rows i .. issued-1
+            for (int64_t ii = i; ii < min(issued, nr); ++ii)
+                mbar_wait(bars + 8u * static_cast<uint32_t>(ii % nst), static_cast<uint32_t>(ii / nst) & 1u);
         }
         // the unfinished rows of dx and this block's partial row of dw: NaN
-        for (int64_t r = r0 + i; r < r1; ++r)
-            for (int v = tid; v < nvec; v += NT) stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, nan16<T>());
+        for (int64_t ii = i; ii < nr; ++ii)
+            for (int v = tid; v < nvec; v += NT)
+                stg16(dx + row_of(ii) * cols + static_cast<int64_t>(v) * EPV, nan16<T>());
         for (int64_t c = static_cast<int64_t>(tid) * 4; c < cols; c += static_cast<int64_t>(NT) * 4)
             stg16(pr + c, nan16<float>());
         return;
@@ -530,9 +627,9 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads) rmsnorm_bwd_staged(const
         const int v = j * NT + tid;
         if (v < nvec) {
 #pragma unroll
-            for (int e = 0; e < EPV; e += 4) {
-                float q[4] = {dwa[j][e], dwa[j][e + 1], dwa[j][e + 2], dwa[j][e + 3]};
-                stg16(pr + static_cast<int64_t>(v) * EPV + e, pack(q));
+            for (int e = 0; e < NP; e += 2) {
+                const float2 q2[2] = {dwa[j][e], dwa[j][e + 1]};
+                stg16(pr + static_cast<int64_t>(v) * EPV + 2 * e, pack2(q2));
             }
         }
     }
@@ -558,11 +655,11 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
     T* dxp = static_cast<T*>(dx);
     bool done = false;
     const int rbytes = cols * static_cast<int>(sizeof(T));
-    if (cols % EPV == 0 && cols / EPV <= 2 * kBwdStagedMaxThreads && bwd_staged_smem(rbytes, 2) <= 100u * 1024u) {
+    if (cols % EPV == 0 && cols / EPV <= 2 * kBwdStagedMaxThreads && bwd_staged_smem(rbytes, 4) <= 100u * 1024u) {
         // staged path: up to 4 rows in flight per block, about 3 blocks per SM at 8 KB rows
         const int nvec = cols / EPV;
-        int nst = 4;
-        while (nst > 2 && bwd_staged_smem(rbytes, nst) > 72u * 1024u) --nst;
+        // a ring of 4 (dy, x) row pairs: two rows in use, two in flight
+        const int nst = 4;
         const size_t ssm = bwd_staged_smem(rbytes, nst);
         auto go = [&](auto kern, int vpt) -> int {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm)) !=
@@ -583,8 +680,8 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
         };
         int rc0 = LIGER_OK;
         // one column vector per thread up to kBwdStagedMaxThreads vectors (more warps per SM)
-        if (nvec <= kBwdStagedMaxThreads) rc0 = go(rmsnorm_bwd_staged<T, 1>, 1);
-        else rc0 = go(rmsnorm_bwd_staged<T, 2>, 2);
+        if (nvec <= kBwdStagedMaxThreads) rc0 = go(rmsnorm_bwd_staged2<T, 1>, 1);
+        else rc0 = go(rmsnorm_bwd_staged2<T, 2>, 2);
         if (rc0) return rc0;
     }
     if (!done && cols % EPV == 0) {
@@ -604,8 +701,7 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
                                                                             rpb);
     int rc = check_launch("rmsnorm_bwd");
     if (rc) return rc;
-    rmsnorm_dw_reduce<T><<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, st>>>(
-        part, static_cast<T*>(dw), static_cast<int>(grid_used), cols);
+    launch_dw_reduce<T>(part, static_cast<T*>(dw), static_cast<int>(grid_used), cols, st);
     return check_launch("rmsnorm_dw_reduce");
 }
 
@@ -746,8 +842,7 @@ int launch_bwd_noalloc(const void* dy, const void* x, const void* w, const float
                                                                             rpb);
     int rc = check_launch("rmsnorm_bwd_noalloc");
     if (rc) return rc;
-    rmsnorm_dw_reduce<T><<<static_cast<unsigned>(ceil_div(cols, 32)), 256, 0, st>>>(
-        part, static_cast<T*>(dw), static_cast<int>(grid), cols);
+    launch_dw_reduce<T>(part, static_cast<T*>(dw), static_cast<int>(grid), cols, st);
     return check_launch("rmsnorm_dw_reduce");
 }
 

@@ -8,11 +8,18 @@
 // theta^(-2i/D) (standard RoPE; the pages give none).
 //
 // GB300 design (HBM-bound: every element read and written once):
-//  * one block per group of npos positions (4 at head_dim 128, so that each
-//    thread forms one angle) and batch group: the angles are formed once in
-//    shared memory and reused by every head of Q and K and, when the
-//    positions are implicit (p = s), by every batch row -- 160x reuse at
-//    Llama-3-8B shapes -- so the fp64 angle work is negligible;
+//  * staged form (16-byte vectors, the common case): one block per tile of
+//    consecutive tokens of one batch row (about 32 KB of Q and K rows); the
+//    tile is brought into shared memory by 1-D bulk copies issued at the
+//    block's start, while the threads form the tile's angles, so a whole
+//    tile per block is in flight without registers: the kernel keeps HBM
+//    busy at the power-capped SM clock of a long training step, where a
+//    register-bound form loses a quarter of its bandwidth;
+//  * otherwise (scalar elements, or a tile that does not fit): one block per
+//    group of npos positions (4 at head_dim 128, so that each thread forms
+//    one angle) and batch group: the angles are formed once in shared memory
+//    and reused by every head of Q and K and, when the positions are
+//    implicit (p = s), by every batch row;
 //  * the inverse frequencies theta^(-2i/D) are computed on the host in
 //    double precision and passed as a kernel parameter;
 //  * angle phi = p * inv_freq in double, reduced modulo 2 pi in double
@@ -21,13 +28,18 @@
 //    fp32 p * inv_freq would err by ~p ulp;
 //  * each thread rotates 16-byte vectors (half-split pairing: the two halves
 //    of a head; interleaved pairing: four adjacent pairs); a warp covers
-//    whole 128-byte lines.
+//    whole 128-byte lines; the block's (vector, token) tasks are dealt to the
+//    threads in turn, so every thread gets the same share whatever the head
+//    counts (40 heads of 128 give 320 vector slots per token).
 // The extended entry points add the interleaved pairing (2i, 2i+1), per-token
 // strides (Q and K as views into a packed QKV buffer) and caller-supplied
 // cos/sin tables (for scaled frequency schedules).
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
+#include "mbarrier.cuh"
 #include "rope_angle.cuh"
 
 namespace liger {
@@ -87,56 +99,67 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(const RopeArgs a, const 
     if (VEC) {
         constexpr int EPV = Vec<T>::N;
         // half-split: a slot is the pair of vectors (v, v + D/2) of a head; interleaved:
-        // one vector.  Each thread decodes its slots once; the loop over the block's
-        // positions and batch rows only adds token offsets.
+        // one vector.  The block's work is nslot x (positions x batch rows) tasks, dealt
+        // to the threads in turn (task t: slot t mod nslot, row t / nslot), so that every
+        // thread gets the same share whatever the head counts (40 heads of 128 at 8
+        // vectors per head: 320 slots, 1.25 per thread per row); a thread steps through
+        // its tasks by adding kThreads to (slot, row) instead of dividing.
         const int vph = INTER ? D / EPV : half / EPV;
         const int nslot = H * vph;
-        for (int slot = threadIdx.x; slot < nslot; slot += kThreads) {
+        const int ntask = nslot * np * nb;
+        int slot = threadIdx.x, row = 0;
+        while (slot >= nslot) {
+            slot -= nslot;
+            ++row;
+        }
+        for (int t = threadIdx.x; t < ntask; t += kThreads) {
             const int h = slot / vph, v = slot - h * vph;
+            const int pp = row / nb, bl = row - pp * nb;
             const bool isq = h < Hq;
             T* hb = isq ? q + static_cast<int64_t>(h) * D + v * EPV : k + static_cast<int64_t>(h - Hq) * D + v * EPV;
             const int64_t ts = isq ? a.q_ts : a.k_ts;
             const int coff = INTER ? (v * EPV) >> 1 : v * EPV;   // first angle index of this slot
-            for (int pp = 0; pp < np; ++pp) {
-                for (int bl = 0; bl < nb; ++bl) {
-                    T* pa = hb + (static_cast<int64_t>(b0 + bl) * S + s0 + pp) * ts;
-                    const float4* c4 = reinterpret_cast<const float4*>(cs + (pp * na + (a.pos ? bl : 0)) * half + coff);
-                    if (INTER) {
-                        float e[EPV];
-                        unpack(ldg16(pa), e);
+            slot += kThreads;
+            while (slot >= nslot) {
+                slot -= nslot;
+                ++row;
+            }
+            T* pa = hb + (static_cast<int64_t>(b0 + bl) * S + s0 + pp) * ts;
+            const float4* c4 = reinterpret_cast<const float4*>(cs + (pp * na + (a.pos ? bl : 0)) * half + coff);
+            if (INTER) {
+                float e[EPV];
+                unpack(ldg16(pa), e);
 #pragma unroll
-                        for (int j = 0; j < EPV / 2; j += 2) {
-                            const float4 r = c4[j >> 1];   // two (cos, sin) pairs
-                            float x0 = e[2 * j], x1 = e[2 * j + 1];
-                            e[2 * j] = x0 * r.x - x1 * r.y;
-                            e[2 * j + 1] = x1 * r.x + x0 * r.y;
-                            x0 = e[2 * j + 2];
-                            x1 = e[2 * j + 3];
-                            e[2 * j + 2] = x0 * r.z - x1 * r.w;
-                            e[2 * j + 3] = x1 * r.z + x0 * r.w;
-                        }
-                        stg16(pa, pack(e));
-                    } else {
-                        T* pb = pa + half;
-                        float av[EPV], bv[EPV];
-                        // the two halves of a head sit in one 256-byte block: ask L2 for all of it
-                        unpack(ldg16_pf256(pa), av);
-                        unpack(ldg16_pf256(pb), bv);
-#pragma unroll
-                        for (int e = 0; e < EPV; e += 2) {
-                            const float4 r = c4[e >> 1];
-                            float x0 = av[e], x1 = bv[e];
-                            av[e] = x0 * r.x - x1 * r.y;
-                            bv[e] = x1 * r.x + x0 * r.y;
-                            x0 = av[e + 1];
-                            x1 = bv[e + 1];
-                            av[e + 1] = x0 * r.z - x1 * r.w;
-                            bv[e + 1] = x1 * r.z + x0 * r.w;
-                        }
-                        stg16(pa, pack(av));
-                        stg16(pb, pack(bv));
-                    }
+                for (int j = 0; j < EPV / 2; j += 2) {
+                    const float4 r = c4[j >> 1];   // two (cos, sin) pairs
+                    float x0 = e[2 * j], x1 = e[2 * j + 1];
+                    e[2 * j] = x0 * r.x - x1 * r.y;
+                    e[2 * j + 1] = x1 * r.x + x0 * r.y;
+                    x0 = e[2 * j + 2];
+                    x1 = e[2 * j + 3];
+                    e[2 * j + 2] = x0 * r.z - x1 * r.w;
+                    e[2 * j + 3] = x1 * r.z + x0 * r.w;
                 }
+                stg16(pa, pack(e));
+            } else {
+                T* pb = pa + half;
+                float av[EPV], bv[EPV];
+                // the two halves of a head sit in one 256-byte block: ask L2 for all of it
+                unpack(ldg16_pf256(pa), av);
+                unpack(ldg16_pf256(pb), bv);
+#pragma unroll
+                for (int e = 0; e < EPV; e += 2) {
+                    const float4 r = c4[e >> 1];
+                    float x0 = av[e], x1 = bv[e];
+                    av[e] = x0 * r.x - x1 * r.y;
+                    bv[e] = x1 * r.x + x0 * r.y;
+                    x0 = av[e + 1];
+                    x1 = bv[e + 1];
+                    av[e + 1] = x0 * r.z - x1 * r.w;
+                    bv[e + 1] = x1 * r.z + x0 * r.w;
+                }
+                stg16(pa, pack(av));
+                stg16(pb, pack(bv));
             }
         }
     } else {
@@ -157,6 +180,126 @@ __global__ void __launch_bounds__(kThreads) rope_kernel(const RopeArgs a, const 
             stf(pb, x1 * r.x + x0 * r.y);
         }
     }
+}
+
+// ------------------------------------------------------------ staged form
+// One block per tile of npos consecutive tokens of one batch row.  Thread 0
+// bulk-copies the tile's Q and K token rows into shared memory (two 1-D copies
+// per token, all counted on one mbarrier) while every thread forms the tile's
+// angles; the threads then rotate 16-byte vectors read from shared memory and
+// store them in place.  A whole tile (about 32 KB) is in flight per block
+// without holding it in registers, so the loads do not wait on the issue rate
+// of the threads, whatever the SM clock.  The angle table is laid out
+// [token][element of a vector][vector] so that the threads of a quarter warp,
+// which hold consecutive vectors of a head, read consecutive words.
+// The wait is bounded; on expiry the kernel records it in g_rope_err (read and
+// cleared by liger_device_status), waits (bounded) for its copies, writes NaN
+// into its tile and stops.
+static __device__ int g_rope_err;
+
+template <typename T, bool INTER>
+__global__ void __launch_bounds__(kThreads) rope_staged_kernel(const RopeArgs a, const __grid_constant__ InvFreq f) {
+    constexpr int EPV = Vec<T>::N;
+    constexpr int APV = INTER ? EPV / 2 : EPV;   // angles per 16-byte vector
+    extern __shared__ __align__(128) uint8_t sm[];
+    T* q = static_cast<T*>(a.q);
+    T* k = static_cast<T*>(a.k);
+    const int D = a.D, half = D >> 1, S = a.S, Hq = a.Hq, Hk = a.Hk, H = Hq + Hk;
+    const int s0 = blockIdx.x * a.npos;
+    const int np = min(a.npos, S - s0);
+    const int64_t b = blockIdx.y;
+    const uint32_t qrow = static_cast<uint32_t>(Hq * D) * sizeof(T), krow = static_cast<uint32_t>(Hk * D) * sizeof(T);
+    const uint32_t rowb = qrow + krow;                        // a multiple of 16
+    uint8_t* tile = sm;                                       // [npos][rowb]
+    float2* cs = reinterpret_cast<float2*>(sm + static_cast<size_t>(a.npos) * rowb);   // [npos][APV][vph]
+    const uint32_t bar = smem_u32(cs + a.npos * half);
+    const int vph = half / APV;                               // vectors per head (half-split: per half)
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_expect_tx(bar, static_cast<uint32_t>(np) * rowb);
+        for (int pp = 0; pp < np; ++pp) {
+            const int64_t bs = b * S + s0 + pp;
+            if (qrow) bulk_g2s(smem_u32(tile + static_cast<size_t>(pp) * rowb), q + bs * a.q_ts, qrow, bar);
+            if (krow) bulk_g2s(smem_u32(tile + static_cast<size_t>(pp) * rowb + qrow), k + bs * a.k_ts, krow, bar);
+        }
+    }
+    for (int t = threadIdx.x; t < np * half; t += kThreads) {
+        const int pp = t / half, i = t - pp * half;
+        const int64_t p = a.pos ? static_cast<int64_t>(a.pos[b * S + s0 + pp]) : static_cast<int64_t>(s0 + pp);
+        float2 r;
+        if (a.cos_tab != nullptr) {
+            const int64_t pc = p < 0 ? 0 : (p >= a.n_tab ? a.n_tab - 1 : p);   // positions outside the table clamp
+            r = make_float2(a.cos_tab[pc * half + i], a.sign * a.sin_tab[pc * half + i]);
+        } else {
+            r = angle_cs(static_cast<double>(p), f.v[i], a.sign);
+        }
+        const int v = i / APV, e = i - v * APV;
+        cs[pp * half + e * vph + v] = r;
+    }
+    const bool got = mbar_wait(bar, 0);
+    if (!__syncthreads_and(got ? 1 : 0)) {
+        if (threadIdx.x == 0) {
+            atomicExch(&g_rope_err, 1);
+            mbar_wait(bar, 0);   // the copies still in flight into this block's shared memory
+        }
+        __syncthreads();
+        const int nv = H * (D / EPV);
+        for (int t = threadIdx.x; t < np * nv; t += kThreads) {
+            const int pp = t / nv, slot = t - pp * nv, h = slot / (D / EPV), v = slot - h * (D / EPV);
+            const int64_t bs = b * S + s0 + pp;
+            T* dst = h < Hq ? q + bs * a.q_ts + static_cast<int64_t>(h) * D : k + bs * a.k_ts + static_cast<int64_t>(h - Hq) * D;
+            stg16(dst + v * EPV, nan16<T>());
+        }
+        return;
+    }
+    const int nslot = H * vph;
+    const int ntask = nslot * np;
+    for (int t = threadIdx.x; t < ntask; t += kThreads) {
+        const int pp = t / nslot, slot = t - pp * nslot;
+        const int h = slot / vph, v = slot - h * vph;
+        const int64_t bs = b * S + s0 + pp;
+        T* dst = h < Hq ? q + bs * a.q_ts + static_cast<int64_t>(h) * D : k + bs * a.k_ts + static_cast<int64_t>(h - Hq) * D;
+        const uint8_t* src = tile + static_cast<size_t>(pp) * rowb + static_cast<size_t>(h * D) * sizeof(T);
+        const float2* ang = cs + pp * half + v;
+        if (INTER) {
+            float e8[EPV];
+            unpack(*reinterpret_cast<const uint4*>(src + v * 16), e8);
+#pragma unroll
+            for (int j = 0; j < APV; ++j) {
+                const float2 r = ang[j * vph];
+                const float x0 = e8[2 * j], x1 = e8[2 * j + 1];
+                e8[2 * j] = x0 * r.x - x1 * r.y;
+                e8[2 * j + 1] = x1 * r.x + x0 * r.y;
+            }
+            stg16(dst + v * EPV, pack(e8));
+        } else {
+            float av[EPV], bv[EPV];
+            unpack(*reinterpret_cast<const uint4*>(src + v * 16), av);
+            unpack(*reinterpret_cast<const uint4*>(src + static_cast<size_t>(half) * sizeof(T) + v * 16), bv);
+#pragma unroll
+            for (int j = 0; j < APV; ++j) {
+                const float2 r = ang[j * vph];
+                const float x0 = av[j], x1 = bv[j];
+                av[j] = x0 * r.x - x1 * r.y;
+                bv[j] = x1 * r.x + x0 * r.y;
+            }
+            stg16(dst + v * EPV, pack(av));
+            stg16(dst + half + v * EPV, pack(bv));
+        }
+    }
+}
+
+// Tokens per block of the staged form: a tile of about 32 KB, at most 4096
+// angles; 0 when one token row does not fit the shared memory.
+int staged_tokens(int64_t row_bytes, int half, int64_t S) {
+    const int64_t cap = max_smem_optin();
+    int64_t np = std::max<int64_t>(1, std::min<int64_t>({(32 << 10) / std::max<int64_t>(row_bytes, 1), 4096 / half, S}));
+    if (static_cast<int64_t>(np) * (row_bytes + 8 * half) + 8 > cap) return 0;
+    return static_cast<int>(np);
 }
 
 int rope_run(void* q, void* k, const int32_t* pos, int64_t B, int64_t S, int64_t Hq, int64_t Hk, int64_t D,
@@ -200,6 +343,27 @@ int rope_run(void* q, void* k, const int32_t* pos, int64_t B, int64_t S, int64_t
     // 16-byte vectors need every head start aligned: strides and head_dim in whole vectors
     const bool vec = (pairing ? (D % epv) : (half % epv)) == 0 && q_ts % epv == 0 && k_ts % epv == 0 && q16 && k16;
     RopeArgs a{q, k, pos, cos_tab, sin_tab, n_tab, q_ts, k_ts, (int)B, (int)S, (int)Hq, (int)Hk, (int)D, npos, sign};
+    if (vec && B <= 65535) {
+        const int64_t row_bytes = (Hq + Hk) * D * static_cast<int64_t>(esz);
+        const int nps = staged_tokens(row_bytes, half, S);
+        if (nps > 0) {
+            a.npos = nps;
+            const size_t ssm = static_cast<size_t>(nps) * (row_bytes + 8 * half) + 8;
+            dim3 g2(static_cast<unsigned>(ceil_div(S, static_cast<int64_t>(nps))), static_cast<unsigned>(B));
+            auto go2 = [&](auto kern) -> int {
+                if (ssm > 48u * 1024u &&
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm)) !=
+                        cudaSuccess)
+                    return check_launch(who);
+                kern<<<g2, kThreads, ssm, st>>>(a, f);
+                return check_launch(who);
+            };
+            if (dtype == LIGER_F32)
+                return pairing ? go2(rope_staged_kernel<float, true>) : go2(rope_staged_kernel<float, false>);
+            using Bf = __nv_bfloat16;
+            return pairing ? go2(rope_staged_kernel<Bf, true>) : go2(rope_staged_kernel<Bf, false>);
+        }
+    }
     auto go = [&](auto kern) { kern<<<grid, kThreads, smem, st>>>(a, f); };
     if (dtype == LIGER_F32) {
         if (pairing) vec ? go(rope_kernel<float, true, true>) : go(rope_kernel<float, false, true>);
@@ -213,6 +377,21 @@ int rope_run(void* q, void* k, const int32_t* pos, int64_t B, int64_t S, int64_t
 }
 
 }  // namespace
+
+int rope_err_word(int** out) {
+    static std::atomic<int*> addr[64];   // per device; racing threads store the same address
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(LIGER_ERR_CUDA, "no CUDA device");
+    int* p = addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_rope_err) != cudaSuccess)
+            return check_launch("rope error word");
+        addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return LIGER_OK;
+}
+
 }  // namespace liger
 
 extern "C" int liger_rope_fwd(void* q, void* k, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,

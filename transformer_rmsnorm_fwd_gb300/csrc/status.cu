@@ -63,22 +63,29 @@ int max_smem_optin() {
 // The library-owned error words, read and cleared on the caller's stream by
 // one thread (atomic exchange), the values landing in g_taken for the copy
 // back to the host.
-static __device__ int g_taken[3];
+constexpr int kWords = 4;
+static const char* const kFamily[kWords] = {"RMSNorm (staged kernels)", "FusedLinearSwiGLU",
+                                            "fused RMSNorm+QKV+RoPE", "RoPE (staged kernel)"};
 
-__global__ void take_error_words(int* a, int* b, int* c) {
-    g_taken[0] = atomicExch(a, 0);
-    g_taken[1] = atomicExch(b, 0);
-    g_taken[2] = atomicExch(c, 0);
+struct Words {
+    int* w[kWords];
+};
+
+static __device__ int g_taken[kWords];
+
+__global__ void take_error_words(Words w) {
+    for (int i = 0; i < kWords; ++i) g_taken[i] = atomicExch(w.w[i], 0);
 }
 
 __global__ void set_error_word(int* a) { atomicExch(a, 1); }
 
 static std::mutex g_status_mu;   // one g_taken per device: one reader at a time
 
-static int error_words(int* (&w)[3]) {
-    if (int rc = rmsnorm_err_word(&w[0])) return rc;
-    if (int rc = lsw_err_word(&w[1])) return rc;
-    return qkv_err_word(&w[2]);
+static int error_words(Words& w) {
+    if (int rc = rmsnorm_err_word(&w.w[0])) return rc;
+    if (int rc = lsw_err_word(&w.w[1])) return rc;
+    if (int rc = qkv_err_word(&w.w[2])) return rc;
+    return rope_err_word(&w.w[3]);
 }
 
 }  // namespace liger
@@ -88,31 +95,33 @@ extern "C" const char* liger_last_error(void) { return liger::g_msg; }
 extern "C" int liger_device_status(void* stream) {
     using namespace liger;
     clear_error();
-    int* w[3];
+    Words w;
     if (int rc = error_words(w)) return rc;
     cudaStream_t st = as_stream(stream);
-    int h[3] = {0, 0, 0};
+    int h[kWords] = {0};
     {
         std::lock_guard<std::mutex> lock(g_status_mu);
-        take_error_words<<<1, 1, 0, st>>>(w[0], w[1], w[2]);
+        take_error_words<<<1, 1, 0, st>>>(w);
         if (int rc = check_launch("device_status")) return rc;
         cudaError_t e = cudaMemcpyFromSymbolAsync(h, g_taken, sizeof(h), 0, cudaMemcpyDeviceToHost, st);
         if (e == cudaSuccess) e = cudaStreamSynchronize(st);
         if (e != cudaSuccess) return fail(LIGER_ERR_CUDA, "device_status: %s", cudaGetErrorString(e));
     }
-    if (h[0] || h[1] || h[2])
-        return fail(LIGER_ERR_CUDA, "a bounded wait expired in:%s%s%s; the outputs of that call are incomplete",
-                    h[0] ? " RMSNorm (staged kernels)" : "", h[1] ? " FusedLinearSwiGLU" : "",
-                    h[2] ? " fused RMSNorm+QKV+RoPE" : "");
+    char names[256] = "";
+    size_t n = 0;
+    for (int i = 0; i < kWords; ++i)
+        if (h[i]) n += snprintf(names + n, sizeof(names) - n, "%s%s", n ? ", " : "", kFamily[i]);
+    if (n) return fail(LIGER_ERR_CUDA, "a bounded wait expired in: %s; the outputs of that call are incomplete", names);
     return LIGER_OK;
 }
 
 extern "C" int liger_device_status_mark(int which, void* stream) {
     using namespace liger;
     clear_error();
-    if (which < 0 || which > 2) return fail(LIGER_ERR_SHAPE, "device_status_mark: which=%d (0, 1 or 2)", which);
-    int* w[3];
+    if (which < 0 || which >= kWords)
+        return fail(LIGER_ERR_SHAPE, "device_status_mark: which=%d (0 to %d)", which, kWords - 1);
+    Words w;
     if (int rc = error_words(w)) return rc;
-    set_error_word<<<1, 1, 0, as_stream(stream)>>>(w[which]);
+    set_error_word<<<1, 1, 0, as_stream(stream)>>>(w.w[which]);
     return check_launch("device_status_mark");
 }

@@ -141,6 +141,11 @@ struct EpiParams {
     // ksplit_nkb > 0 -- k-blocks from ksplit_nkb on come from the A2 / B2 maps,
     // their k coordinate restarting at 0 (a sum of two products)
     int bsplit, ksplit_nkb;
+    // msplit_mt > 0 (EPI_ACCUM without labels, keys or the fp32 sum) -- row blocks from
+    // msplit_mt on come from the A2 map, their row coordinate restarting at 0, and their
+    // rows (< M2) go to out2: two products with the same B in one launch (dW_g and
+    // dW_u), so that their tiles share waves
+    int msplit_mt, M2;
     // EPI_SWIGLU: out[row, ni*128 + j] = silu(acc[j]) * acc[128 + j], j < 128, col < N; with
     // out2 set, g = acc[j] and u = acc[128 + j] also go to out2 and out3 (bf16, same layout).
     // EPI_SWIGLU_BWD: with dh = src[row, col] recomputes g, u from the
@@ -489,7 +494,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         prefetch_map(&tmA);
         prefetch_map(&tmB);
-        if (ep.bsplit || ep.ksplit_nkb > 0) {
+        if (ep.bsplit || ep.ksplit_nkb > 0 || ep.msplit_mt > 0) {
             prefetch_map(&tmA2);
             prefetch_map(&tmB2);
         }
@@ -567,10 +572,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         else tma_load_2d_hint(dst, m, fb, x, y, pol);
                     };
                     const bool second = ep.ksplit_nkb > 0 && kb >= ep.ksplit_nkb;
-                    const CUtensorMap* mA = second ? &tmA2 : &tmA;
+                    const bool mhi = ep.msplit_mt > 0 && mi >= ep.msplit_mt;
+                    const CUtensorMap* mA = second || mhi ? &tmA2 : &tmA;
                     const CUtensorMap* mB = second ? &tmB2 : &tmB;
                     const int kc = (second ? kb - ep.ksplit_nkb : kb) * BK;
-                    const int arow = mi * Cfg::TM + a_row0;
+                    const int arow = (mhi ? mi - ep.msplit_mt : mi) * Cfg::TM + a_row0;
                     if (A_MN) {
 #pragma unroll
                         for (int j = 0; j < BM / MN_BOX; ++j) load(sa + j * MN_BOX_BYTES, mA, arow + j * MN_BOX, kc, pol_a);
@@ -695,9 +701,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             tile_mn(t, mi, ni);
             const int as = it & 1;
             const uint32_t aphase = (it >> 1) & 1;
-            const int row = mi * Cfg::TM + static_cast<int>(crank) * BM + rl;
+            const bool mhi = ep.msplit_mt > 0 && mi >= ep.msplit_mt;   // a row block of the second product
+            const int row = (mhi ? mi - ep.msplit_mt : mi) * Cfg::TM + static_cast<int>(crank) * BM + rl;
             const int n0 = ni * BN;
-            const bool row_ok = row < ep.M;
+            const bool row_ok = row < (mhi ? ep.M2 : ep.M);
             const float cscale = ep.scale_ptr != nullptr ? *ep.scale_ptr : ep.corr_scale;
             // EPI_ACCUM: everything that does not depend on the accumulator is fetched
             // before waiting for it (label range, first 32 columns of the fp32 sum)
@@ -1049,8 +1056,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) release_acc(as);
             } else {
-                uint8_t* oblk = ep.out != nullptr
-                                    ? reinterpret_cast<uint8_t*>(ep.out + static_cast<int64_t>(row - lane) * ep.ldo + n0)
+                __nv_bfloat16* obase = mhi ? ep.out2 : ep.out;
+                uint8_t* oblk = obase != nullptr
+                                    ? reinterpret_cast<uint8_t*>(obase + static_cast<int64_t>(row - lane) * ep.ldo + n0)
                                     : nullptr;
                 const int64_t ylab = (row_ok && ep.labels != nullptr) ? ep.labels[row] : ep.ignore_index;
                 const bool zero_row = ep.labels != nullptr && ylab == ep.ignore_index;
