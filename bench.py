@@ -365,10 +365,13 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER):
 
 
 WARMUP_ITERS, MIN_ITERS, MIN_TIMED_MS, FLOOR_ITERS = 10, 50, 200.0, 5
-# DRAM bytes (read + written) of one linear-CE call at seq 32768 (one ncu capture of the DRAM
-# byte counters over every launch of one call, kernels as of that capture); not re-measured
-# since, and reported as that capture's figure
-LINEAR_CE_TRAFFIC = 154_224_649_216
+# DRAM bytes (read + written) of one linear-CE call at seq 32768, scaled from an ncu capture of
+# the DRAM byte counters over the 11 launches of one call at seq 8192 with one chunk of 8192
+# tokens (the call's unit of work: the same launch shapes as each of the 4 chunks at seq 32768):
+# 4 x 32.78 GB per chunk, less the 3 bf16 dW writes only the last chunk makes (3 x 1.24 GB),
+# plus the fp32 dW sum the multi-chunk call passes through HBM 6 times (6 x 2.49 GB)
+LINEAR_CE_CHUNK_TRAFFIC = 32_780_587_776
+LINEAR_CE_TRAFFIC = 4 * LINEAR_CE_CHUNK_TRAFFIC - 3 * VOCAB * HIDDEN * 2 + 6 * VOCAB * HIDDEN * 4
 
 
 def timed_median(fn, pre=None):
@@ -947,8 +950,10 @@ def native_arm(args):
                 "bound": "tensor", "achieved": round(ce_tf, 1), "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                 "frac": round(ce_tf / pk["bf16_sustained"], 4),
                 "traffic": LINEAR_CE_TRAFFIC if S == 32768 else None, "traffic_unit": "bytes per call",
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over every launch of one "
-                                  "call at seq 32768, from an earlier capture (not re-measured)",
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the launches of one "
+                                  "call with a single 8192-token chunk (seq 8192), scaled to the 4 chunks of seq "
+                                  "32768 plus the fp32 dW sum's 6 passes",
+                "traffic_algorithmic_approx": 84_000_000_000,
                 "peak_source": f"{pk['src']} bf16 sustained (cuBLAS loop under the power cap)",
                 "ms_per_call": round(per_op["linear_ce"], 3)}
     cpu = None
