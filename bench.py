@@ -368,9 +368,9 @@ WARMUP_ITERS, MIN_ITERS, MIN_TIMED_MS, FLOOR_ITERS = 10, 50, 200.0, 5
 # DRAM bytes (read + written) of one linear-CE call at seq 32768, scaled from an ncu capture of
 # the DRAM byte counters over the 11 launches of one call at seq 8192 with one chunk of 8192
 # tokens (the call's unit of work: the same launch shapes as each of the 4 chunks at seq 32768):
-# 4 x 32.78 GB per chunk, less the 3 bf16 dW writes only the last chunk makes (3 x 1.24 GB),
+# 4 x 34.48 GB per chunk, less the 3 bf16 dW writes only the last chunk makes (3 x 1.24 GB),
 # plus the fp32 dW sum the multi-chunk call passes through HBM 6 times (6 x 2.49 GB)
-LINEAR_CE_CHUNK_TRAFFIC = 32_780_587_776
+LINEAR_CE_CHUNK_TRAFFIC = 34_476_864_768
 LINEAR_CE_TRAFFIC = 4 * LINEAR_CE_CHUNK_TRAFFIC - 3 * VOCAB * HIDDEN * 2 + 6 * VOCAB * HIDDEN * 4
 
 

@@ -57,13 +57,11 @@ int64_t dx_slab(int64_t V) {
     return ((V + n - 1) / n + 255) / 256 * 256;
 }
 
-constexpr int kRoundCtrs = 64;
 struct Hdr {
     unsigned long long n_valid;
     int bad;
     int err;
     float scale;   // the gradient scale, when it is formed on the device (no host wait)
-    unsigned int round_ctr[kRoundCtrs];   // one per dX / dW GEMM launch (rounds of tiles in step)
 };
 
 struct Layout {
@@ -551,10 +549,6 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     // 8192-token segments with absolute indices, several per chunk
     const bool rel = L.seg == L.C;
     if (a.dW && (rc = sort_labels(a.labels, a.T, L.seg, a.ignore, V, !rel, keys, lstart, a.st))) return rc;
-    // the dX and dW GEMMs stream both operands from HBM: their CTA pairs start rounds of
-    // tiles in step (one zeroed header word per launch, while the words last)
-    int nctr = 0;
-    auto round_ctr = [&]() { return nctr < kRoundCtrs ? &hdr->round_ctr[nctr++] : nullptr; };
     for (int64_t c = 0; c < L.nchunks; ++c) {
         const int64_t t0 = c * L.C;
         const int cl = static_cast<int>(std::min(L.C, a.T - t0));
@@ -617,7 +611,6 @@ int run_tc(const Args& a, const Layout& L, float scale) {
                 d.ld_corr = H;
                 d.corr_scale = scale;
                 d.scale_ptr = a.scale_dev;
-                d.round_ctr = round_ctr();
                 if ((rc = launch_gemm<0, 1, EPI_ACCUM, 1>(mDs_k, mWs_mn, cl, H, vl, d, a.st))) return rc;
             }
         } else if (a.dX) {
@@ -633,7 +626,6 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             d.ld_corr = H;
             d.corr_scale = scale;
             d.scale_ptr = a.scale_dev;
-            d.round_ctr = round_ctr();
             if ((rc = launch_gemm<0, 1, EPI_STORE, 1>(mD_k, mW_mn, cl, H, V, d, a.st))) return rc;
         }
         // 4. dW (+)= D^T X_c, minus scale * X_t in fp32 for each token t labelled with the row
@@ -670,7 +662,6 @@ int run_tc(const Args& a, const Layout& L, float scale) {
             d.acc_read = first ? 0 : 1;
             d.acc_write = last ? 0 : 1;
             d.out_write = last ? 1 : 0;
-            d.round_ctr = round_ctr();
             if ((rc = launch_gemm<1, 1, EPI_ACCUM, 1>(mD_mn, mX_mn, V, H, cl, d, a.st))) return rc;
         }
     }

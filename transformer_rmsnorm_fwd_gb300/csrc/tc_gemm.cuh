@@ -141,13 +141,6 @@ struct EpiParams {
     // ksplit_nkb > 0 -- k-blocks from ksplit_nkb on come from the A2 / B2 maps,
     // their k coordinate restarting at 0 (a sum of two products)
     int bsplit, ksplit_nkb;
-    // round_ctr non-null (a device word zeroed before the launch): the CTA pairs start
-    // their rounds of tiles (the j-th tile of every pair) in step -- a pair begins round
-    // j only when every pair has begun round j - 1 -- so that the tiles of a wave, which
-    // share operand slices, stream them through L2 together instead of drifting apart
-    // over a long launch.  Each wait is bounded; a pair that waits too long stops waiting
-    // for the rest of the launch (the order is only a hint).
-    unsigned int* round_ctr;
     // msplit_mt > 0 (EPI_ACCUM without labels, keys or the fp32 sum) -- row blocks from
     // msplit_mt on come from the A2 map, their row coordinate restarting at 0, and their
     // rows (< M2) go to out2: two products with the same B in one launch (dW_g and
@@ -177,13 +170,6 @@ struct EpiParams {
 };
 
 // ------------------------------------------------------------ PTX wrappers
-// bound of one wait for the other CTA pairs to begin a round of tiles (round_ctr)
-constexpr unsigned long long kRoundWaitNs = 2000000ull;
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
 // L2 eviction policy of an operand's loads (createpolicy, whole access)
 enum Hint : int { HINT_NORMAL = 0, HINT_EVICT_FIRST = 1, HINT_EVICT_LAST = 2 };
 __device__ __forceinline__ uint64_t make_policy(int hint) {
@@ -567,21 +553,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int s = 0; s < Cfg::ST; ++s) issued[s] = false, issued_phase[s] = 0;
             bool ok = true;
             const int a_row0 = static_cast<int>(crank) * BM;   // this CTA's rows within the tile
-            bool in_step = ep.round_ctr != nullptr && leader;
-            for (int t = unit, j = 0; t < ntiles && ok; t += nunits, ++j) {
-                if (ep.round_ctr != nullptr && leader) {
-                    if (in_step && j > 0) {
-                        const unsigned need = static_cast<unsigned>(j) * static_cast<unsigned>(nunits);
-                        const uint64_t t0 = globaltimer();
-                        while (ld_acquire_u32(ep.round_ctr) < need) {
-                            if (globaltimer() - t0 > kRoundWaitNs) {
-                                in_step = false;
-                                break;
-                            }
-                        }
-                    }
-                    atomicAdd(ep.round_ctr, 1u);
-                }
+            for (int t = unit; t < ntiles && ok; t += nunits) {
                 int mi, ni;
                 tile_mn(t, mi, ni);
                 for (int kb = 0; kb < nkb; ++kb) {
