@@ -132,6 +132,22 @@ def test_rope_ragged_positions(cuda_lib, dtype, B, S, Hq, Hk, D):
     assert oracle.rel_err(host(tq), q64) <= (1e-5 if dtype == "f32" else 2e-2)
 
 
+@pytest.mark.parametrize("dtype,B,S,Hq,Hk,D", [("f32", 1, 40, 400, 112, 128),    # a token row of 256 KB: no staged tile
+                                               ("bf16", 70000, 2, 1, 1, 64)])    # batch beyond the staged grid
+def test_rope_fallback_layouts(cuda_lib, dtype, B, S, Hq, Hk, D):
+    """The RoPE forms the staged kernel does not take: token rows larger than a
+    block's shared memory, and batches beyond its grid; explicit positions."""
+    q = datagen.normal(4, "fq", (B, S, Hq, D), dtype)
+    k = datagen.normal(4, "fk", (B, S, Hk, D), dtype)
+    pos = datagen.positions(4, "fp", (B, S), 8192)
+    tq, tk = dev(q), dev(k)
+    cuda_lib.liger_rope_fwd(tq, tk, dev(pos), 1e4)
+    assert oracle.rel_err(host(tq), oracle.rope(q, 1e4, pos=pos)) <= TOL[dtype]
+    assert oracle.rel_err(host(tk), oracle.rope(k, 1e4, pos=pos)) <= TOL[dtype]
+    cuda_lib.liger_rope_bwd(tq, tk, dev(pos), 1e4)
+    assert oracle.rel_err(host(tq), datagen.to_f64(q, dtype)) <= (1e-5 if dtype == "f32" else 2e-2)
+
+
 def test_rope_fp32_long_positions_accuracy(cuda_lib):
     """fp32 at positions up to 32767: the fp64 angle reduction keeps ~1e-6."""
     q = datagen.normal(9, "lq", (1, 4, 2, 128), "f32")

@@ -345,7 +345,12 @@ int rope_run(void* q, void* k, const int32_t* pos, int64_t B, int64_t S, int64_t
     RopeArgs a{q, k, pos, cos_tab, sin_tab, n_tab, q_ts, k_ts, (int)B, (int)S, (int)Hq, (int)Hk, (int)D, npos, sign};
     if (vec && B <= 65535) {
         const int64_t row_bytes = (Hq + Hk) * D * static_cast<int64_t>(esz);
-        const int nps = staged_tokens(row_bytes, half, S);
+        int nps = staged_tokens(row_bytes, half, S);
+        // small problems: fewer tokens per block, so that at least two blocks per SM share the work
+        if (nps > 1) {
+            const int64_t per = ceil_div(B * S, 2 * static_cast<int64_t>(sm_count()));
+            nps = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(nps, per)));
+        }
         if (nps > 0) {
             a.npos = nps;
             const size_t ssm = static_cast<size_t>(nps) * (row_bytes + 8 * half) + 8;
