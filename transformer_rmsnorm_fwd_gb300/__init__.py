@@ -10,8 +10,9 @@ This package is the Python binding of that library: see ``_native`` for the
 functions, which carry the C entry points' names.
 """
 from ._native import (LIGER_BF16, LIGER_F32, LigerError,  # noqa: F401
-                      liger_device_status, liger_device_status_mark, liger_fused_linear_swiglu_bwd, liger_fused_linear_swiglu_bwd_saved,
-                      liger_fused_linear_swiglu_fwd, liger_fused_linear_swiglu_fwd_save,
+                      liger_device_status, liger_device_status_mark, liger_fused_linear_swiglu_bwd,
+                      liger_fused_linear_swiglu_bwd_saved, liger_fused_linear_swiglu_fwd,
+                      liger_fused_linear_swiglu_fwd_save,
                       liger_fused_linear_swiglu_workspace, liger_linear_ce_fwd_bwd, liger_linear_ce_two_pass_fwd_bwd,
                       liger_linear_ce_two_pass_workspace, liger_linear_ce_workspace,
                       liger_rmsnorm_bwd, liger_rmsnorm_bwd_noalloc, liger_rmsnorm_bwd_workspace, liger_rmsnorm_fwd,
