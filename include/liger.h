@@ -191,7 +191,8 @@ int liger_rmsnorm_bwd_noalloc(const void* dy, const void* x, const void* w, cons
  * The angle is formed and reduced modulo 2 pi in double precision, then
  * cos/sin are taken in single precision.  head_dim must be even.  pos is an
  * int32 device array [batch, seq] of values >= 0, or NULL.  q (k) may be NULL
- * only when n_q_heads (n_k_heads) is 0.
+ * only when n_q_heads (n_k_heads) is 0.  q and k must not overlap: each block
+ * of tokens is read into shared memory, rotated there and written back.
  */
 int liger_rope_fwd(void* q, void* k, const int32_t* pos, int64_t batch, int64_t seq, int64_t n_q_heads,
                    int64_t n_k_heads, int64_t head_dim, double theta, int dtype, void* stream);
