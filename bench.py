@@ -156,9 +156,13 @@ def workload_config(S):
                            "dw after the backward)"}
 
 
-def algorithmic(S):
-    """Algorithmic bytes (memory-bound kernels) and flops (linear-CE) per call."""
+def algorithmic(S, n_valid=None):
+    """Algorithmic bytes (memory-bound kernels) and flops (linear-CE) per call.  The
+    linear CE's required flops are 6 * n_valid * H * V: a token whose label is
+    ignored needs no logits and adds nothing to dX or dW (its dX row is 0), and the
+    call computes none for it; 6 * S * H * V is also given, as all_tokens."""
     e = 2
+    n_valid = S if n_valid is None else n_valid
     SH, SI = S * HIDDEN, S * INTER
     qk = 2 * S * HEADS * HEAD_DIM
     return {
@@ -168,7 +172,8 @@ def algorithmic(S):
         "rope_bwd": 2 * qk * e,
         "swiglu_fwd": 3 * SI * e,
         "swiglu_bwd": 5 * SI * e,
-        "linear_ce_flops": 6 * S * HIDDEN * VOCAB,
+        "linear_ce_flops": 6 * n_valid * HIDDEN * VOCAB,
+        "linear_ce_flops_all_tokens": 6 * S * HIDDEN * VOCAB,
     }
 
 
@@ -207,6 +212,7 @@ class Chain:
         bf = torch.bfloat16
         S = inputs["x"].shape[0]
         self.S = S
+        self.n_valid = int((inputs["labels"] != -100).sum())
         self.inp = {k: (to_torch(v, device) if v is not None else None) for k, v in inputs.items()}
         self.y = torch.empty(S, HIDDEN, dtype=bf, device=device)
         self.rstd = torch.empty(S, dtype=torch.float32, device=device)
@@ -223,16 +229,26 @@ class Chain:
                                 device=device)
 
     def launches_per_step(self):
-        chunk = min(self.S, 8192, max(128, (self.S + 1) // 2))
-        nchunks = -(-self.S // chunk)
+        # the linear CE runs its GEMMs on the tokens that are not ignored (when some are),
+        # after 4 launches that compact them (count, scan, index, gather) and before 2 that
+        # put dX, lse and the loss terms back
+        S = self.S
+        nv = getattr(self, "n_valid", S)
+        T = nv if 0 < nv < S else S
+        compaction = 6 if 0 < nv < S else 0
+        chunk = min(T, 8192, max(128, (T + 1) // 2))
+        if chunk >= 1024:
+            chunk = min(8192, -(-chunk // 256) * 256)
+        chunk = min(chunk, T)
+        nchunks = -(-T // chunk)
         # the logits GEMM runs over at most 32 MiB of X rows per launch (4096 rows at hidden 4096)
         sub = max(1, min(chunk, max(256, (32 << 20) // (2 * HIDDEN) // 256 * 256)))
-        logits = sum(-(-min(chunk, self.S - c * chunk) // sub) for c in range(nchunks))
+        logits = sum(-(-min(chunk, T - c * chunk) // sub) for c in range(nchunks))
         # the dX GEMM runs over vocabulary slabs of at most 65536 rows
         dx = 1 if VOCAB <= 65536 else -(-VOCAB // 65536)
         # linear CE: label scan, label sort and start tables (once), the logits GEMM launches, per
         # chunk dlogits, the dX GEMM launches and the dW GEMM, loss reduction
-        return 1 + 1 + 1 + (1 + 2 + logits + (2 + dx) * nchunks + 1) + 1 + 1 + 2
+        return 1 + 1 + 1 + (1 + 2 + logits + (2 + dx) * nchunks + 1 + compaction) + 1 + 1 + 2
 
     def step(self, ev=None):
         """One pass of every operator; ev: dict name -> list of (start, end) events."""
@@ -579,7 +595,7 @@ def llama3_norm_rope_config(L, dev, flush, pk):
 def llama3_head_config(L, dev, pk):
     """Fused linear-CE fwd+bwd at the Llama-3 head: 8192 tokens x hidden 4096 x
     vocab 128256 bf16, 10 % ignored labels, mean (seed 3), back-to-back calls
-    (lm_head 1.05 GB: larger than L2).  6*T*H*V useful flops per call."""
+    (lm_head 1.05 GB: larger than L2).  6*n_valid*H*V required flops per call."""
     import torch
     from datagen import workloads
     c = workloads.linear_ce_llama3()
@@ -591,9 +607,11 @@ def llama3_head_config(L, dev, pk):
     dX, dW = torch.empty_like(X), torch.empty_like(W)
     ws = torch.empty(L.liger_linear_ce_workspace(T, H, V, 0, L.LIGER_BF16), dtype=torch.uint8, device=dev)
     ms = timed_median(lambda: L.liger_linear_ce_fwd_bwd(X, W, lab, loss, dX, dW, ws))
-    tf = 6.0 * T * H * V / (ms / 1000.0) / 1e12
+    n_valid = int((lab != -100).sum().item())
+    tf = 6.0 * n_valid * H * V / (ms / 1000.0) / 1e12
     return {"shape": "T=8192 H=4096 V=128256 bf16, mean, 10% ignored", "ms": round(ms, 3),
-            "tokens_per_s": round(T / (ms / 1000.0), 1), "tflops_6thv": round(tf, 1),
+            "tokens_per_s": round(T / (ms / 1000.0), 1), "n_valid": n_valid,
+            "tflops_6nhv": round(tf, 1), "tflops_counting_all_tokens": round(6.0 * T * H * V / (ms / 1000.0) / 1e12, 1),
             "frac_sustained": round(tf / pk["bf16_sustained"], 4), "frac_burst": round(tf / pk["bf16"], 4),
             "loss": float(loss.item()),
             "timing": "median of >= 50 back-to-back calls after 10 warm-ups (power-capped clock: compare with "
@@ -937,7 +955,8 @@ def native_arm(args):
     configs = None
     if not args.no_configs:
         configs = named_configs(L, dev, pk, inputs)
-    alg = algorithmic(S)
+    n_valid = int((inputs["labels"] != -100).sum())
+    alg = algorithmic(S, n_valid)
     hbm = {}
     for k in ("rmsnorm_fwd", "rmsnorm_bwd", "rope_fwd", "rope_bwd", "swiglu_fwd", "swiglu_bwd"):
         gbs = alg[k] / (per_op[k] / 1000.0) / 1e9
@@ -946,9 +965,12 @@ def native_arm(args):
                   "frac": round(gbs / pk["hbm_gbs"], 4), "ms_isolated": round(iso[k], 4),
                   "gbs_isolated": round(gi, 1), "frac_isolated": round(gi / pk["hbm_gbs"], 4)}
     ce_tf = alg["linear_ce_flops"] / (per_op["linear_ce"] / 1000.0) / 1e12
-    roofline = {"kernel": "liger_linear_ce_fwd_bwd (tcgen05 GEMMs + fused epilogues; 6*S*H*V flops per call)",
+    roofline = {"kernel": "liger_linear_ce_fwd_bwd (tcgen05 GEMMs + fused epilogues; 6*n_valid*H*V flops per call: "
+                          "the ignored tokens' logits are not computed)",
                 "bound": "tensor", "achieved": round(ce_tf, 1), "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                "frac": round(ce_tf / pk["bf16_sustained"], 4),
+                "frac": round(ce_tf / pk["bf16_sustained"], 4), "n_valid": n_valid, "tokens": S,
+                "achieved_counting_all_tokens": round(alg["linear_ce_flops_all_tokens"] /
+                                                      (per_op["linear_ce"] / 1000.0) / 1e12, 1),
                 "traffic": LINEAR_CE_TRAFFIC if S == 32768 else None, "traffic_unit": "bytes per call",
                 "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the launches of one "
                                   "call with a single 8192-token chunk (seq 8192), scaled to the 4 chunks of seq "
@@ -1018,7 +1040,8 @@ def single_op(args):
             ws = torch.empty(L.liger_linear_ce_workspace(S, HIDDEN, VOCAB, args.chunk, L.LIGER_BF16),
                              dtype=torch.uint8, device=dev)
             fn = lambda: L.liger_linear_ce_fwd_bwd(X, W, lab, loss, dX, dW, ws, chunk=args.chunk)
-            flops = 6.0 * S * HIDDEN * VOCAB
+            # the GEMMs run on the tokens whose label is not ignored
+            flops = 6.0 * int((lab != -100).sum()) * HIDDEN * VOCAB
         else:
             ws = torch.empty(L.liger_linear_ce_two_pass_workspace(S, HIDDEN, VOCAB), dtype=torch.uint8, device=dev)
             fn = lambda: L.liger_linear_ce_two_pass_fwd_bwd(X, W, lab, loss, dX, dW, ws)

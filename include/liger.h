@@ -349,8 +349,15 @@ int liger_fused_linear_swiglu_bwd_saved(const void* X, const void* Wg, const voi
  *   loss: one float on the device; dX: [T, H] and dW: [V, H] in dtype, each
  *   may be NULL (not computed).  Rows of dX whose label is ignore_index are
  *   written as +0.0.
+ *   On the bf16 tensor-core path, when some labels are ignore_index, the
+ *   tokens with the other labels are gathered (in order) into the workspace
+ *   and only they go through the GEMMs: an ignored token needs no logits and
+ *   adds nothing to dW (6 n_valid H V flops instead of 6 T H V); dX, lse and
+ *   the loss terms are then put back in place, 0 on ignored rows.  The chunks
+ *   below are chunks of those tokens.
  *   The tokens are processed in chunks of `chunk` rows (0 = automatic:
- *   min(T, 8192, max(128, ceil(T/2))) on the bf16 tensor-core path; there a
+ *   min(T, 8192, max(128, ceil(T/2)), from 1024 rows on rounded up to a
+ *   multiple of 256) on the bf16 tensor-core path; there a
  *   chunk above 8192 rows is rounded down to a multiple of 8192, at most
  *   65536); per chunk the logits
  *   exist only in a [chunk x V] workspace buffer, never as a [T x V] tensor
@@ -407,9 +414,12 @@ int liger_linear_ce_two_pass_fwd_bwd(const void* X, const void* W, const int64_t
  *     counted in n_valid, its lse, loss term and gradient rows 0) and the
  *     loss is NaN, so the error shows in the result.  Argument errors are
  *     still returned before anything is queued;
- *   - the count n_valid and the gradient scale are formed on the device.
- * Results are bit-identical to the waiting variant whenever every label is
- * valid. */
+ *   - the count n_valid and the gradient scale are formed on the device, so
+ *     the GEMMs run over all T tokens (the ignored ones give D = 0).
+ * Results are bit-identical to the waiting variant whenever no label is
+ * ignored; with ignored labels, lse and dX still are, while dW and the loss
+ * are the same sums over a different grouping of the tokens (equal within
+ * rounding). */
 int liger_linear_ce_fwd_bwd_async(const void* X, const void* W, const int64_t* labels, int64_t T, int64_t H,
                                   int64_t V, int64_t ignore_index, int reduction, float grad_scale, float* loss,
                                   void* dX, void* dW, void* ws, size_t ws_bytes, int64_t chunk, int dtype,

@@ -59,6 +59,8 @@ def test_algorithmic_work():
     assert a["swiglu_bwd"] == 5 * 8192 * 11008 * 2
     assert a["rope_fwd"] == 2 * 2 * 8192 * 32 * 128 * 2
     assert a["linear_ce_flops"] == 6 * 8192 * 4096 * 151936
+    b = bench.algorithmic(8192, 7373)
+    assert b["linear_ce_flops"] == 6 * 7373 * 4096 * 151936 and b["linear_ce_flops_all_tokens"] == a["linear_ce_flops"]
 
 
 @pytest.mark.slow
@@ -73,15 +75,21 @@ def test_reference_arm_json_contract():
 
 
 def test_launch_count_per_step():
-    """The benchmark's gpu_launches claim: 39 launches of this library per chain step
-    at seq 32768 (an ncu launch list of 3 steps counted 117): RMSNorm, RoPE and SwiGLU
-    forwards, the linear CE (label scan, sort and starts, 4 chunks x (2 logits launches,
-    dlogits, 3 dX slab launches, dW), loss reduction), SwiGLU and RoPE backwards,
-    RMSNorm backward (2)."""
+    """The benchmark's gpu_launches claim per chain step at seq 32768: RMSNorm, RoPE and
+    SwiGLU forwards, the linear CE (label scan, sort and starts, 4 chunks x (2 logits
+    launches, dlogits, 3 dX slab launches, dW), loss reduction, and with ignored labels
+    the 6 launches that compact the other tokens and put the results back), SwiGLU and
+    RoPE backwards, RMSNorm backward (2): 39 with every label valid (an ncu launch list
+    of 3 such steps counted 117), 45 with the chain's 10 % ignored (29491 valid tokens:
+    chunks of 8192, 8192, 8192 and 4915 rows)."""
     class _C:
         S = 32768
     assert bench.Chain.launches_per_step(_C()) == 39
     assert 3 * bench.Chain.launches_per_step(_C()) == 117
+
+    class _D:
+        S, n_valid = 32768, 29491
+    assert bench.Chain.launches_per_step(_D()) == 45
 
 
 def test_cpu_model_names_x86_and_arm_hosts():

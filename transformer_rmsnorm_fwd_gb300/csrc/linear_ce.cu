@@ -81,7 +81,12 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     int64_t C;
     if (chunk > 0) C = chunk;
     // automatic: at most half the tokens (never all T rows at once, for T > 128), at most kAutoChunkTC rows
-    else if (L.tc) C = std::min<int64_t>(kAutoChunkTC, std::max<int64_t>(128, (T + 1) / 2));
+    else if (L.tc) {
+        C = std::min<int64_t>(kAutoChunkTC, std::max<int64_t>(128, (T + 1) / 2));
+        // large chunks in whole 256-row tiles of the CTA-pair GEMMs (7373 tokens: 3840 + 3533
+        // rows, 15 + 14 row tiles, rather than 2 x 3687 rows in 15 + 15)
+        if (C >= 1024) C = std::min<int64_t>(kAutoChunkTC, (C + 255) / 256 * 256);
+    }
     else C = std::max<int64_t>(128, (int64_t{1} << 26) / std::max<int64_t>(V, 1));
     if (L.tc) {
         C = std::min<int64_t>(C, kMaxChunkTC);
@@ -114,7 +119,128 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     return L;
 }
 
+// Workspace of the waiting tensor-core entry point, which runs the chunked GEMMs
+// on the tokens that are not ignored only: the ordinary layout's lse, loss_row and
+// header first (lse and loss_row of every token, as documented), then the region
+// the chunked path runs in for those tokens (at most the ordinary layout's size),
+// then their X rows, their dX rows, their labels and the index maps.
+struct CompactLayout {
+    size_t core, xc, dxc, labc, idx, inv, cnt, total;
+};
+
+constexpr int kCompactBlock = 1024;   // tokens per block of the compaction's index pass
+
+CompactLayout compact_layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
+    const Layout L = layout(T, H, V, chunk, dtype);
+    const size_t esz = dtype == LIGER_F32 ? 4 : 2;
+    const size_t t = static_cast<size_t>(std::max<int64_t>(T, 1));
+    CompactLayout C{};
+    size_t o = L.labs;   // after lse, loss_row, z_label and the header of the ordinary layout
+    C.core = o; o = up256(o + L.total);
+    C.xc = o; o = up256(o + t * static_cast<size_t>(H) * esz);
+    C.dxc = o; o = up256(o + t * static_cast<size_t>(H) * esz);
+    C.labc = o; o = up256(o + t * sizeof(int64_t));
+    C.idx = o; o = up256(o + t * sizeof(int64_t));
+    C.inv = o; o = up256(o + t * sizeof(int));
+    C.cnt = o; o = up256(o + sizeof(int) * static_cast<size_t>(ceil_div(static_cast<int64_t>(t), int64_t{kCompactBlock})));
+    C.total = o;
+    return C;
+}
+
 // ---------------------------------------------------------------- kernels
+// ---- compaction of the tokens that are not ignored (stable: their order is kept)
+__global__ void __launch_bounds__(kCompactBlock) compact_count(const int64_t* __restrict__ labels, int64_t T,
+                                                               int64_t ignore, int* __restrict__ cnt) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kCompactBlock + threadIdx.x;
+    const int c = __syncthreads_count(t < T && labels[t] != ignore);
+    if (threadIdx.x == 0) cnt[blockIdx.x] = c;
+}
+
+// cnt[0, nb) -> exclusive prefix sums, in place (one block of 1024 threads)
+__global__ void __launch_bounds__(1024) compact_scan(int* cnt, int64_t nb) {
+    __shared__ int sums[1024];
+    const int64_t per = (nb + 1023) / 1024;
+    const int64_t b0 = threadIdx.x * per, b1 = min(nb, b0 + per);
+    int s = 0;
+    for (int64_t b = b0; b < b1; ++b) s += cnt[b];
+    sums[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = 1; o < 1024; o <<= 1) {
+        const int v = threadIdx.x >= o ? sums[threadIdx.x - o] : 0;
+        __syncthreads();
+        sums[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = threadIdx.x ? sums[threadIdx.x - 1] : 0;
+    for (int64_t b = b0; b < b1; ++b) {
+        const int c = cnt[b];
+        cnt[b] = run;
+        run += c;
+    }
+}
+
+// idx[p] = t and lab_c[p] = labels[t] for the p-th token that is not ignored; inv[t] = p, or -1
+__global__ void __launch_bounds__(kCompactBlock) compact_index(const int64_t* __restrict__ labels, int64_t T,
+                                                               int64_t ignore, const int* __restrict__ off,
+                                                               int64_t* __restrict__ idx, int* __restrict__ inv,
+                                                               int64_t* __restrict__ lab_c) {
+    __shared__ int wsum[kCompactBlock / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kCompactBlock + threadIdx.x;
+    const int64_t y = t < T ? labels[t] : ignore;
+    const bool v = t < T && y != ignore;
+    const unsigned m = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) wsum[wid] = __popc(m);
+    __syncthreads();
+    int before = 0;
+    for (int w = 0; w < wid; ++w) before += wsum[w];
+    const int p = off[blockIdx.x] + before + __popc(m & ((1u << lane) - 1u));
+    if (v) {
+        idx[p] = t;
+        lab_c[p] = y;
+    }
+    if (t < T) inv[t] = v ? p : -1;
+}
+
+// rows (16-byte vectors, hv per row): dst[r] = src[idx[r]], r < n
+__global__ void gather_rows(const uint4* __restrict__ src, const int64_t* __restrict__ idx, int64_t n, int64_t hv,
+                            uint4* __restrict__ dst) {
+    for (int64_t r = blockIdx.x; r < n; r += gridDim.x) {
+        const uint4* s = src + idx[r] * hv;
+        uint4* d = dst + r * hv;
+        for (int64_t v = threadIdx.x; v < hv; v += blockDim.x) d[v] = ldg16_nc(s + v);
+    }
+}
+
+// rows back in place: dst[t] = src[inv[t]], or +0 where inv[t] < 0 (an ignored token)
+__global__ void scatter_rows(const uint4* __restrict__ src, const int* __restrict__ inv, int64_t T, int64_t hv,
+                             uint4* __restrict__ dst) {
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const int p = inv[t];
+        uint4* d = dst + t * hv;
+        if (p < 0) {
+            for (int64_t v = threadIdx.x; v < hv; v += blockDim.x) d[v] = make_uint4(0, 0, 0, 0);
+        } else {
+            const uint4* s = src + static_cast<int64_t>(p) * hv;
+            for (int64_t v = threadIdx.x; v < hv; v += blockDim.x) d[v] = ldg16_nc(s + v);
+        }
+    }
+}
+
+// lse and loss_row of every token from those of the tokens that were run (+0 where ignored),
+// and the run's kernel error word into the entry point's header
+__global__ void scatter_rowvals(const float* __restrict__ lse_c, const float* __restrict__ loss_c,
+                                const int* __restrict__ inv, int64_t T, float* __restrict__ lse,
+                                float* __restrict__ loss, const int* core_err, int* err) {
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int p = inv[t];
+        lse[t] = p < 0 ? 0.f : lse_c[p];
+        loss[t] = p < 0 ? 0.f : loss_c[p];
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && *core_err != 0) atomicExch(err, *core_err);
+}
+
 // Counts the labels that are not ignore_index and flags any outside [0, V).  With
 // lab_out set, also writes the labels with every bad one replaced by ignore_index
 // (and not counted), so that no later kernel indexes with it.
@@ -668,6 +794,54 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     return LIGER_OK;
 }
 
+// The chunked path on the tokens that are not ignored only (n_valid of T, known on
+// the host from the label scan): an ignored token has D = 0, so it adds nothing to
+// dW and its dX row, lse and loss term are 0; its logits, which the GEMMs would
+// otherwise compute, are not needed.  The tokens are compacted in order (their X
+// rows and labels gathered), the chunked path runs on them in its own region of the
+// workspace, and dX, lse and the loss terms are put back in place.
+int run_tc_compact(const Args& a, int64_t n_valid, int64_t chunk, float scale) {
+    const CompactLayout C = compact_layout(a.T, a.H, a.V, chunk, a.dtype);
+    const Layout Lt = layout(a.T, a.H, a.V, chunk, a.dtype);   // the documented lse / loss_row of every token
+    const Layout Lc = layout(n_valid, a.H, a.V, chunk, a.dtype);
+    if (Lc.total > Lt.total) return run_tc(a, Lt, scale);   // the region holds any layout of fewer tokens
+    uint8_t* w8 = a.ws;
+    int* cnt = reinterpret_cast<int*>(w8 + C.cnt);
+    int64_t* idx = reinterpret_cast<int64_t*>(w8 + C.idx);
+    int* inv = reinterpret_cast<int*>(w8 + C.inv);
+    int64_t* labc = reinterpret_cast<int64_t*>(w8 + C.labc);
+    const int64_t nb = ceil_div(a.T, static_cast<int64_t>(kCompactBlock));
+    compact_count<<<static_cast<unsigned>(nb), kCompactBlock, 0, a.st>>>(a.labels, a.T, a.ignore, cnt);
+    compact_scan<<<1, 1024, 0, a.st>>>(cnt, nb);
+    compact_index<<<static_cast<unsigned>(nb), kCompactBlock, 0, a.st>>>(a.labels, a.T, a.ignore, cnt, idx, inv, labc);
+    const int64_t hv = a.H * 2 / 16;   // 16-byte vectors per bf16 row (H is a multiple of 8 on this path)
+    const int rgrid = static_cast<int>(std::min<int64_t>(std::max<int64_t>(n_valid, 1), 8 * sm_count()));
+    gather_rows<<<rgrid, 256, 0, a.st>>>(static_cast<const uint4*>(a.X), idx, n_valid, hv,
+                                         reinterpret_cast<uint4*>(w8 + C.xc));
+    if (int rc = check_launch("linear_ce compaction")) return rc;
+    Hdr* hc = reinterpret_cast<Hdr*>(w8 + C.core + Lc.hdr);
+    if (cudaMemsetAsync(hc, 0, sizeof(Hdr), a.st) != cudaSuccess) return check_launch("linear_ce memset");
+    Args b = a;
+    b.X = w8 + C.xc;
+    b.labels = labc;
+    b.T = n_valid;
+    b.dX = a.dX ? static_cast<void*>(w8 + C.dxc) : nullptr;
+    b.ws = w8 + C.core;
+    if (int rc = run_tc(b, Lc, scale)) return rc;
+    if (a.dX) {
+        const int tgrid = static_cast<int>(std::min<int64_t>(a.T, 8 * sm_count()));
+        scatter_rows<<<tgrid, 256, 0, a.st>>>(reinterpret_cast<const uint4*>(w8 + C.dxc), inv, a.T, hv,
+                                              static_cast<uint4*>(a.dX));
+    }
+    const int vgrid = static_cast<int>(std::min<int64_t>(ceil_div(a.T, int64_t{256}), 4 * sm_count()));
+    scatter_rowvals<<<vgrid, 256, 0, a.st>>>(reinterpret_cast<const float*>(w8 + C.core + Lc.lse),
+                                             reinterpret_cast<const float*>(w8 + C.core + Lc.lossrow), inv, a.T,
+                                             reinterpret_cast<float*>(w8 + Lt.lse),
+                                             reinterpret_cast<float*>(w8 + Lt.lossrow), &hc->err,
+                                             &reinterpret_cast<Hdr*>(w8 + Lt.hdr)->err);
+    return check_launch("linear_ce scatter");
+}
+
 // --------------------------------------- two-pass (vocab-chunked) variant
 // The same loss and gradients with no [tokens x vocab] buffer at all: pass 1
 // computes only lse (the logits GEMM keeps per-tile (m, s) partials, token
@@ -838,6 +1012,7 @@ using namespace liger;
 
 extern "C" size_t liger_linear_ce_workspace(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     if (T < 0 || H <= 0 || V <= 0 || chunk < 0 || (dtype != LIGER_F32 && dtype != LIGER_BF16)) return 0;
+    if (use_tc(H, V, dtype)) return compact_layout(T, H, V, chunk, dtype).total;
     return layout(T, H, V, chunk, dtype).total;
 }
 
@@ -877,7 +1052,7 @@ int ce_entry(const char* who, const void* X, const void* W, const int64_t* label
         ce_scale<<<1, 1, 0, st>>>(hdr, reduction, grad_scale);
         if (int rc = check_launch("ce_scale")) return rc;
         Args a{X, W, labs, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st, &hdr->scale};
-        if (int rc = run(a, 0.0f)) return rc;
+        if (int rc = run(a, 0.0f, int64_t{-1})) return rc;   // the count stays on the device
         loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + CL.lossrow), T, 0.0, hdr, loss,
                                        reduction == 0 ? 1 : 2);
         return check_launch("loss_final");
@@ -908,7 +1083,7 @@ int ce_entry(const char* who, const void* X, const void* W, const int64_t* label
     const float scale = reduction == 0 ? static_cast<float>(static_cast<double>(grad_scale) / static_cast<double>(n_valid))
                                        : grad_scale;
     Args a{X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, w8, dtype, st, nullptr};
-    if (int rc = run(a, scale)) return rc;
+    if (int rc = run(a, scale, n_valid)) return rc;
     const double denom = reduction == 0 ? static_cast<double>(n_valid) : 1.0;
     loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<float*>(w8 + CL.lossrow), T, denom, hdr, loss, 0);
     return check_launch("loss_final");
@@ -928,12 +1103,17 @@ int linear_ce_impl(const void* X, const void* W, const int64_t* labels, int64_t 
         return fail(LIGER_ERR_SHAPE, "linear_ce: T=%lld H=%lld V=%lld chunk=%lld reduction=%d", (long long)T,
                     (long long)H, (long long)V, (long long)chunk, reduction);
     const Layout L = layout(T, H, V, chunk, dtype);
-    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.labs, L.total};
+    const size_t total = L.tc ? compact_layout(T, H, V, chunk, dtype).total : L.total;
+    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.labs, total};
     return ce_entry(
         "linear_ce", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws, ws_bytes, dtype,
         stream, CL,
-        [&](const Args& a, float scale) {
-            if (L.tc) return run_tc(a, L, scale);
+        [&](const Args& a, float scale, int64_t n_valid) {
+            if (L.tc) {
+                // some tokens ignored, and their count known on the host: run the others only
+                if (n_valid > 0 && n_valid < a.T) return run_tc_compact(a, n_valid, chunk, scale);
+                return run_tc(a, L, scale);
+            }
             if (dtype == LIGER_F32) return run_simt<float>(a, L, scale);
             return run_simt<__nv_bfloat16>(a, L, scale);
         },
@@ -977,7 +1157,7 @@ int linear_ce_two_pass_impl(const void* X, const void* W, const int64_t* labels,
     const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.labs, L.total};
     return ce_entry(
         "linear_ce_two_pass", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws, ws_bytes,
-        dtype, stream, CL, [&](const Args& a, float scale) { return run_two_pass(a, L, scale); }, sync);
+        dtype, stream, CL, [&](const Args& a, float scale, int64_t) { return run_two_pass(a, L, scale); }, sync);
 }
 }  // namespace
 
