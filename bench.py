@@ -381,13 +381,28 @@ def fused_linear_swiglu_measure(L, dev, T=8192, H=HIDDEN, I=INTER):
 
 
 WARMUP_ITERS, MIN_ITERS, MIN_TIMED_MS, FLOOR_ITERS = 10, 50, 200.0, 5
-# DRAM bytes (read + written) of one linear-CE call at seq 32768, scaled from an ncu capture of
-# the DRAM byte counters over the 11 launches of one call at seq 8192 with one chunk of 8192
-# tokens (the call's unit of work: the same launch shapes as each of the 4 chunks at seq 32768):
-# 4 x 34.48 GB per chunk, less the 3 bf16 dW writes only the last chunk makes (3 x 1.24 GB),
-# plus the fp32 dW sum the multi-chunk call passes through HBM 6 times (6 x 2.49 GB)
-LINEAR_CE_CHUNK_TRAFFIC = 34_476_864_768
-LINEAR_CE_TRAFFIC = 4 * LINEAR_CE_CHUNK_TRAFFIC - 3 * VOCAB * HIDDEN * 2 + 6 * VOCAB * HIDDEN * 4
+# DRAM bytes (read + written) of one linear-CE call at seq 32768 with 10 % of the labels ignored
+# (29491 valid tokens: compaction, then chunks of 8192, 8192, 8192 and 4915 rows): the sum of
+# ncu's dram__bytes_read.sum + dram__bytes_write.sum over the 38 launches of one whole call
+LINEAR_CE_TRAFFIC = 144_775_323_904
+
+
+def linear_ce_algorithmic_bytes(n_valid, T, H=None, V=None, chunk=8192):
+    """The bytes a token-chunked linear-CE call must move at least, each tensor once per pass
+    that has to touch it: per valid token 10*V bytes of the bf16 chunk buffer (P written,
+    dlogits reading P and writing D, the dX and dW GEMMs reading D), W read twice per chunk
+    (logits, dX), the fp32 dW sum written by every chunk but the last and read by every
+    chunk but the first, the bf16 dW written once, the compacted X rows read twice (logits,
+    dW) and dX rows written once, and the compaction's gather (valid X rows read and
+    written) and scatter (valid dX rows read, all T dX rows written)."""
+    H = HIDDEN if H is None else H
+    V = VOCAB if V is None else V
+    nchunks = -(-n_valid // chunk)
+    b = 10 * n_valid * V + 2 * nchunks * V * H * 2 + 2 * max(0, nchunks - 1) * V * H * 4 + V * H * 2
+    b += 3 * n_valid * H * 2
+    if n_valid < T:
+        b += 2 * n_valid * H * 2 + n_valid * H * 2 + T * H * 2
+    return b
 
 
 def timed_median(fn, pre=None):
@@ -972,10 +987,9 @@ def native_arm(args):
                 "achieved_counting_all_tokens": round(alg["linear_ce_flops_all_tokens"] /
                                                       (per_op["linear_ce"] / 1000.0) / 1e12, 1),
                 "traffic": LINEAR_CE_TRAFFIC if S == 32768 else None, "traffic_unit": "bytes per call",
-                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum over the launches of one "
-                                  "call with a single 8192-token chunk (seq 8192), scaled to the 4 chunks of seq "
-                                  "32768 plus the fp32 dW sum's 6 passes",
-                "traffic_algorithmic_approx": 84_000_000_000,
+                "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum summed over the 38 launches "
+                                  "of one whole call (seq 32768, 29491 valid tokens)",
+                "traffic_algorithmic": linear_ce_algorithmic_bytes(n_valid, S),
                 "peak_source": f"{pk['src']} bf16 sustained (cuBLAS loop under the power cap)",
                 "ms_per_call": round(per_op["linear_ce"], 3)}
     cpu = None

@@ -195,3 +195,16 @@ def test_data_parallel_exchanges_over_two_gloo_ranks():
         assert p.exitcode == 0
     for rank, n, loss, dW, dw, mean in out:
         assert n == 12 and loss == 4.5 and dW == [[3.0, 3.0]] * 3 and dw == [1.0, 2.0] and mean == 4.5 / 12
+
+
+def test_linear_ce_algorithmic_bytes():
+    """The roofline's algorithmic bytes, counted by hand for small shapes. One chunk, no
+    token ignored (T = 4, H = 8, V = 16): 10*T*V chunk-buffer bytes + W read twice + bf16
+    dW + X read twice and dX written once. Two chunks with 3 of 10 tokens ignored (chunk 4,
+    7 valid): the fp32 dW sum adds one write and one read, W is read twice per chunk, and
+    the compaction adds the gather (7 rows read and written) and the scatter (7 rows read,
+    10 written)."""
+    assert bench.linear_ce_algorithmic_bytes(4, 4, 8, 16) == 10 * 4 * 16 + 2 * 16 * 8 * 2 + 16 * 8 * 2 + 3 * 4 * 8 * 2
+    b = bench.linear_ce_algorithmic_bytes(7, 10, 8, 16, chunk=4)
+    assert b == (10 * 7 * 16 + 4 * 16 * 8 * 2 + 2 * 16 * 8 * 4 + 16 * 8 * 2 + 3 * 7 * 8 * 2
+                 + 2 * 7 * 8 * 2 + 7 * 8 * 2 + 10 * 8 * 2)
