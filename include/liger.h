@@ -391,7 +391,9 @@ int liger_linear_ce_fwd_bwd(const void* X, const void* W, const int64_t* labels,
  *           V > vchunk); the rows dW_c = D_c^T X are finished and written.
  *   8 T H V flops (the logits twice) against 6 T H V for
  *   liger_linear_ce_fwd_bwd; the workspace is O(T (H + vchunk)), not
- *   O(chunk V + V H).  bf16 only (tensor cores), H >= 64 and a multiple of 8,
+ *   O(chunk V + V H).  As there, when some labels are ignore_index only the
+ *   other tokens (gathered in order) go through both passes (8 n_valid H V
+ *   flops); the workspace holds their X and dX rows for that.  bf16 only (tensor cores), H >= 64 and a multiple of 8,
  *   V >= 256, vchunk a multiple of 8.  ws: at least
  *   liger_linear_ce_two_pass_workspace(T, H, V, vchunk) bytes, 256-byte
  *   aligned, with float lse[T] and float loss_row[T] at the same offsets as

@@ -208,3 +208,29 @@ def test_linear_ce_algorithmic_bytes():
     b = bench.linear_ce_algorithmic_bytes(7, 10, 8, 16, chunk=4)
     assert b == (10 * 7 * 16 + 4 * 16 * 8 * 2 + 2 * 16 * 8 * 4 + 16 * 8 * 2 + 3 * 7 * 8 * 2
                  + 2 * 7 * 8 * 2 + 7 * 8 * 2 + 10 * 8 * 2)
+
+
+def test_chain_step_waits_for_each_input_before_its_first_reader(monkeypatch):
+    """The end-to-end arm copies a step's inputs one by one; the step makes each
+    operator wait only for the inputs it is the first to read, in reading order,
+    and every per-step input is waited for exactly once."""
+    import numpy as np
+    import torch
+    monkeypatch.setattr(bench, "HIDDEN", 8)
+    monkeypatch.setattr(bench, "INTER", 12)
+    monkeypatch.setattr(bench, "VOCAB", 10)
+    S = 4
+    inputs = {k: np.zeros(sh, np.float32) for k, sh in
+              {"x": (S, 8), "w": (8,), "dy_r": (S, 8), "q": (1, S, 2, 4), "k": (1, S, 2, 4), "dq": (1, S, 2, 4),
+               "dk": (1, S, 2, 4), "gate": (S, 12), "up": (S, 12), "dy_s": (S, 12), "X": (S, 8),
+               "W": (10, 8)}.items()}
+    inputs["labels"] = np.array([1, -100, 3, 4], np.int64)
+    log = []
+    ch = bench.Chain(_RecordingLib(log), inputs, torch.device("cpu"))
+    ch.step(ready=lambda k: log.append(("ready", k, None)))
+    seq = [e[1] if e[0] == "ready" else e[0] for e in log]
+    assert seq == ["x", "liger_rmsnorm_fwd", "q", "k", "liger_rope_fwd", "gate", "up", "liger_swiglu_fwd",
+                   "X", "labels", "liger_linear_ce_fwd_bwd", "dy_s", "liger_swiglu_bwd", "dq", "dk",
+                   "liger_rope_bwd", "dy_r", "liger_rmsnorm_bwd"]
+    waited = sorted(e[1] for e in log if e[0] == "ready")
+    assert waited == sorted(k for k in inputs if k not in bench.PARAMETERS)

@@ -1,8 +1,8 @@
 """The linear cross-entropies without their host wait (liger_linear_ce_fwd_bwd_async,
 liger_linear_ce_two_pass_fwd_bwd_async), through the C-ABI: bit-identical to
 the waiting forms when no label is ignored (tensor-core and fp32 SIMT paths,
-both reductions); with ignored labels the waiting token-chunked form runs the
-other tokens only, so lse and dX stay bit-identical (each row is computed from
+both reductions); with ignored labels the waiting bf16 forms (token-chunked and
+two-pass) run the other tokens only, so lse and dX stay bit-identical (each row is computed from
 the same operands in the same order) while dW and the loss are sums over a
 different grouping of the tokens, equal within rounding; a bad label is
 treated as ignored and makes the loss NaN,
@@ -71,7 +71,7 @@ def test_async_matches_waiting_form(cuda_lib, T, H, V, dtype, two_pass, reductio
     X, W, lab = _inputs(71, T, H, V, dtype)
     a = _call(cuda_lib, X, W, lab, two_pass, True, reduction, 0.5, chunk)
     b = _call(cuda_lib, X, W, lab, two_pass, False, reduction, 0.5, chunk)
-    compacted = dtype == "bf16" and not two_pass
+    compacted = dtype == "bf16"
     if not compacted:
         _same(a, b)
         return
@@ -91,13 +91,11 @@ def test_async_bad_labels_are_ignored_and_the_loss_is_nan(cuda_lib, two_pass):
     got = _call(cuda_lib, X, W, bad, two_pass, wait=False)
     want = _call(cuda_lib, X, W, fixed, two_pass, wait=True)
     assert math.isnan(got[0].item())
-    if two_pass:
-        _same(got[1:], want[1:])
-    else:   # the waiting form runs the non-ignored tokens only: dW summed over another grouping
-        import oracle
-        from gpu_util import host
-        _same((got[1], got[3]), (want[1], want[3]))
-        assert oracle.rel_err(host(got[2]), host(want[2])) <= 1e-2
+    # the waiting form runs the non-ignored tokens only: dW summed over another grouping
+    import oracle
+    from gpu_util import host
+    _same((got[1], got[3]), (want[1], want[3]))
+    assert oracle.rel_err(host(got[2]), host(want[2])) <= 1e-2
     with pytest.raises(cuda_lib.LigerError) as e:   # the waiting form refuses the batch
         _call(cuda_lib, X, W, bad, two_pass, wait=True)
     assert e.value.status == -5

@@ -119,24 +119,24 @@ Layout layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
     return L;
 }
 
-// Workspace of the waiting tensor-core entry point, which runs the chunked GEMMs
-// on the tokens that are not ignored only: the ordinary layout's lse, loss_row and
-// header first (lse and loss_row of every token, as documented), then the region
-// the chunked path runs in for those tokens (at most the ordinary layout's size),
-// then their X rows, their dX rows, their labels and the index maps.
+// Workspace of the waiting tensor-core entry points, which run their GEMMs on the
+// tokens that are not ignored only: the ordinary layout's lse, loss_row and header
+// first (lse and loss_row of every token, as documented), then the region the
+// variant runs in for those tokens (at most the ordinary layout's size), then
+// their X rows, their dX rows, their labels and the index maps.
 struct CompactLayout {
     size_t core, xc, dxc, labc, idx, inv, cnt, total;
 };
 
 constexpr int kCompactBlock = 1024;   // tokens per block of the compaction's index pass
 
-CompactLayout compact_layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
-    const Layout L = layout(T, H, V, chunk, dtype);
-    const size_t esz = dtype == LIGER_F32 ? 4 : 2;
+// core_at: where the ordinary layout's per-call part ends (after lse, loss_row, z_label
+// and the header); core_total: the ordinary layout's size for all T tokens
+CompactLayout compact_regions(size_t core_at, size_t core_total, int64_t T, int64_t H, size_t esz) {
     const size_t t = static_cast<size_t>(std::max<int64_t>(T, 1));
     CompactLayout C{};
-    size_t o = L.labs;   // after lse, loss_row, z_label and the header of the ordinary layout
-    C.core = o; o = up256(o + L.total);
+    size_t o = core_at;
+    C.core = o; o = up256(o + core_total);
     C.xc = o; o = up256(o + t * static_cast<size_t>(H) * esz);
     C.dxc = o; o = up256(o + t * static_cast<size_t>(H) * esz);
     C.labc = o; o = up256(o + t * sizeof(int64_t));
@@ -145,6 +145,11 @@ CompactLayout compact_layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int
     C.cnt = o; o = up256(o + sizeof(int) * static_cast<size_t>(ceil_div(static_cast<int64_t>(t), int64_t{kCompactBlock})));
     C.total = o;
     return C;
+}
+
+CompactLayout compact_layout(int64_t T, int64_t H, int64_t V, int64_t chunk, int dtype) {
+    const Layout L = layout(T, H, V, chunk, dtype);
+    return compact_regions(L.labs, L.total, T, H, dtype == LIGER_F32 ? 4 : 2);
 }
 
 // ---------------------------------------------------------------- kernels
@@ -794,17 +799,21 @@ int run_tc(const Args& a, const Layout& L, float scale) {
     return LIGER_OK;
 }
 
-// The chunked path on the tokens that are not ignored only (n_valid of T, known on
+// Where a layout keeps its per-token lse and loss terms and its header.
+struct RowVals {
+    size_t lse, lossrow, hdr;
+};
+
+// A variant's GEMMs on the tokens that are not ignored only (n_valid of T, known on
 // the host from the label scan): an ignored token has D = 0, so it adds nothing to
 // dW and its dX row, lse and loss term are 0; its logits, which the GEMMs would
 // otherwise compute, are not needed.  The tokens are compacted in order (their X
-// rows and labels gathered), the chunked path runs on them in its own region of the
-// workspace, and dX, lse and the loss terms are put back in place.
-int run_tc_compact(const Args& a, int64_t n_valid, int64_t chunk, float scale) {
-    const CompactLayout C = compact_layout(a.T, a.H, a.V, chunk, a.dtype);
-    const Layout Lt = layout(a.T, a.H, a.V, chunk, a.dtype);   // the documented lse / loss_row of every token
-    const Layout Lc = layout(n_valid, a.H, a.V, chunk, a.dtype);
-    if (Lc.total > Lt.total) return run_tc(a, Lt, scale);   // the region holds any layout of fewer tokens
+// rows and labels gathered), run_core runs the variant on them in the region C.core
+// (its own layout for n_valid tokens, whose lse, loss terms and header sit at cv),
+// and dX, lse and the loss terms are put back in place (tv: the full layout's).
+template <typename RunCore>
+int run_compacted(const Args& a, int64_t n_valid, const CompactLayout& C, const RowVals& tv, const RowVals& cv,
+                  RunCore run_core) {
     uint8_t* w8 = a.ws;
     int* cnt = reinterpret_cast<int*>(w8 + C.cnt);
     int64_t* idx = reinterpret_cast<int64_t*>(w8 + C.idx);
@@ -819,7 +828,7 @@ int run_tc_compact(const Args& a, int64_t n_valid, int64_t chunk, float scale) {
     gather_rows<<<rgrid, 256, 0, a.st>>>(static_cast<const uint4*>(a.X), idx, n_valid, hv,
                                          reinterpret_cast<uint4*>(w8 + C.xc));
     if (int rc = check_launch("linear_ce compaction")) return rc;
-    Hdr* hc = reinterpret_cast<Hdr*>(w8 + C.core + Lc.hdr);
+    Hdr* hc = reinterpret_cast<Hdr*>(w8 + C.core + cv.hdr);
     if (cudaMemsetAsync(hc, 0, sizeof(Hdr), a.st) != cudaSuccess) return check_launch("linear_ce memset");
     Args b = a;
     b.X = w8 + C.xc;
@@ -827,19 +836,28 @@ int run_tc_compact(const Args& a, int64_t n_valid, int64_t chunk, float scale) {
     b.T = n_valid;
     b.dX = a.dX ? static_cast<void*>(w8 + C.dxc) : nullptr;
     b.ws = w8 + C.core;
-    if (int rc = run_tc(b, Lc, scale)) return rc;
+    if (int rc = run_core(b)) return rc;
     if (a.dX) {
         const int tgrid = static_cast<int>(std::min<int64_t>(a.T, 8 * sm_count()));
         scatter_rows<<<tgrid, 256, 0, a.st>>>(reinterpret_cast<const uint4*>(w8 + C.dxc), inv, a.T, hv,
                                               static_cast<uint4*>(a.dX));
     }
     const int vgrid = static_cast<int>(std::min<int64_t>(ceil_div(a.T, int64_t{256}), 4 * sm_count()));
-    scatter_rowvals<<<vgrid, 256, 0, a.st>>>(reinterpret_cast<const float*>(w8 + C.core + Lc.lse),
-                                             reinterpret_cast<const float*>(w8 + C.core + Lc.lossrow), inv, a.T,
-                                             reinterpret_cast<float*>(w8 + Lt.lse),
-                                             reinterpret_cast<float*>(w8 + Lt.lossrow), &hc->err,
-                                             &reinterpret_cast<Hdr*>(w8 + Lt.hdr)->err);
+    scatter_rowvals<<<vgrid, 256, 0, a.st>>>(reinterpret_cast<const float*>(w8 + C.core + cv.lse),
+                                             reinterpret_cast<const float*>(w8 + C.core + cv.lossrow), inv, a.T,
+                                             reinterpret_cast<float*>(w8 + tv.lse),
+                                             reinterpret_cast<float*>(w8 + tv.lossrow), &hc->err,
+                                             &reinterpret_cast<Hdr*>(w8 + tv.hdr)->err);
     return check_launch("linear_ce scatter");
+}
+
+// The token-chunked path on the tokens that are not ignored only.
+int run_tc_compact(const Args& a, int64_t n_valid, int64_t chunk, float scale) {
+    const Layout Lt = layout(a.T, a.H, a.V, chunk, a.dtype);   // the documented lse / loss_row of every token
+    const Layout Lc = layout(n_valid, a.H, a.V, chunk, a.dtype);
+    if (Lc.total > Lt.total) return run_tc(a, Lt, scale);   // the region holds any layout of fewer tokens
+    return run_compacted(a, n_valid, compact_layout(a.T, a.H, a.V, chunk, a.dtype), RowVals{Lt.lse, Lt.lossrow, Lt.hdr},
+                         RowVals{Lc.lse, Lc.lossrow, Lc.hdr}, [&](const Args& b) { return run_tc(b, Lc, scale); });
 }
 
 // --------------------------------------- two-pass (vocab-chunked) variant
@@ -1005,6 +1023,21 @@ int run_two_pass(const Args& a, const Layout2& L, float scale) {
     return LIGER_OK;
 }
 
+CompactLayout compact_layout2(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
+    const Layout2 L = layout2(T, H, V, vchunk);
+    return compact_regions(L.labs, L.total, T, H, 2);
+}
+
+// The two-pass path on the tokens that are not ignored only (both passes skip the
+// ignored tokens' logits).
+int run_two_pass_compact(const Args& a, int64_t n_valid, int64_t vchunk, float scale) {
+    const Layout2 Lt = layout2(a.T, a.H, a.V, vchunk);
+    const Layout2 Lc = layout2(n_valid, a.H, a.V, vchunk);
+    if (Lc.total > Lt.total) return run_two_pass(a, Lt, scale);
+    return run_compacted(a, n_valid, compact_layout2(a.T, a.H, a.V, vchunk), RowVals{Lt.lse, Lt.lossrow, Lt.hdr},
+                         RowVals{Lc.lse, Lc.lossrow, Lc.hdr}, [&](const Args& b) { return run_two_pass(b, Lc, scale); });
+}
+
 }  // namespace
 }  // namespace liger
 
@@ -1139,7 +1172,7 @@ extern "C" int liger_linear_ce_fwd_bwd_async(const void* X, const void* W, const
 
 extern "C" size_t liger_linear_ce_two_pass_workspace(int64_t T, int64_t H, int64_t V, int64_t vchunk) {
     if (T < 0 || H <= 0 || V <= 0 || vchunk < 0) return 0;
-    return layout2(T, H, V, vchunk).total;
+    return compact_layout2(T, H, V, vchunk).total;
 }
 
 namespace {
@@ -1154,10 +1187,16 @@ int linear_ce_two_pass_impl(const void* X, const void* W, const int64_t* labels,
                     "(H >= 64 and a multiple of 8, V >= 256, vchunk a multiple of 8)", (long long)T, (long long)H,
                     (long long)V, (long long)vchunk, reduction);
     const Layout2 L = layout2(T, H, V, vchunk);
-    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.labs, L.total};
+    const CommonLayout CL{L.lse, L.lossrow, L.hdr, L.labs, compact_layout2(T, H, V, vchunk).total};
     return ce_entry(
         "linear_ce_two_pass", X, W, labels, T, H, V, ignore_index, reduction, grad_scale, loss, dX, dW, ws, ws_bytes,
-        dtype, stream, CL, [&](const Args& a, float scale, int64_t) { return run_two_pass(a, L, scale); }, sync);
+        dtype, stream, CL,
+        [&](const Args& a, float scale, int64_t n_valid) {
+            // some tokens ignored, and their count known on the host: run the others only
+            if (n_valid > 0 && n_valid < a.T) return run_two_pass_compact(a, n_valid, vchunk, scale);
+            return run_two_pass(a, L, scale);
+        },
+        sync);
 }
 }  // namespace
 
