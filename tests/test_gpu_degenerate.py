@@ -71,3 +71,42 @@ def test_rmsnorm_qkv_rope_single_token(cuda_lib):
     assert oracle.rel_err(host(q), oq) <= TOL["bf16"]
     assert oracle.rel_err(host(k), ok_) <= TOL["bf16"]
     assert oracle.rel_err(host(v), ov) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("T,H,V,valid", [(1000, 128, 700, (517,)), (300, 64, 300, (0, 299)),
+                                         (257, 64, 513, "all but 128")])
+def test_linear_ce_compaction_extremes(cuda_lib, T, H, V, valid):
+    """The waiting bf16 entry points run only the tokens whose label is not
+    ignored: one valid token among a thousand (the run is a single row), the first
+    and last tokens only, and every token but one; against the oracle, with the
+    ignored rows of dX and lse exactly +0."""
+    import torch
+    X = datagen.normal(74, "cX", (T, H), "bf16")
+    W = datagen.normal(74, "cW", (V, H), "bf16", 0.0, 0.05)
+    lab = datagen.labels(74, "cl", T, V, 0.0)
+    keep = np.zeros(T, bool)
+    if valid == "all but 128":
+        keep[:] = True
+        keep[128] = False
+    else:
+        keep[list(valid)] = True
+    lab[~keep] = -100
+    o = oracle.linear_ce(X, W, lab)
+    for two_pass in (False, True):
+        n = (cuda_lib.liger_linear_ce_two_pass_workspace(T, H, V) if two_pass
+             else cuda_lib.liger_linear_ce_workspace(T, H, V, 0, cuda_lib.LIGER_BF16))
+        ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+        loss = torch.empty(1, dtype=torch.float32, device="cuda")
+        tX, tW = dev(X), dev(W)
+        dX, dW = torch.full_like(tX, 7.0), torch.empty_like(tW)
+        fn = cuda_lib.liger_linear_ce_two_pass_fwd_bwd if two_pass else cuda_lib.liger_linear_ce_fwd_bwd
+        fn(tX, tW, dev(lab), loss, dX, dW, ws)
+        torch.cuda.synchronize()
+        assert abs(float(loss.item()) - o["loss"]) <= LOSS_TOL_BF16 * abs(o["loss"])
+        hdX = host(dX)
+        assert oracle.rel_err(hdX, o["dX"]) <= TOL["bf16"]
+        assert np.all(hdX[~keep] == 0) and not np.any(np.signbit(hdX[~keep]))
+        assert oracle.rel_err(host(dW), o["dW"]) <= TOL["bf16"]
+        lse = host(ws[: 4 * T].view(torch.float32))
+        assert np.all(lse[~keep] == 0)
+        assert oracle.rel_err(lse[keep], o["lse"][keep]) <= 1e-3
