@@ -480,6 +480,25 @@ __device__ __forceinline__ void bwd_issue_row(uint8_t* sm, uint32_t bars, const 
     bulk_g2s(smem_u32(dst + rb), x + r * cols, rb, bar);
 }
 
+// Two products of packed bf16 pairs in fp32: (a.lo b.lo + c.x, a.hi b.hi + c.y), each
+// rounded once (the product of two bf16 values is exact in fp32).  The mixed-precision
+// fma takes the bf16 halves of the packed words as they are, so neither operand is
+// widened to fp32 by separate instructions first.
+__device__ __forceinline__ float2 fma_bf2(uint32_t a, uint32_t b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %2;\n\t"
+        "mov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %4;\n\t"
+        "fma.rn.f32.bf16 %1, ah, bh, %5;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "r"(a), "r"(b), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ uint32_t word(const uint4& u, int e) {
+    return e == 0 ? u.x : e == 1 ? u.y : e == 2 ? u.z : u.w;
+}
+
 // Staged backward, two rows per block barrier: the block reduces the dot
 // products of its rows i and i + 1 together (two independent shuffle trees,
 // one barrier), then reads both rows again from shared memory for dx and dw,
@@ -488,6 +507,12 @@ __device__ __forceinline__ void bwd_issue_row(uint8_t* sm, uint32_t bars, const 
 // thread 0 refills with rows i - 2 + nst and i - 1 + nst (nst >= 4).  Each
 // block takes a contiguous group of rows (rows interleaved across blocks
 // measured no faster).
+// In bf16 the products are formed from the packed words by the mixed-precision
+// fma (no separate widening of dy and w, nor of x before the barrier): before
+// the barrier q = dy x feeds both the dot product (w q) and the dw sums (q rstd,
+// rstd fetched a pair of rows ahead); after it dx = rstd (w dy) - c x.  Every
+// product of two bf16 values is exact in fp32, so the results are those of the
+// widened arithmetic bit for bit.
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kBwdStagedMaxThreads, 3) rmsnorm_bwd_staged2(const T* dy, const T* __restrict__ x,
                                                            const T* __restrict__ w, const float* __restrict__ rstd,
@@ -513,19 +538,35 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads, 3) rmsnorm_bwd_staged2(c
     // arithmetic on pairs of columns with the packed fp32x2 instructions (half the
     // floating-point instruction count of scalar code)
     constexpr int NP = EPV / 2;
+    constexpr bool MX = sizeof(T) == 2;   // bf16: products from the packed words (mixed-precision fma)
     float2 wf[VPT][NP], dwa[VPT][NP];
+    uint4 wraw[VPT];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = j * NT + tid;
-        unpack2(v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0), wf[j]);
+        wraw[j] = v < nvec ? ldg16_nc(w + static_cast<int64_t>(v) * EPV) : make_uint4(0, 0, 0, 0);
+        unpack2(wraw[j], wf[j]);
 #pragma unroll
         for (int e = 0; e < NP; ++e) dwa[j][e] = make_float2(0.f, 0.f);
     }
     const float inv_cols = 1.0f / static_cast<float>(cols);
+    const float2 nz2 = make_float2(-0.f, -0.f);
+    // bf16: rstd of the current pair of rows (the dw sums use it before the barrier), fetched a
+    // pair ahead
+    float rsc0 = 0.f, rsc1 = 0.f;
+    if (MX) {
+        rsc0 = nr > 0 ? rstd[row_of(0)] : 0.f;
+        rsc1 = nr > 1 ? rstd[row_of(1)] : 0.f;
+    }
     bool ok = true;
     int64_t i = 0;
     int it = 0;
     for (; i < nr; i += 2, ++it) {
+        float rsn0 = 0.f, rsn1 = 0.f;
+        if (MX) {
+            rsn0 = i + 2 < nr ? rstd[row_of(i + 2)] : 0.f;
+            rsn1 = i + 3 < nr ? rstd[row_of(i + 3)] : 0.f;
+        }
         const bool two = i + 1 < nr;
         const int s0 = static_cast<int>(i % nst), s1 = static_cast<int>((i + 1) % nst);
         bool got = mbar_wait(bars + 8u * s0, static_cast<uint32_t>(i / nst) & 1u);
@@ -538,16 +579,40 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads, 3) rmsnorm_bwd_staged2(c
             for (int j = 0; j < VPT; ++j) {
                 const int v = j * NT + tid;
                 if (v < nvec) {
-                    float2 fx[NP], fd[NP];
-                    unpack2(*reinterpret_cast<const uint4*>(b0 + static_cast<size_t>(v) * 16), fd);
-                    unpack2(*reinterpret_cast<const uint4*>(b0 + rb + static_cast<size_t>(v) * 16), fx);
+                    if constexpr (MX) {
+                        // q = dy x in fp32 (exact); the dot product takes w q and the dw sums
+                        // q rstd, both here, before the barrier
+                        const float2 r0 = make_float2(rsc0, rsc0), r1 = make_float2(rsc1, rsc1);
+                        const uint4 ud = *reinterpret_cast<const uint4*>(b0 + static_cast<size_t>(v) * 16);
+                        const uint4 ux = *reinterpret_cast<const uint4*>(b0 + rb + static_cast<size_t>(v) * 16);
 #pragma unroll
-                    for (int e = 0; e < NP; ++e) a0 = __ffma2_rn(__fmul2_rn(fd[e], wf[j][e]), fx[e], a0);
-                    if (two) {
-                        unpack2(*reinterpret_cast<const uint4*>(b1 + static_cast<size_t>(v) * 16), fd);
-                        unpack2(*reinterpret_cast<const uint4*>(b1 + rb + static_cast<size_t>(v) * 16), fx);
+                        for (int e = 0; e < NP; ++e) {
+                            const float2 q = fma_bf2(word(ud, e), word(ux, e), nz2);
+                            a0 = __ffma2_rn(wf[j][e], q, a0);
+                            dwa[j][e] = __ffma2_rn(q, r0, dwa[j][e]);
+                        }
+                        if (two) {
+                            const uint4 vd = *reinterpret_cast<const uint4*>(b1 + static_cast<size_t>(v) * 16);
+                            const uint4 vx = *reinterpret_cast<const uint4*>(b1 + rb + static_cast<size_t>(v) * 16);
 #pragma unroll
-                        for (int e = 0; e < NP; ++e) a1 = __ffma2_rn(__fmul2_rn(fd[e], wf[j][e]), fx[e], a1);
+                            for (int e = 0; e < NP; ++e) {
+                                const float2 q = fma_bf2(word(vd, e), word(vx, e), nz2);
+                                a1 = __ffma2_rn(wf[j][e], q, a1);
+                                dwa[j][e] = __ffma2_rn(q, r1, dwa[j][e]);
+                            }
+                        }
+                    } else {
+                        float2 fx[NP], fd[NP];
+                        unpack2(*reinterpret_cast<const uint4*>(b0 + static_cast<size_t>(v) * 16), fd);
+                        unpack2(*reinterpret_cast<const uint4*>(b0 + rb + static_cast<size_t>(v) * 16), fx);
+#pragma unroll
+                        for (int e = 0; e < NP; ++e) a0 = __ffma2_rn(__fmul2_rn(fd[e], wf[j][e]), fx[e], a0);
+                        if (two) {
+                            unpack2(*reinterpret_cast<const uint4*>(b1 + static_cast<size_t>(v) * 16), fd);
+                            unpack2(*reinterpret_cast<const uint4*>(b1 + rb + static_cast<size_t>(v) * 16), fx);
+#pragma unroll
+                            for (int e = 0; e < NP; ++e) a1 = __ffma2_rn(__fmul2_rn(fd[e], wf[j][e]), fx[e], a1);
+                        }
                     }
                 }
             }
@@ -584,14 +649,26 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads, 3) rmsnorm_bwd_staged2(c
         for (int rr = 0; rr < 2; ++rr) {
             if (rr == 1 && !two) break;
             const int64_t r = row_of(i + rr);
-            const float rs = rstd[r];
+            const float rs = MX ? (rr ? rsc1 : rsc0) : rstd[r];
             const float c = rs * rs * rs * inv_cols * (rr ? t1 : t0);
             const float2 rs2 = make_float2(rs, rs), nc2 = make_float2(-c, -c);
             const uint8_t* bb = rr ? b1 : b0;
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const int v = j * NT + tid;
-                if (v < nvec) {
+                if (v < nvec && MX) {
+                    // dx = rs (w dy) - c x, with w dy formed from the packed words
+                    const uint4 ud = *reinterpret_cast<const uint4*>(bb + static_cast<size_t>(v) * 16);
+                    const uint4 ux = *reinterpret_cast<const uint4*>(bb + rb + static_cast<size_t>(v) * 16);
+                    float2 fx[NP], o[NP];
+                    unpack2(ux, fx);
+#pragma unroll
+                    for (int e = 0; e < NP; ++e) {
+                        const float2 u = fma_bf2(word(wraw[j], e), word(ud, e), nz2);
+                        o[e] = __ffma2_rn(nc2, fx[e], __fmul2_rn(rs2, u));
+                    }
+                    stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, pack2(o));
+                } else if (v < nvec) {
                     float2 fx[NP], fd[NP], o[NP];
                     unpack2(*reinterpret_cast<const uint4*>(bb + static_cast<size_t>(v) * 16), fd);
                     unpack2(*reinterpret_cast<const uint4*>(bb + rb + static_cast<size_t>(v) * 16), fx);
@@ -604,6 +681,10 @@ __global__ void __launch_bounds__(kBwdStagedMaxThreads, 3) rmsnorm_bwd_staged2(c
                     stg16(dx + r * cols + static_cast<int64_t>(v) * EPV, pack2(o));
                 }
             }
+        }
+        if (MX) {
+            rsc0 = rsn0;
+            rsc1 = rsn1;
         }
     }
     float* pr = part + static_cast<int64_t>(blockIdx.x) * cols;
