@@ -17,8 +17,11 @@
 //    each thread owns fixed 16-byte column vectors and keeps its share of dw
 //    in fp32 registers across the group's rows (no atomics); the dot products
 //    of two rows are reduced together (shuffles, one block barrier), then the
-//    two rows are read again from shared memory for dx and dw; the float
-//    arithmetic runs on column pairs with the packed fp32x2 instructions.
+//    two rows are read again from shared memory for dx (and, in fp32, dw); in
+//    bf16 the products come straight from the packed words through the
+//    mixed-precision fma (exact, so no widening instructions for dy and w)
+//    and dw is summed before the barrier; the other float arithmetic runs on
+//    column pairs with the packed fp32x2 instructions.
 //    Other widths: the row in registers, or a generic loop.
 //  * dw: per-block partial rows (workspace) summed by a second kernel in a
 //    fixed order, so dw is deterministic.
