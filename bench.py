@@ -900,15 +900,12 @@ def native_arm(args):
     tokens = sum_over_ranks(float(S * K), dist, dev)
     value = tokens / (ms / 1000.0)
     per_op = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in ev.items()}
-    iso = isolated_times(chain, dev)
-    mlp = fused_linear_swiglu_measure(L, dev)
-    qkv = rmsnorm_qkv_rope_measure(L, dev, S)
-    two_pass = linear_ce_two_pass_measure(chain, dev)
     loss = float(chain.loss.item())
     if dp is not None:
         loss = dp.mean_loss(loss)
 
-    # ---- end to end through host buffers: every step copies its inputs (activations,
+    # ---- end to end through host buffers (measured right after the device-resident steps, so
+    # that both see the GPU in the same power and thermal state): every step copies its inputs (activations,
     # labels, upstream gradients) host -> device from pinned memory and reads its loss back;
     # the parameters (RMSNorm weight, lm_head weight) stay resident on the device, as in a
     # training loop.  The copies run on a second stream into the other half of a
@@ -978,6 +975,12 @@ def native_arm(args):
                "h2d_alone_ms": round(h2d_ms, 3), "h2d_alone_gbs": round(h2d / (h2d_ms / 1000.0) / 1e9, 1)}
         chain.inp = sets[0]
         del host, sets
+
+    # ---- each memory-bound operator alone, and the operators of the next rows
+    iso = isolated_times(chain, dev)
+    mlp = fused_linear_swiglu_measure(L, dev)
+    qkv = rmsnorm_qkv_rope_measure(L, dev, S)
+    two_pass = linear_ce_two_pass_measure(chain, dev)
 
     if rank != 0:
         if dist:
