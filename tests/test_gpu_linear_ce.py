@@ -402,3 +402,28 @@ def test_linear_ce_dw_grouped_tile_order_against_the_oracle(cuda_lib):
             assert np.all(bits(dX)[r] == 0)
             continue
         assert oracle.rel_err(hdX[r], od["dX"][i]) <= 2e-2
+
+
+@pytest.mark.parametrize("two_pass", [False, True])
+@pytest.mark.parametrize("want", [(True, False), (False, True), (False, False)])
+def test_linear_ce_optional_gradients(cuda_lib, two_pass, want):
+    """dX and dW may each be NULL (not computed). With 10 % of the labels ignored the
+    bf16 entry points run only the other tokens (compacted), and the loss, lse and
+    whichever gradients were asked for still match the oracle."""
+    import torch
+    T, H, V = 700, 192, 3000
+    X = datagen.normal(27, "oX", (T, H), "bf16")
+    W = datagen.normal(27, "oW", (V, H), "bf16", 0.0, 0.05)
+    lab = datagen.labels(27, "ol", T, V, 0.1)
+    tX, tW = dev(X), dev(W)
+    n = (cuda_lib.liger_linear_ce_two_pass_workspace(T, H, V) if two_pass
+         else cuda_lib.liger_linear_ce_workspace(T, H, V, 0, cuda_lib.LIGER_BF16))
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    loss = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    dX = torch.empty_like(tX) if want[0] else None
+    dW = torch.empty_like(tW) if want[1] else None
+    fn = cuda_lib.liger_linear_ce_two_pass_fwd_bwd if two_pass else cuda_lib.liger_linear_ce_fwd_bwd
+    fn(tX, tW, dev(lab), loss, dX, dW, ws)
+    torch.cuda.synchronize()
+    lse = ws[: 4 * T].view(torch.float32).cpu().numpy().astype(np.float64)
+    _check_full(X, W, lab, "bf16", float(loss.item()), dX, dW, lse)
