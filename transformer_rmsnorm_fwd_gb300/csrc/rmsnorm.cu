@@ -358,10 +358,10 @@ __global__ void rmsnorm_fwd_staged(const T* x, const T* __restrict__ w, T* y, fl
     bool ok = __all_sync(0xffffffffu, mbar_wait(wbar, 0));
     const float inv_cols = 1.0f / static_cast<float>(cols);
     int it = 0;
+    int s = 0;          // it % nst, kept without a division (nst is a runtime value)
+    uint32_t ph = 0;    // (it / nst) & 1
     int64_t r = gw;
     for (; ok && r < rows; r += stride, ++it) {
-        const int s = it % nst;
-        const uint32_t ph = static_cast<uint32_t>(it / nst) & 1u;
         if (!__all_sync(0xffffffffu, mbar_wait(mybar + 8u * s, ph))) {
             ok = false;
             break;
@@ -395,14 +395,18 @@ __global__ void rmsnorm_fwd_staged(const T* x, const T* __restrict__ w, T* y, fl
                 bulk_g2s(smem_u32(ring + s * rb), x + rn * cols, rb, mybar + 8u * s);
             }
         }
+        if (++s == nst) {
+            s = 0;
+            ph ^= 1u;
+        }
     }
     if (!ok) {
         if (lane == 0) {
             atomicExch(&g_stage_err, 1);
             // copies already issued into this warp's ring: the next phase of each buffer
-            for (int s = 0; s < nst; ++s) {
-                const int64_t first = static_cast<int64_t>(it) + ((s - it % nst) + nst) % nst;  // next use of buffer s
-                if (gw + first * stride < rows) mbar_wait(mybar + 8u * s, static_cast<uint32_t>(first / nst) & 1u);
+            for (int sb = 0; sb < nst; ++sb) {
+                const int64_t first = static_cast<int64_t>(it) + ((sb - it % nst) + nst) % nst;  // next use of buffer sb
+                if (gw + first * stride < rows) mbar_wait(mybar + 8u * sb, static_cast<uint32_t>(first / nst) & 1u);
             }
         }
         // the rows this warp did not finish: NaN
@@ -471,6 +475,7 @@ int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
 }
 
 constexpr int kBwdStagedMaxThreads = 256;
+constexpr int kBwdRing = 4;   // (dy, x) row buffers of a staged backward block: two in use, two in flight
 
 // Row r of dy and x into ring buffer s (one mbarrier per buffer).
 template <typename T>
@@ -520,7 +525,8 @@ template <typename T, int VPT>
 __global__ void __launch_bounds__(kBwdStagedMaxThreads, 3) rmsnorm_bwd_staged2(const T* dy, const T* __restrict__ x,
                                                            const T* __restrict__ w, const float* __restrict__ rstd,
                                                            T* dx, float* __restrict__ part, int64_t rows, int cols,
-                                                           int64_t rows_per_block, int nst) {
+                                                           int64_t rows_per_block) {
+    constexpr int nst = kBwdRing;   // ring slots: slot and phase arithmetic on a constant
     constexpr int EPV = Vec<T>::N;
     extern __shared__ __align__(128) uint8_t sm[];
     __shared__ float red[2][2][32];
@@ -739,12 +745,11 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
     T* dxp = static_cast<T*>(dx);
     bool done = false;
     const int rbytes = cols * static_cast<int>(sizeof(T));
-    if (cols % EPV == 0 && cols / EPV <= 2 * kBwdStagedMaxThreads && bwd_staged_smem(rbytes, 4) <= 100u * 1024u) {
+    if (cols % EPV == 0 && cols / EPV <= 2 * kBwdStagedMaxThreads && bwd_staged_smem(rbytes, kBwdRing) <= 100u * 1024u) {
         // staged path: up to 4 rows in flight per block, about 3 blocks per SM at 8 KB rows
         const int nvec = cols / EPV;
-        // a ring of 4 (dy, x) row pairs: two rows in use, two in flight
-        const int nst = 4;
-        const size_t ssm = bwd_staged_smem(rbytes, nst);
+        // a ring of kBwdRing (dy, x) row pairs: two rows in use, two in flight
+        const size_t ssm = bwd_staged_smem(rbytes, kBwdRing);
         auto go = [&](auto kern, int vpt) -> int {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm)) !=
                 cudaSuccess)
@@ -757,8 +762,7 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
                                                                        kMaxPartials}));
             const int64_t rpb2 = ceil_div(rows, P2);
             grid_used = ceil_div(rows, rpb2);
-            kern<<<static_cast<unsigned>(grid_used), nt, ssm, st>>>(dyp, xp, wp, rstd, dxp, part, rows, cols, rpb2,
-                                                                    nst);
+            kern<<<static_cast<unsigned>(grid_used), nt, ssm, st>>>(dyp, xp, wp, rstd, dxp, part, rows, cols, rpb2);
             done = true;
             return check_launch("rmsnorm_bwd_staged");
         };
