@@ -495,46 +495,54 @@ __global__ void __launch_bounds__(1024) loss_final(const float* __restrict__ los
 //  mode 0: outf[m, n]  = acc          mode 2: outf[m, n] += acc
 //  mode 1: outT[m, n]  = acc          mode 3: outT[m, n]  = acc + outf[m, n]
 // mode 1 writes +0 on rows whose label is ignore_index (labels may be NULL).
+// SBT x SBT output tiles (64, or 32 when 64-wide tiles would leave SMs idle), 256
+// threads each holding (SBT/16)^2 of them; k steps of SKT (16, or 64 with the small
+// tiles: fewer load-then-synchronise rounds, more loads in flight in each).
 constexpr int SB = 64, SK = 16;
-template <typename TA, typename TB, typename TO, int MODE>
+template <typename TA, typename TB, typename TO, int MODE, int SBT, int SKT>
 __global__ void __launch_bounds__(256) simt_gemm(int M, int N, int K, const TA* __restrict__ A, int64_t sam,
                                                  int64_t sak, const TB* __restrict__ B, int64_t sbk, int64_t sbn,
                                                  float* outf, TO* outT, int64_t ldo, const int64_t* __restrict__ labels,
                                                  int64_t ignore) {
-    __shared__ float As[SK][SB + 1], Bs[SK][SB + 1];
-    const int m0 = blockIdx.y * SB, n0 = blockIdx.x * SB;
+    constexpr int RT = SBT / 16;
+    __shared__ float As[SKT][SBT + 1], Bs[SKT][SBT + 1];
+    const int m0 = blockIdx.y * SBT, n0 = blockIdx.x * SBT;
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < K; k0 += SK) {
-        for (int i = threadIdx.x; i < SB * SK; i += 256) {
-            const int mm = i / SK, kk = i % SK;
+    float acc[RT][RT] = {};
+    const bool ak = sak == 1, bn = sbn == 1;
+    for (int k0 = 0; k0 < K; k0 += SKT) {
+        // consecutive threads take consecutive elements of each operand's contiguous
+        // dimension (k when sak == 1, else m; n when sbn == 1, else k), so the loads coalesce
+        // whichever operand is transposed
+        for (int i = threadIdx.x; i < SBT * SKT; i += 256) {
+            const int mm = ak ? i / SKT : i % SBT, kk = ak ? i % SKT : i / SBT;
             const int gm = m0 + mm, gk = k0 + kk;
             As[kk][mm] = (gm < M && gk < K) ? ldf(A + gm * sam + gk * sak) : 0.f;
-            const int nn = i % SB, kb = i / SB;
+            const int nn = bn ? i % SBT : i / SKT, kb = bn ? i / SBT : i % SKT;
             const int gn = n0 + nn, gk2 = k0 + kb;
             Bs[kb][nn] = (gn < N && gk2 < K) ? ldf(B + gk2 * sbk + gn * sbn) : 0.f;
         }
         __syncthreads();
 #pragma unroll
-        for (int kk = 0; kk < SK; ++kk) {
-            float a[4], b[4];
+        for (int kk = 0; kk < SKT; ++kk) {
+            float a[RT], b[RT];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i], b[i] = Bs[kk][tx * 4 + i];
+            for (int i = 0; i < RT; ++i) a[i] = As[kk][ty * RT + i], b[i] = Bs[kk][tx * RT + i];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < RT; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < RT; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int gm = m0 + ty * 4 + i;
+    for (int i = 0; i < RT; ++i) {
+        const int gm = m0 + ty * RT + i;
         if (gm >= M) continue;
         const bool zero = MODE == 1 && labels != nullptr && labels[gm] == ignore;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int gn = n0 + tx * 4 + j;
+        for (int j = 0; j < RT; ++j) {
+            const int gn = n0 + tx * RT + j;
             if (gn >= N) continue;
             const int64_t o = static_cast<int64_t>(gm) * ldo + gn;
             if (MODE == 0) outf[o] = acc[i][j];
@@ -549,10 +557,17 @@ template <typename TA, typename TB, typename TO, int MODE>
 int simt(int M, int N, int K, const TA* A, int64_t sam, int64_t sak, const TB* B, int64_t sbk, int64_t sbn,
          float* outf, TO* outT, int64_t ldo, const int64_t* labels, int64_t ignore, cudaStream_t st) {
     if (M == 0 || N == 0) return LIGER_OK;
+    const int64_t tiles64 = ceil_div(N, SB) * ceil_div(M, SB);
+    if (tiles64 < sm_count()) {   // too few 64-wide tiles to fill the GPU: 32-wide ones
+        dim3 grid(static_cast<unsigned>(ceil_div(N, SB / 2)), static_cast<unsigned>(ceil_div(M, SB / 2)));
+        simt_gemm<TA, TB, TO, MODE, SB / 2, 4 * SK><<<grid, 256, 0, st>>>(M, N, K, A, sam, sak, B, sbk, sbn, outf, outT, ldo,
+                                                                  labels, ignore);
+        return check_launch("simt_gemm");
+    }
     dim3 grid(static_cast<unsigned>(ceil_div(N, SB)), static_cast<unsigned>(ceil_div(M, SB)));
     if (grid.y > 65535) return fail(LIGER_ERR_SHAPE, "linear_ce: SIMT grid too large");
-    simt_gemm<TA, TB, TO, MODE><<<grid, 256, 0, st>>>(M, N, K, A, sam, sak, B, sbk, sbn, outf, outT, ldo, labels,
-                                                      ignore);
+    simt_gemm<TA, TB, TO, MODE, SB, SK><<<grid, 256, 0, st>>>(M, N, K, A, sam, sak, B, sbk, sbn, outf, outT, ldo, labels,
+                                                          ignore);
     return check_launch("simt_gemm");
 }
 
