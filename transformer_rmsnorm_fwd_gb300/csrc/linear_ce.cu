@@ -1071,6 +1071,19 @@ struct CommonLayout {
     size_t lse, lossrow, hdr, labs, total;
 };
 
+// A pinned host copy of the header for this thread (allocated on first use, kept for
+// the thread's lifetime; pinned memory is visible to every device's context).
+int pinned_hdr(Hdr** out) {
+    thread_local Hdr* buf = nullptr;
+    if (buf == nullptr) {
+        void* p = nullptr;
+        if (cudaMallocHost(&p, sizeof(Hdr)) != cudaSuccess) return check_launch("linear_ce pinned header");
+        buf = static_cast<Hdr*>(p);
+    }
+    *out = buf;
+    return LIGER_OK;
+}
+
 // Shared tail of both entry points: pointer and workspace checks, the label
 // scan (bad labels -> LIGER_ERR_LABEL before any other work), the all-ignored
 // case, the gradient scale, the variant's GEMMs, the final loss.
@@ -1110,9 +1123,14 @@ int ce_entry(const char* who, const void* X, const void* W, const int64_t* label
         const int grid = static_cast<int>(std::min<int64_t>(ceil_div(T, 256), 4 * sm_count()));
         label_scan<<<grid, 256, 0, st>>>(labels, T, V, ignore_index, hdr, nullptr);
         if (int rc = check_launch("label_scan")) return rc;
-        if (cudaMemcpyAsync(&h, hdr, sizeof(Hdr), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        // read through a pinned buffer of this thread: a copy into pageable memory takes the
+        // driver's staging path, which can wait behind other copies in flight
+        Hdr* hp = nullptr;
+        if (int rc = pinned_hdr(&hp)) return rc;
+        if (cudaMemcpyAsync(hp, hdr, sizeof(Hdr), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
             cudaStreamSynchronize(st) != cudaSuccess)
             return check_launch("linear_ce label scan");
+        h = *hp;
         if (h.bad) return fail(LIGER_ERR_LABEL, "%s: a label is outside [0, %lld) and is not %lld", who,
                                (long long)V, (long long)ignore_index);
     }
