@@ -215,8 +215,9 @@ def test_linear_ce_llama3_full_size_sampled(cuda_lib):
 def test_linear_ce_qwen_chain_seq32768(cuda_lib):
     """The benchmark's own linear-CE call: the Qwen-7B head of the chain at seq
     32768 (hidden 4096, vocab 151936, 10 % ignored), auto chunk (4 chunks of
-    8192 tokens): the mean loss and the lse of every 64th token against the
-    oracle's full forward (cached in tests/golden), dX on sampled rows, and the
+    8192 tokens of the 29491 that are not ignored): the mean loss and the lse of
+    every token against the oracle's full forward (cached in tests/golden), 16 or
+    more rows of dW against the oracle given that lse, dX on sampled rows, and the
     properties that hold at any size."""
     import torch
     c = workloads.qwen_chain(32768)["linear_ce"]

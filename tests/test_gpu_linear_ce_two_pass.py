@@ -122,11 +122,13 @@ def test_linear_ce_two_pass_all_ignored_and_errors(cuda_lib):
 
 def test_linear_ce_two_pass_qwen7b_seq32768_sampled(cuda_lib):
     """The Qwen-7B head of the benchmark's chain (seq 32768, hidden 4096, vocab
-    151936, 10 % ignored), auto vocabulary chunk: the mean loss and the lse of
-    every 64th token against the oracle's full forward (cached in tests/golden),
-    oracle on sampled rows (lse, loss term, dX row); the loss is the mean of the
-    row terms and close to its Gaussian-logit value; dW rows sum to ~0 over the
-    vocabulary; ignored rows exact zeros."""
+    151936, 10 % ignored, so the ignored tokens are dropped before both passes),
+    auto vocabulary chunk: the mean loss and the lse of every token against the
+    oracle's full forward (cached in tests/golden); 16 or more rows of dW (labels
+    of tokens across the sequence, random rows, the first and last) against the
+    oracle given that lse; the oracle on sampled rows (lse, loss term, dX row); the
+    loss is the mean of the row terms and close to its Gaussian-logit value; dW
+    rows sum to ~0 over the vocabulary; ignored rows exact zeros."""
     from datagen import workloads
     c = workloads.qwen_chain(32768)["linear_ce"]
     X, W, lab = c.make("X"), c.make("W"), c.make("labels")
@@ -139,6 +141,15 @@ def test_linear_ce_two_pass_qwen7b_seq32768_sampled(cuda_lib):
     keep = lab[::st] != -100
     assert np.max(np.abs(lse[::st][keep] - olse[keep]) / np.abs(olse[keep])) <= 1e-5
     assert abs(loss - g["loss_mean"]) <= LOSS_TOL_BF16 * abs(g["loss_mean"])
+    if st == 1:
+        # rows of dW (each finished in one pass over all valid tokens of its vocabulary chunk)
+        lab_rows = [int(lab[t]) for t in (3, 8200, 16390, 32760) if lab[t] >= 0]
+        vrows = np.unique(np.concatenate([lab_rows, np.random.default_rng(7).choice(V, 14, replace=False),
+                                          [0, V - 1]]))
+        assert len(vrows) >= 16
+        odW = oracle.linear_ce_dw_rows(X, W, lab, olse, vrows)
+        import torch
+        assert oracle.rel_err(host(dW[torch.as_tensor(vrows, device="cuda")]), odW) <= 2e-2
     n_valid = int((lab != -100).sum())
     assert abs(loss - lrow.sum() / n_valid) <= 1e-5 * abs(loss)
     rows = np.array([0, 8191, 8192, 32767])
