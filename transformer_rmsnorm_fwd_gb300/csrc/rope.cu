@@ -258,9 +258,15 @@ __global__ void __launch_bounds__(kThreads) rope_staged_kernel(const RopeArgs a,
     }
     const int nslot = H * vph;
     const int ntask = nslot * np;
+    // task t = (token pp, head h, vector v): pp and the slot advance with the thread's
+    // stride instead of being divided out of t, and h, v come from a shift and a mask when
+    // vph is a power of two (every power-of-two head size)
+    const bool vpow2 = (vph & (vph - 1)) == 0;
+    const int vsh = __ffs(vph) - 1;
+    int pp = static_cast<int>(threadIdx.x) / nslot, slot = static_cast<int>(threadIdx.x) - pp * nslot;
     for (int t = threadIdx.x; t < ntask; t += kThreads) {
-        const int pp = t / nslot, slot = t - pp * nslot;
-        const int h = slot / vph, v = slot - h * vph;
+        const int h = vpow2 ? slot >> vsh : slot / vph;
+        const int v = vpow2 ? slot & (vph - 1) : slot - h * vph;
         const int64_t bs = b * S + s0 + pp;
         T* dst = h < Hq ? q + bs * a.q_ts + static_cast<int64_t>(h) * D : k + bs * a.k_ts + static_cast<int64_t>(h - Hq) * D;
         const uint8_t* src = tile + static_cast<size_t>(pp) * rowb + static_cast<size_t>(h * D) * sizeof(T);
@@ -289,6 +295,11 @@ __global__ void __launch_bounds__(kThreads) rope_staged_kernel(const RopeArgs a,
             }
             stg16(dst + v * EPV, pack(av));
             stg16(dst + half + v * EPV, pack(bv));
+        }
+        slot += kThreads;
+        while (slot >= nslot) {
+            slot -= nslot;
+            ++pp;
         }
     }
 }
