@@ -60,7 +60,7 @@ def parse_args(argv=None):
     p.add_argument("--no-configs", action="store_true", help="skip the per-workload entries (configs)")
     p.add_argument("--op", default="chain",
                    choices=["chain", "linear_ce", "linear_ce_two_pass", "rmsnorm_qkv_rope", "fused_linear_swiglu",
-                            "rmsnorm", "rope", "swiglu"],
+                            "fused_linear_swiglu_bwd_saved", "rmsnorm", "rope", "swiglu"],
                    help="chain: the benchmark step (default); otherwise time that one operator alone at --seq "
                         "tokens (single-kernel profiling cases; prints a JSON line with ms per call)")
     p.add_argument("--chunk", type=int, default=0, help="--op linear_ce: token chunk (0 = automatic)")
@@ -1133,8 +1133,18 @@ def single_op(args):
         Wg = to_torch(normal(7, "op.Wg", (INTER, HIDDEN), "bf16", 0.0, 0.02), dev)
         Wu = to_torch(normal(7, "op.Wu", (INTER, HIDDEN), "bf16", 0.0, 0.02), dev)
         out = torch.empty(S, INTER, dtype=bf, device=dev)
-        fn = lambda: L.liger_fused_linear_swiglu_fwd(X, Wg, Wu, out)
-        flops = 4.0 * S * HIDDEN * INTER
+        if op == "fused_linear_swiglu":
+            fn = lambda: L.liger_fused_linear_swiglu_fwd(X, Wg, Wu, out)
+            flops = 4.0 * S * HIDDEN * INTER
+        else:
+            # the backward from the g, u of the saving forward: dG, dU, then dX and dW_g, dW_u
+            g, u = torch.empty_like(out), torch.empty_like(out)
+            L.liger_fused_linear_swiglu_fwd_save(X, Wg, Wu, out, g, u)
+            dH = to_torch(normal(7, "op.mdH", (S, INTER), "bf16"), dev)
+            dX, dWg, dWu = torch.empty_like(X), torch.empty_like(Wg), torch.empty_like(Wu)
+            ws = torch.empty(L.liger_fused_linear_swiglu_workspace(S, INTER), dtype=torch.uint8, device=dev)
+            fn = lambda: L.liger_fused_linear_swiglu_bwd_saved(X, Wg, Wu, dH, g, u, dX, dWg, dWu, ws)
+            flops = 8.0 * S * HIDDEN * INTER
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
