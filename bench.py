@@ -64,6 +64,8 @@ def parse_args(argv=None):
                    help="chain: the benchmark step (default); otherwise time that one operator alone at --seq "
                         "tokens (single-kernel profiling cases; prints a JSON line with ms per call)")
     p.add_argument("--chunk", type=int, default=0, help="--op linear_ce: token chunk (0 = automatic)")
+    p.add_argument("--ignore-frac", type=float, default=0.1,
+                   help="--op linear_ce / linear_ce_two_pass: fraction of labels set to ignore_index")
     return p.parse_args(argv)
 
 
@@ -1068,7 +1070,7 @@ def single_op(args):
     if op in ("linear_ce", "linear_ce_two_pass"):
         X = to_torch(normal(7, "op.X", (S, HIDDEN), "bf16"), dev)
         W = to_torch(normal(7, "op.W", (VOCAB, HIDDEN), "bf16", 0.0, 0.02), dev)
-        lab = torch.from_numpy(labels(7, "op.labels", S, VOCAB, 0.1)).to(dev)
+        lab = torch.from_numpy(labels(7, "op.labels", S, VOCAB, args.ignore_frac)).to(dev)
         loss = torch.empty(1, dtype=torch.float32, device=dev)
         dX, dW = torch.empty_like(X), torch.empty_like(W)
         if op == "linear_ce":
