@@ -509,10 +509,12 @@ __device__ __forceinline__ uint32_t word(const uint4& u, int e) {
 
 // Staged backward, two rows per block barrier: the block reduces the dot
 // products of its rows i and i + 1 together (two independent shuffle trees,
-// one barrier), then reads both rows again from shared memory for dx and dw,
-// so no row is held in registers across the barrier.  After the barrier of
-// rows (i, i + 1) every thread is past rows (i - 2, i - 1), whose buffers
-// thread 0 refills with rows i - 2 + nst and i - 1 + nst (nst >= 4).  Each
+// one barrier), then reads both rows again from shared memory for dx (and, in
+// fp32, dw), so no row is held in registers across the barrier.  After the
+// barrier of rows (i, i + 1) every thread is past rows (i - 2, i - 1), whose
+// buffers thread 0 refills with rows i - 2 + nst and i - 1 + nst (a ring of
+// nst = kBwdRing = 4 buffers, a compile-time constant so that slot and phase
+// are masks and shifts rather than divisions).  Each
 // block takes a contiguous group of rows (rows interleaved across blocks
 // measured no faster).
 // In bf16 the products are formed from the packed words by the mixed-precision
