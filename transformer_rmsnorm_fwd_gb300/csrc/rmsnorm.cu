@@ -13,7 +13,7 @@
 //    block barrier.  Other widths: the row held in registers (warp per row)
 //    or a block per row.
 //  * backward (the same rows): a persistent block per contiguous group of
-//    rows, its (dy, x) rows brought into a ring of 4 buffers by bulk copies;
+//    rows, its (dy, x) rows brought into a ring of 6 buffers by bulk copies;
 //    each thread owns fixed 16-byte column vectors and keeps its share of dw
 //    in fp32 registers across the group's rows (no atomics); the dot products
 //    of two rows are reduced together (shuffles, one block barrier), then the
@@ -475,7 +475,11 @@ int launch_fwd(const void* x, const void* w, void* y, float* rstd, int64_t rows,
 }
 
 constexpr int kBwdStagedMaxThreads = 256;
-constexpr int kBwdRing = 4;   // (dy, x) row buffers of a staged backward block: two in use, two in flight
+// (dy, x) row buffers of a staged backward block: two in use, four in flight (with rows of
+// at most 8 KB the ring takes at most 96 KB, two blocks per SM; measured faster at the
+// power-capped clock of a long step than a ring of 4 with three blocks per SM)
+constexpr int kBwdRing = 6;
+constexpr size_t kBwdStagedSmemMax = 100u * 1024u;
 
 // Row r of dy and x into ring buffer s (one mbarrier per buffer).
 template <typename T>
@@ -513,7 +517,7 @@ __device__ __forceinline__ uint32_t word(const uint4& u, int e) {
 // fp32, dw), so no row is held in registers across the barrier.  After the
 // barrier of rows (i, i + 1) every thread is past rows (i - 2, i - 1), whose
 // buffers thread 0 refills with rows i - 2 + nst and i - 1 + nst (a ring of
-// nst = kBwdRing = 4 buffers, a compile-time constant so that slot and phase
+// nst = kBwdRing = 6 buffers, a compile-time constant so that slot and phase
 // are masks and shifts rather than divisions).  Each
 // block takes a contiguous group of rows (rows interleaved across blocks
 // measured no faster).
@@ -747,10 +751,9 @@ int launch_bwd(const void* dy, const void* x, const void* w, const float* rstd, 
     T* dxp = static_cast<T*>(dx);
     bool done = false;
     const int rbytes = cols * static_cast<int>(sizeof(T));
-    if (cols % EPV == 0 && cols / EPV <= 2 * kBwdStagedMaxThreads && bwd_staged_smem(rbytes, kBwdRing) <= 100u * 1024u) {
-        // staged path: up to 4 rows in flight per block, about 3 blocks per SM at 8 KB rows
+    if (cols % EPV == 0 && cols / EPV <= 2 * kBwdStagedMaxThreads && bwd_staged_smem(rbytes, kBwdRing) <= kBwdStagedSmemMax) {
+        // staged path: a ring of kBwdRing (dy, x) row pairs, two rows in use, the rest in flight
         const int nvec = cols / EPV;
-        // a ring of kBwdRing (dy, x) row pairs: two rows in use, two in flight
         const size_t ssm = bwd_staged_smem(rbytes, kBwdRing);
         auto go = [&](auto kern, int vpt) -> int {
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm)) !=
