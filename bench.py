@@ -60,7 +60,8 @@ def parse_args(argv=None):
     p.add_argument("--no-configs", action="store_true", help="skip the per-workload entries (configs)")
     p.add_argument("--op", default="chain",
                    choices=["chain", "linear_ce", "linear_ce_two_pass", "rmsnorm_qkv_rope", "fused_linear_swiglu",
-                            "fused_linear_swiglu_bwd_saved", "rmsnorm", "rope", "swiglu"],
+                            "fused_linear_swiglu_fwd_save", "fused_linear_swiglu_bwd_saved", "rmsnorm", "rope",
+                            "swiglu"],
                    help="chain: the benchmark step (default); otherwise time that one operator alone at --seq "
                         "tokens (single-kernel profiling cases; prints a JSON line with ms per call)")
     p.add_argument("--chunk", type=int, default=0, help="--op linear_ce: token chunk (0 = automatic)")
@@ -1137,6 +1138,10 @@ def single_op(args):
         out = torch.empty(S, INTER, dtype=bf, device=dev)
         if op == "fused_linear_swiglu":
             fn = lambda: L.liger_fused_linear_swiglu_fwd(X, Wg, Wu, out)
+            flops = 4.0 * S * HIDDEN * INTER
+        elif op == "fused_linear_swiglu_fwd_save":
+            g, u = torch.empty_like(out), torch.empty_like(out)
+            fn = lambda: L.liger_fused_linear_swiglu_fwd_save(X, Wg, Wu, out, g, u)
             flops = 4.0 * S * HIDDEN * INTER
         else:
             # the backward from the g, u of the saving forward: dG, dU, then dX and dW_g, dW_u
